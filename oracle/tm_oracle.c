@@ -1,0 +1,202 @@
+/*
+ * tm_oracle.c -- plain, slow, single-threaded CPU oracle for the tiled fp32 maps.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library includes, links
+ * or calls this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg load it.  It shares no code, header, table or helper with
+ * the CUDA path.
+ *
+ * Build: gcc -O2 -std=c11 -fno-fast-math -ffp-contract=off -fPIC -shared
+ * (no FTZ, no contraction: every float operation rounds once, as written).
+ *
+ * Sources (cited by page title and section):
+ *   [AL]  Phobos docs, "@aligned" -- "A minimal kernel", "When the promise is broken".
+ *   [PZ]  Mojo GPU puzzles, "Aligned Load & Store" -- "The exercise", "Solution".
+ *   [SB]  Phobos docs, "Slicing, bounds and masking" -- "Masking",
+ *         "Loops over a dynamic extent", "Promising whole tiles with @aligned",
+ *         "Reductions over a ragged tile".
+ *   [MC]  teenygrad, "Memory Coalescing and Tensor Layout" -- "What it actually
+ *         costs", "Strides, and reading an index expression".
+ *
+ * Layout convention everywhere: row-major [M, N] with an explicit leading
+ * dimension ld >= N (element (i, j) lives at i*ld + j), per [MC] "The alignment
+ * constraint": use the passed row stride, never the shape's last extent.
+ *
+ * Parity status: every function here is pinned by the CPU test suite (closed
+ * forms, the pages' printed examples, brute force, library routines); none is
+ * "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Tile walk over a runtime extent.                                          */
+/* [SB] "Loops over a dynamic extent": a loop `for kt in range(0, K, T)` over  */
+/* a runtime extent is split into whole tiles, which need no mask, and one     */
+/* masked iteration over the remainder.  Written as the walk itself: visit     */
+/* kt = 0, T, 2T, ... < K and classify each visit.                             */
+/* out[0] = whole (unmasked) iterations, out[1] = masked iterations (0 or 1),  */
+/* out[2] = columns covered by the masked iteration, out[3] = all iterations.  */
+/* Returns -1 for T <= 0 or K < 0 ([AL]: a tile divisor must be positive).     */
+/* ------------------------------------------------------------------------ */
+int oracle_tile_walk(int64_t K, int64_t T, int64_t out[4])
+{
+    int64_t kt, whole = 0, masked = 0, rem = 0, iters = 0;
+    if (T <= 0 || K < 0)
+        return -1;
+    for (kt = 0; kt < K; kt += T) {
+        if (kt + T <= K) {
+            whole += 1;
+        } else {
+            masked += 1;
+            rem = K - kt;
+        }
+        iters += 1;
+    }
+    out[0] = whole;
+    out[1] = masked;
+    out[2] = rem;
+    out[3] = iters;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* In-bounds elements of tile (pm, pn) in a TM x TN tiling of [M, N].         */
+/* [SB] "Masking": a slice X[pm*TM :+ TM, pn*TN :+ TN] may run past the end;  */
+/* elements past the end are masked.  Counted element by element.             */
+/* ------------------------------------------------------------------------ */
+int64_t oracle_tile_valid(int64_t M, int64_t N, int64_t TM, int64_t TN,
+                          int64_t pm, int64_t pn)
+{
+    int64_t r, c, valid = 0;
+    for (r = 0; r < TM; ++r)
+        for (c = 0; c < TN; ++c) {
+            int64_t i = pm * TM + r, j = pn * TN + c;
+            if (i < M && j < N)
+                valid += 1;
+        }
+    return valid;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The @aligned promise.  [AL] "When the promise is broken" and [SB]          */
+/* "Promising whole tiles with @aligned": the host promises that M and N are  */
+/* whole numbers of tiles.  Returns 1 when the promise holds, 0 when broken,  */
+/* -1 when a tile is not positive.                                            */
+/* ------------------------------------------------------------------------ */
+int oracle_promise_kept(int64_t M, int64_t N, int64_t TM, int64_t TN)
+{
+    if (TM <= 0 || TN <= 0)
+        return -1;
+    return (M % TM == 0 && N % TN == 0) ? 1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a1: the memory-bound map of [PZ] "The exercise": out[i] = a[i]*SCALE+BIAS  */
+/* with SCALE = 2 and BIAS = 1, over every one of the n elements.  The three  */
+/* kernels of the puzzle differ only in memory access and give identical      */
+/* output, so one definition covers them all.                                 */
+/* ------------------------------------------------------------------------ */
+void oracle_affine(const float *a, float *out, int64_t n)
+{
+    const float SCALE = 2.0f, BIAS = 1.0f;
+    int64_t i;
+    for (i = 0; i < n; ++i) {
+        float v = a[i] * SCALE;   /* rounds once (exact: power-of-two scale) */
+        out[i] = v + BIAS;        /* rounds once */
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a2: Y = alpha * X of [AL] "A minimal kernel" (kernel `scale`), restricted  */
+/* to the in-bounds elements of [M, N]: [SB] "Masking" skips every store past */
+/* the end, so words in the ld gap (j >= N) and past row M are never written. */
+/* ------------------------------------------------------------------------ */
+void oracle_scale2d(const float *X, int64_t ldx, float *Y, int64_t ldy,
+                    int64_t M, int64_t N, float alpha)
+{
+    int64_t i, j;
+    for (i = 0; i < M; ++i)
+        for (j = 0; j < N; ++j)
+            Y[i * ldy + j] = alpha * X[i * ldx + j];
+}
+
+/* ------------------------------------------------------------------------ */
+/* a3: B = A of [SB] "Promising whole tiles with @aligned" (kernel copy2d),  */
+/* in-bounds only, as raw 32-bit words so NaN payloads survive bit for bit.   */
+/* ------------------------------------------------------------------------ */
+void oracle_copy2d(const uint32_t *A, int64_t lda, uint32_t *B, int64_t ldb,
+                   int64_t M, int64_t N)
+{
+    int64_t i, j;
+    for (i = 0; i < M; ++i)
+        for (j = 0; j < N; ++j)
+            B[i * ldb + j] = A[i * lda + j];
+}
+
+/* ------------------------------------------------------------------------ */
+/* a5: per-row sums of a row-major matrix -- the stride-1 walk of [MC] "What  */
+/* it actually costs" (the page fixes the access order, not the arithmetic;   */
+/* the reading is a sum).  Accumulated in fp64: r[i] = sum_j X[i, j].         */
+/* ------------------------------------------------------------------------ */
+void oracle_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N, double *r)
+{
+    int64_t i, j;
+    for (i = 0; i < M; ++i) {
+        double s = 0.0;
+        for (j = 0; j < N; ++j)
+            s += (double)X[i * ldx + j];
+        r[i] = s;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* a6: per-column sums -- the stride-COLS walk of [MC] "What it actually      */
+/* costs", same bytes, same arithmetic: c[j] = sum_i X[i, j] in fp64, rows    */
+/* added in ascending order.                                                  */
+/* ------------------------------------------------------------------------ */
+void oracle_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, double *c)
+{
+    int64_t i, j;
+    for (j = 0; j < N; ++j)
+        c[j] = 0.0;
+    for (i = 0; i < M; ++i)
+        for (j = 0; j < N; ++j)
+            c[j] += (double)X[i * ldx + j];
+}
+
+/* ------------------------------------------------------------------------ */
+/* a8: masked row-max over ragged column tiles, following [SB] "Reductions    */
+/* over a ragged tile" step by step for each row i:                            */
+/*   for kt in range(0, N, BC):                                               */
+/*     s[c] = S[i, kt + c] when kt + c < N, else 0  (a masked load reads 0,   */
+/*            [SB] "Masking")                                                 */
+/*     fill_mode 0: s[c] = (c < N - kt) ? s[c] : -inf  (the where/iota mask;  */
+/*            -inf is the value no real score reaches)                        */
+/*     fill_mode 1: no where step -- the zero-fill pitfall the page warns of  */
+/*     m = max(m, max_c s[c])                                                 */
+/* m starts at -inf, the identity of max, so N = 0 gives -inf.  max follows   */
+/* C's fmaxf: a NaN operand is ignored unless both are NaN.                   */
+/* Returns -1 for BC <= 0 or an unknown fill_mode.                            */
+/* ------------------------------------------------------------------------ */
+int oracle_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N,
+                         int64_t BC, int fill_mode, float *m)
+{
+    int64_t i, kt, c;
+    if (BC <= 0 || (fill_mode != 0 && fill_mode != 1))
+        return -1;
+    for (i = 0; i < M; ++i) {
+        float mi = -INFINITY;
+        for (kt = 0; kt < N; kt += BC) {
+            for (c = 0; c < BC; ++c) {
+                float s = (kt + c < N) ? S[i * lds + kt + c] : 0.0f;
+                if (fill_mode == 0)
+                    s = (c < N - kt) ? s : -INFINITY;
+                mi = fmaxf(mi, s);
+            }
+        }
+        m[i] = mi;
+    }
+    return 0;
+}
