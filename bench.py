@@ -1,7 +1,527 @@
-"""Benchmark of the tiled fp32 maps on one GB300 (filled in with the kernels)."""
+"""Benchmark of the tiled fp32 maps on GB300.
+
+One step is one pass of the whole hot path over one batch: the fp32
+[8192, 8192] matrix X ~ N(0,1) (seed 1) of the aligned 2-D scale workload
+("@aligned", "A minimal kernel": TM = 32, TN = 128), fed through every kernel:
+
+  affine      out = X*2 + 1 over all 67,108,864 elements (1-D, widest vectors)
+  scale2d     Y = 1.5*X, 32 x 128 tiles, aligned promise
+  copy2d      B = X, 64 x 64 tiles, aligned promise
+  rowsum      r = sum over each row (8 rows per block, 512-column tiles)
+  colsum      c = sum over each column (32 x 128 strips, AUTO = TMA-staged)
+  rowmax      m = ragged row max, 64-column tiles, -inf fill
+
+Metric: achieved HBM GB/s (GB = 1e9 bytes, the pages' convention) over the
+algorithmic bytes (each input byte read once, each output byte written once),
+and its fraction of the measured HBM peak.  Inputs are larger than L2 (256 MiB
+vs 126 MB), so no flush runs between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 HBM roofline per kernel (1 GPU)"
+WORKLOAD = "scale_8192"
+M = N = 8192
+ALPHA = 1.5
+FALLBACK_HBM_GBS = 6800.0
+STEP_LAUNCHES = 7  # affine, scale2d, copy2d, rowsum, colsum (partials + finish), rowmax
 
 
 def gbps(nbytes: int, seconds: float) -> float:
     """Bandwidth in GB/s with GB = 1e9 bytes (the pages' convention: their
     "64 MB" read in 111.6 us is quoted as 601 GB/s, i.e. 2^26 bytes / 1e9)."""
     return nbytes / seconds / 1e9
+
+
+def kernel_bytes(M: int, N: int) -> dict:
+    """Algorithmic bytes of each kernel of one step over an [M, N] fp32 batch."""
+    e = M * N
+    return {
+        "affine": 8 * e,
+        "scale2d": 8 * e,
+        "copy2d": 8 * e,
+        "rowsum": 4 * e + 4 * M,
+        "colsum": 4 * e + 4 * N,
+        "rowmax_masked": 4 * e + 4 * M,
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs: torch copy of 1 Gi bf16, read+write)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, an earlier GB300 measurement)"
+
+
+def aggregate(elapsed_s: float, nbytes: int, world: int):
+    """Max of the ranks' elapsed times and sum of their bytes (torch.distributed
+    when world > 1; the process group must be initialised)."""
+    if world <= 1:
+        return elapsed_s, nbytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64)
+    b = torch.tensor([float(nbytes)], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t, b = t.cuda(), b.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1 + 0.25]
+        rows = inside or [r for (_, r) in self.rows]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows if len(r) >= 9 for k in range(4) if r[5 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------------- traffic
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken
+    on the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "masking_tm_affine_gb300", "csrc", ent["source"])
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if digest != ent.get("source_sha256_16"):
+        return None
+    return ent.get("dram_bytes_per_launch_full")
+
+
+# --------------------------------------------------------------------- GPU arm
+def make_step(tm, bufs, ws_bytes, stream):
+    """The hot path over one batch, as (name, launch) pairs on `stream`."""
+    X, A1, Y, B, r, c, m, W = (bufs[k] for k in ("X", "A1", "Y", "B", "r", "c", "m", "W"))
+    s = stream.cuda_stream
+    return [
+        ("affine", lambda: tm.tm_affine(X, A1, M * N, tm.TM_VAR_AUTO, s)),
+        ("scale2d", lambda: tm.tm_scale2d(X, N, Y, N, M, N, ALPHA, 32, 128, tm.TM_ALIGNED, s)),
+        ("copy2d", lambda: tm.tm_copy2d(X, N, B, N, M, N, 64, 64, tm.TM_ALIGNED, s)),
+        ("rowsum", lambda: tm.tm_rowsum(X, N, M, N, r, 8, 512, tm.TM_ALIGNED, s)),
+        ("colsum", lambda: tm.tm_colsum(X, N, M, N, c, W, ws_bytes, 32, 128, tm.TM_VAR_AUTO, tm.TM_ALIGNED, s)),
+        ("rowmax_masked", lambda: tm.tm_rowmax_masked(X, N, M, N, m, 8, 64, tm.TM_FILL_NEG_INF, tm.TM_ALIGNED, s)),
+    ]
+
+
+def verify_step(bufs, x, oracle):
+    """Sampled parity at full size (the oracle computes the sampled outputs one
+    by one): 64 rows of every output, and every column sum."""
+    import numpy as np
+    rows = np.linspace(0, M - 1, 64).astype(np.int64)
+    xs = x[rows]
+    A1 = bufs["A1"].view(M, N)[rows].cpu().numpy()
+    Y = bufs["Y"].view(M, N)[rows].cpu().numpy()
+    B = bufs["B"].view(M, N)[rows].cpu().numpy()
+    assert np.array_equal(A1.view(np.uint32), oracle.affine(xs).reshape(xs.shape).view(np.uint32)), "affine"
+    want = np.zeros_like(xs)
+    oracle.scale2d(xs, N, want, N, len(rows), N, ALPHA)
+    assert np.array_equal(Y.view(np.uint32), want.view(np.uint32)), "scale2d"
+    assert np.array_equal(B.view(np.uint32), xs.view(np.uint32)), "copy2d"
+    r = bufs["r"].cpu().numpy()[rows]
+    rw = oracle.rowsum(xs, N, len(rows), N)
+    assert np.all(np.abs(r - rw) <= 1e-5 * oracle.rowsum(np.abs(xs), N, len(rows), N)), "rowsum"
+    c = bufs["c"].cpu().numpy()
+    cw = oracle.colsum(x, N, M, N)
+    assert np.all(np.abs(c - cw) <= 1e-5 * oracle.colsum(np.abs(x), N, M, N)), "colsum"
+    mm = bufs["m"].cpu().numpy()[rows]
+    assert np.array_equal(mm, oracle.rowmax_masked(xs, N, len(rows), N, 64)), "rowmax"
+
+
+def cpu_baseline(x, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands, one thread pinned to one core, over a bounded
+    sample: rows [0, 1024) of the batch, whole passes until ~budget_s."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    R = 1024
+    xs = np.ascontiguousarray(x[:R])
+    by = sum(kernel_bytes(R, N).values())
+    prev = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    if prev:
+        os.sched_setaffinity(0, {min(prev)})
+    try:
+        Yw = np.empty_like(xs)
+        Bw = np.empty(xs.size, dtype=np.uint32)
+
+        def one_pass():
+            oracle.affine(xs)
+            oracle.scale2d(xs, N, Yw, N, R, N, ALPHA)
+            oracle.copy2d(xs, N, Bw, N, R, N)
+            oracle.rowsum(xs, N, R, N)
+            oracle.colsum(xs, N, R, N)
+            oracle.rowmax_masked(xs, N, R, N, 64)
+
+        one_pass()  # warm-up
+        t0 = time.perf_counter()
+        passes = 0
+        while True:
+            one_pass()
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    finally:
+        if prev:
+            os.sched_setaffinity(0, prev)
+    return {"value": round(gbps(by * passes, el), 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "oracle step (all six maps) over rows [0,%d) of the [8192,8192] batch, %d passes in "
+                      "%.1f s, single thread pinned to one core of %d" % (R, passes, el, os.cpu_count())}
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from masking_tm_affine_gb300 import synth, tm
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tm.load()
+
+    x = synth.workload_input(WORKLOAD)
+    bufs = {
+        "X": torch.from_numpy(x.reshape(-1)).to(dev),
+        "A1": torch.empty(M * N, dtype=torch.float32, device=dev),
+        "Y": torch.empty(M * N, dtype=torch.float32, device=dev),
+        "B": torch.empty(M * N, dtype=torch.float32, device=dev),
+        "r": torch.empty(M, dtype=torch.float32, device=dev),
+        "c": torch.empty(N, dtype=torch.float32, device=dev),
+        "m": torch.empty(M, dtype=torch.float32, device=dev),
+    }
+    ws_bytes = tm.tm_colsum_workspace_bytes(M, N, 32, 128)
+    bufs["W"] = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    step = make_step(tm, bufs, ws_bytes, stream)
+    names = [n for n, _ in step]
+    kb = kernel_bytes(M, N)
+    step_bytes = sum(kb.values())
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            for _, fn in step:
+                fn()
+        tm.tm_check(stream.cuda_stream)
+    if rank == 0 and not args.no_verify:
+        import oracle
+        oracle.build()
+        verify_step(bufs, x, oracle)
+
+    # timed region: K steps, an event pair around every kernel launch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(step) + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.6)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            evs[k][0].record(stream)
+            for i, (_, fn) in enumerate(step):
+                fn()
+                evs[k][i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    tm.tm_check(stream.cuda_stream)
+
+    elapsed = evs[0][0].elapsed_time(evs[-1][-1]) * 1e-3
+    per_kernel_s = {n: sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)) * 1e-3 / args.steps
+                    for i, n in enumerate(names)}
+    t_max, total_bytes = aggregate(elapsed, step_bytes * args.steps, world)
+
+    # end to end through the C ABI: pinned host X in, every output back to pinned host memory
+    e2e = None
+    if rank == 0:
+        e2e = run_e2e(tm, bufs, x, step, stream, dev, min(args.steps, args.e2e_steps), step_bytes)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    peak, peak_src = measured_peak()
+    kernels = {}
+    for n in names:
+        t = per_kernel_s[n]
+        a = gbps(kb[n], t)
+        kernels[n] = {"bytes": kb[n], "us": round(t * 1e6, 2), "GBps": round(a, 1), "frac": round(a / peak, 4)}
+    dom = max(names, key=lambda n: per_kernel_s[n])
+    dom_ach = gbps(kb[dom], per_kernel_s[dom])
+    line = {
+        "metric": METRIC,
+        "value": round(gbps(total_bytes, t_max), 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic: numpy PCG64, X ~ N(0,1) seed 1, rounded once to fp32",
+        "config": {
+            "workload": "scale_8192: fp32 [8192,8192] X~N(0,1) seed 1; one step = affine(1-D, all elements) + "
+                        "scale2d(alpha 1.5, 32x128, aligned) + copy2d(64x64, aligned) + rowsum(8x512) + "
+                        "colsum(32x128, AUTO) + rowmax_masked(8x64, -inf fill)",
+            "M": M, "N": N, "step_bytes": step_bytes,
+            "l2": "inputs larger than L2 (X 256 MiB, each output 256 MiB vs 126 MB L2); no flush between steps",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(dom_ach, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(dom_ach / peak, 4),
+                     "traffic": recorded_traffic(dom), "peak_source": peak_src + ", of measured"
+                     if peak_src.startswith("measured") else peak_src},
+        "kernels": kernels,
+        "gpu_launches": STEP_LAUNCHES * args.steps,
+        "clocks": sampler.summary(wall0, wall1),
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(x)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes):
+    import torch
+    steps = max(steps, 3)
+    hx = torch.from_numpy(x.reshape(-1)).pin_memory()
+    outs = ["A1", "Y", "B", "r", "c", "m"]
+    host = {k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs}
+    h2d = hx.numel() * 4
+    d2h = sum(bufs[k].numel() * 4 for k in outs)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            bufs["X"].copy_(hx, non_blocking=True)
+            for _, fn in step:
+                fn()
+            for k in outs:
+                host[k].copy_(bufs[k], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            bufs["X"].copy_(hx, non_blocking=True)
+            for _, fn in step:
+                fn()
+            for k in outs:
+                host[k].copy_(bufs[k], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t = e0.elapsed_time(e1) * 1e-3
+    return {"value": round(gbps(step_bytes * steps, t), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3),
+            "path": "pinned host X -> device, six C-ABI calls, every output -> pinned host, one stream"}
+
+
+# --------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm: same metric and workload, each step
+    one pass over a row slice sized so the whole run stays within minutes."""
+    import numpy as np
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    from masking_tm_affine_gb300 import synth
+    oracle.build()
+    x = synth.workload_input(WORKLOAD)
+    prev = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    if prev:
+        os.sched_setaffinity(0, {min(prev)})
+
+    def one_pass(R):
+        xs = x[:R]
+        Yw = np.empty_like(xs)
+        Bw = np.empty(xs.size, dtype=np.uint32)
+        oracle.affine(xs)
+        oracle.scale2d(xs, N, Yw, N, R, N, ALPHA)
+        oracle.copy2d(xs, N, Bw, N, R, N)
+        oracle.rowsum(xs, N, R, N)
+        oracle.colsum(xs, N, R, N)
+        oracle.rowmax_masked(xs, N, R, N, 64)
+
+    t0 = time.perf_counter()
+    one_pass(64)
+    per_row = (time.perf_counter() - t0) / 64
+    budget = 90.0
+    R = int(max(1, min(M, budget / max(args.steps + args.warmup, 1) / per_row)))
+    for _ in range(args.warmup):
+        one_pass(R)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_pass(R)
+    el = time.perf_counter() - t0
+    if prev:
+        os.sched_setaffinity(0, prev)
+    by = sum(kernel_bytes(R, N).values()) * args.steps
+    v = round(gbps(by, el), 3)
+    sample = ("oracle step (all six maps) over rows [0,%d) of the [8192,8192] batch per step, single thread "
+              "pinned to one core of %d" % (R, os.cpu_count()))
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic: numpy PCG64, X ~ N(0,1) seed 1, rounded once to fp32",
+            "config": {"workload": "scale_8192 (row slice per step, see cpu_baseline.sample)", "M": R, "N": N},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------- size sweep
+def run_sweep(args):
+    """Y = 1.5*X over tensors of 2^10 .. 2^30 bytes (and the affine map over the
+    same sizes), median of CUDA-event times with L2 flushed between reps."""
+    import torch
+
+    from masking_tm_affine_gb300 import tm
+    tm.load()
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peak()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for lg in range(10, 31):
+        E = (1 << lg) // 4
+        if E >= 4096:
+            n = min(8192, E // 32)
+            shape, flags = (E // n, n), tm.TM_ALIGNED
+        else:
+            shape, flags = (1, E), 0
+        X = torch.randn(E, device=dev)
+        Y = torch.empty_like(X)
+        A1 = torch.empty_like(X)
+        res = {}
+        for name, fn in (("scale2d", lambda: tm.tm_scale2d(X, shape[1], Y, shape[1], shape[0], shape[1], ALPHA,
+                                                          32, 128, flags, stream.cuda_stream)),
+                         ("affine", lambda: tm.tm_affine(X, A1, E, tm.TM_VAR_AUTO, stream.cuda_stream))):
+            ts = []
+            for rep in range(args.sweep_reps + 3):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if rep >= 3:
+                    ts.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(ts)
+            res[name] = {"us": round(t * 1e6, 2), "GBps": round(gbps(8 * E, t), 1), "frac": round(gbps(8 * E, t) / peak, 4)}
+        out.append({"bytes_per_tensor": 1 << lg, "shape": list(shape), **res})
+        del X, Y, A1
+    tm.tm_check()
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true", help="print the 1 KB..1 GB size sweep instead")
+    ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-verify", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.sweep:
+        for row in run_sweep(args):
+            print(json.dumps(row))
+        return
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * tm.h -- C ABI of libtm: memory-bound tiled maps over fp32 tensors, each with
+ * a whole-tile fast path (unmasked 16/32-byte vector access, taken only under
+ * an explicit promise that the extents are whole numbers of tiles) and a
+ * ragged-edge path (out-of-bounds loads read 0, out-of-bounds stores are
+ * skipped).  Hand-written CUDA for sm_103a (GB300).
+ *
+ * Sources, cited by page title and section:
+ *   "@aligned" (Phobos docs): "A minimal kernel", "What it changes",
+ *       "When the promise is broken", "Interactions".
+ *   "Aligned Load & Store" (Mojo GPU puzzles, puzzle 35): "The exercise",
+ *       "Key API", "Tips", "Solution".
+ *   "Slicing, bounds and masking" (Phobos docs): "Subscript forms", "Masking",
+ *       "Loops over a dynamic extent", "Promising whole tiles with @aligned",
+ *       "Reductions over a ragged tile".
+ *   "Memory Coalescing and Tensor Layout" (teenygrad): "Coalescing",
+ *       "What it actually costs", "Seeing it in a real kernel", "Strides",
+ *       "Block pointers and descriptors", "The alignment constraint".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.   2-D tensors are row-major [M, N] fp32 with an explicit leading
+ *           dimension (row stride, in elements) ld >= N: element (i, j) is at
+ *           base[i*ld + j].  The stride is always the passed one, never N
+ *           ("Memory Coalescing and Tensor Layout", "The alignment constraint").
+ * Pointers. Every pointer (except `workspace` sizes and host-side out-params
+ *           of the probes, which say so) is a DEVICE pointer on the current
+ *           CUDA device.  The caller owns all memory; libtm allocates nothing
+ *           and keeps no pointer after the call returns.  Its only state is one
+ *           status word per device (see tm_check).
+ * Streams.  `stream` is a cudaStream_t passed as void*; NULL selects the legacy
+ *           default stream.  Every call is asynchronous on that stream: the
+ *           return value covers host-side validation and the launch itself.
+ * Errors.   No call prints, aborts or throws.  A call that returns anything but
+ *           TM_OK has launched nothing and written nothing.  A promise broken
+ *           on the device side is reported by the next tm_check, mirroring
+ *           "the next synchronize on the host fails" ("@aligned", "When the
+ *           promise is broken").
+ * Empty.    M == 0, N == 0 or n == 0 is legal.  Maps then do nothing; a
+ *           reduction still writes its outputs (sum of nothing = 0, max of
+ *           nothing = -inf).
+ * Overlap.  The maps may run in place (out == a; Y == X with ldy == ldx;
+ *           B == A with ldb == lda).  Any other overlap of inputs and outputs
+ *           is rejected with TM_ERR_INVALID_ARG.
+ * Tiles.    Tile extents must be positive ("@aligned": a divisor must be
+ *           positive) and one of the shapes each entry point lists (the
+ *           kernels are instantiated per shape); anything else returns
+ *           TM_ERR_UNSUPPORTED_TILE.
+ */
+#ifndef TM_H_
+#define TM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tm_status {
+    TM_OK = 0,
+    TM_ERR_INVALID_ARG = 1,      /* negative extent, ld < N, NULL pointer with work, bad overlap, unknown flag or variant */
+    TM_ERR_UNSUPPORTED_TILE = 2, /* tile not positive, or not an instantiated shape */
+    TM_ERR_MISALIGNED = 3,       /* a vector path or TM_ALIGNED with a pointer or ld that breaks 16-byte alignment */
+    TM_ERR_BROKEN_PROMISE = 4,   /* TM_ALIGNED while M % TM != 0 or N % TN != 0 */
+    TM_ERR_CUDA = 5,             /* a CUDA runtime call or kernel launch failed */
+    TM_ERR_WORKSPACE = 6,        /* colsum workspace NULL, too small or not 16-byte aligned */
+    TM_ERR_TIMEOUT = 7           /* a bounded device-side wait gave up (reported by tm_check) */
+} tm_status;
+
+/* A cudaStream_t, passed as an opaque pointer; NULL = legacy default stream. */
+typedef void *tm_stream_t;
+
+/* flags (bitwise OR) */
+/* The @aligned promise: M % TM == 0 and N % TN == 0 (and, implied by the
+ * 16-byte access it unlocks, every base pointer 16-byte aligned and every ld a
+ * multiple of 4).  Masks are dropped.  Checked on the host before launch
+ * (TM_ERR_MISALIGNED / TM_ERR_BROKEN_PROMISE, nothing launched) and once more
+ * at kernel entry ("@aligned", "When the promise is broken"; "Slicing, bounds
+ * and masking", "Promising whole tiles with @aligned"). */
+#define TM_ALIGNED 0x1u
+/* Path forcing, for tests and ablations; at most one may be set.  Without
+ * them the library picks the fastest path the arguments allow. */
+#define TM_PATH_SCALAR 0x10u /* per-element accesses with per-element masks */
+#define TM_PATH_VEC 0x20u    /* 16-byte register accesses (needs the vector alignment) */
+#define TM_PATH_TMA 0x40u    /* TMA tile copies through shared memory (needs 16-byte rows) */
+
+typedef enum tm_variant {
+    TM_VAR_AUTO = 0,
+    /* tm_affine ("Aligned Load & Store", "The exercise") */
+    TM_VAR_SCALAR = 1,        /* one element per thread, one 4-byte load and store */
+    TM_VAR_VEC_UNALIGNED = 2, /* 4 elements per thread through 4 scalar 4-byte loads and stores */
+    TM_VAR_VEC4 = 3,          /* 4 elements per access, one 16-byte load and store (needs 16-byte pointers) */
+    TM_VAR_VEC8 = 4,          /* 8 elements per access, one 32-byte load and store (needs 32-byte pointers) */
+    /* tm_colsum ("Memory Coalescing and Tensor Layout", "What it actually costs",
+     * "Seeing it in a real kernel") */
+    TM_VAR_NAIVE = 5,     /* the column walk: 256-lane programs over rows, stride ld between lanes */
+    TM_VAR_STAGED = 6,    /* TMA tiles staged in shared memory, columns reduced from there */
+    TM_VAR_REGDIRECT = 7  /* lanes over columns: coalesced row segments straight into registers */
+} tm_variant;
+
+typedef enum tm_fill {
+    TM_FILL_NEG_INF = 0, /* where(iota < N - kt, s, -inf): padding never wins the max */
+    TM_FILL_ZERO = 1     /* no where step: padding reads as 0 (the pitfall, kept as a foil) */
+} tm_fill;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *tm_status_string(tm_status st);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int tm_version(void);
+
+/*
+ * tm_affine -- out[i] = a[i]*2 + 1 for 0 <= i < n.
+ * "Aligned Load & Store", "The exercise" and "Solution": the same map through
+ * three access patterns.  Every variant writes every element (the puzzle's
+ * vector kernels skip the n % 4 tail; here a scalar tail finishes it) and all
+ * variants are bit-identical: 2a is exact, so the result is 2a + 1 rounded once.
+ *   a, out   device pointers to n floats (out == a allowed, no other overlap)
+ *   n        element count, >= 0
+ *   variant  TM_VAR_AUTO (widest access the alignment allows), _SCALAR,
+ *            _VEC_UNALIGNED, _VEC4 (a, out 16-byte aligned), _VEC8 (32-byte)
+ * Errors: INVALID_ARG (n < 0, NULL with n > 0, bad variant, partial overlap),
+ *         MISALIGNED (VEC4/VEC8 with misaligned pointers), CUDA.
+ */
+tm_status tm_affine(const float *a, float *out, int64_t n, tm_variant variant, tm_stream_t stream);
+
+/*
+ * tm_scale2d -- Y[i, j] = alpha * X[i, j] for i < M, j < N, one TM x TN tile
+ * per work unit.  "@aligned", "A minimal kernel" (kernel `scale`, TM = 32,
+ * TN = 128).  Words of Y outside [M, N] (the ld gap, past row M) are never
+ * written ("Slicing, bounds and masking", "Masking").
+ *   X, ldx   device input [M, ldx]     Y, ldy   device output [M, ldy]
+ *   TM, TN   tile: (8,8) (16,16) (32,32) (64,64) (32,128) (128,128)
+ *   flags    TM_ALIGNED and/or one TM_PATH_* bit
+ * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
+ */
+tm_status tm_scale2d(const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M, int64_t N,
+                     float alpha, int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream);
+
+/*
+ * tm_copy2d -- B[i, j] = A[i, j] bit for bit, for i < M, j < N.
+ * "Slicing, bounds and masking", "Promising whole tiles with @aligned"
+ * (kernel copy2d, TM = TN = 64).  Same tiles, flags, masking and errors as
+ * tm_scale2d.  NaN payloads are preserved.
+ */
+tm_status tm_copy2d(const float *A, int64_t lda, float *B, int64_t ldb, int64_t M, int64_t N,
+                    int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream);
+
+/*
+ * tm_rowsum -- r[i] = sum_j X[i, j] (fp32 accumulation), the stride-1 walk of
+ * "Memory Coalescing and Tensor Layout", "What it actually costs".  Each row
+ * is walked in TN-column tiles: the whole tiles unmasked, then one masked
+ * remainder tile whose missing columns read 0 ("Slicing, bounds and masking",
+ * "Loops over a dynamic extent").  One warp per row, TM rows per block.
+ *   X, ldx   device input [M, ldx]     r   device output, M floats
+ *   TM       rows per block: 1, 2, 4, 8, 16, 32
+ *   TN       columns per tile: 128, 256, 512, 1024
+ *   flags    TM_ALIGNED (no remainder tile and no row mask), TM_PATH_SCALAR, TM_PATH_VEC
+ * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
+ */
+tm_status tm_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *r, int32_t TM,
+                    int32_t TN, uint32_t flags, tm_stream_t stream);
+
+/*
+ * tm_colsum_workspace_bytes -- bytes of scratch tm_colsum needs for these
+ * arguments (a partial sum per column per row chunk).  0 for invalid
+ * arguments or when no scratch is needed (M == 0 or N == 0).
+ */
+size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, tm_variant variant);
+
+/*
+ * tm_colsum -- c[j] = sum_i X[i, j] (fp32 accumulation), the stride-COLS walk
+ * of "Memory Coalescing and Tensor Layout", "What it actually costs", and its
+ * fix from "Seeing it in a real kernel" (load a tile once into fast memory).
+ * Row chunks write partial sums to `workspace`; a second pass adds them in a
+ * fixed order, so the result is deterministic run to run.
+ *   X, ldx      device input [M, ldx]        c   device output, N floats
+ *   workspace   device scratch of >= tm_colsum_workspace_bytes(...) bytes,
+ *               16-byte aligned, owned by the caller; its contents on entry do
+ *               not matter and on exit are unspecified
+ *   TM, TN      row tile x column strip: TM in 8..256 (powers of two),
+ *               TN in 64, 128, 256; TM*TN <= 8192 for STAGED
+ *               (NAIVE ignores them: its programs are 256 rows x 1 column)
+ *   variant     TM_VAR_AUTO, _NAIVE, _STAGED, _REGDIRECT
+ *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR
+ * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE,
+ *         WORKSPACE, CUDA; a stalled TMA pipeline is reported by tm_check as
+ *         TM_ERR_TIMEOUT.
+ */
+tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, void *workspace,
+                    size_t ws_bytes, int32_t TM, int32_t TN, tm_variant variant, uint32_t flags,
+                    tm_stream_t stream);
+
+/*
+ * tm_rowmax_masked -- m[i] = max_{j < N} S[i, j] over ragged BC-column tiles.
+ * "Slicing, bounds and masking", "Reductions over a ragged tile": whole tiles
+ * are read unmasked; the remainder tile's missing columns read 0 and are then
+ * replaced by where(iota < N - kt, s, fill).  fill = TM_FILL_NEG_INF gives the
+ * true row maximum (a value no real score reaches); TM_FILL_ZERO skips the
+ * where step and reproduces the pitfall (max(0, true max) when N % BC != 0).
+ * N == 0 gives -inf.  max ignores a NaN operand unless both are NaN.
+ *   S, lds   device input [M, lds]     m   device output, M floats
+ *   BR       rows per block (one warp per row): 1, 2, 4, 8, 16, 32
+ *   BC       columns per tile: 16, 32, 64, 128, 256, 512
+ *   flags    TM_ALIGNED (M % BR == 0, N % BC == 0: no remainder, no row mask),
+ *            TM_PATH_SCALAR, TM_PATH_VEC
+ * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
+ */
+tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N, float *m, int32_t BR,
+                           int32_t BC, tm_fill fill, uint32_t flags, tm_stream_t stream);
+
+/*
+ * tm_check -- synchronize `stream`, then read and clear this device's status
+ * word.  Returns TM_ERR_BROKEN_PROMISE if a kernel's entry check found the
+ * aligned promise broken (that kernel stored nothing), TM_ERR_MISALIGNED if it
+ * found a misaligned pointer or ld, TM_ERR_TIMEOUT if a bounded wait gave up,
+ * TM_ERR_CUDA if the stream reports a CUDA error, else TM_OK.
+ */
+tm_status tm_check(tm_stream_t stream);
+
+/*
+ * Diagnostic entry points (used by the test suite; safe for any caller).
+ *
+ * tm_tile_walk_probe -- runs, on the device, the tile-walk planner every
+ * kernel uses for a loop over a runtime extent K in steps of T ("Slicing,
+ * bounds and masking", "Loops over a dynamic extent") and writes four int64 to
+ * the DEVICE pointer out4: whole (unmasked) tiles, masked tiles (0 or 1),
+ * columns in the masked tile, total iterations.
+ * Errors: INVALID_ARG (K < 0, T <= 0, out4 NULL), CUDA.
+ */
+tm_status tm_tile_walk_probe(int64_t K, int32_t T, int64_t *out4, tm_stream_t stream);
+
+/*
+ * tm_scale2d_unchecked -- tm_scale2d on its TM_ALIGNED path without the host
+ * promise check, so the kernel's own entry check is what stands between a
+ * broken promise and the tensor's end.  With a broken promise no element is
+ * read or written and the next tm_check returns TM_ERR_BROKEN_PROMISE (or
+ * TM_ERR_MISALIGNED).  Still validates everything except the promise and the
+ * alignment.  Tiles as tm_scale2d.
+ */
+tm_status tm_scale2d_unchecked(const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M,
+                               int64_t N, float alpha, int32_t TM, int32_t TN, tm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TM_H_ */

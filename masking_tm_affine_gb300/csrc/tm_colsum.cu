@@ -1,0 +1,605 @@
+// tm_colsum.cu -- c[j] = sum_i X[i, j]: the column walk and its fixes.
+//
+// Source: "Memory Coalescing and Tensor Layout".  "What it actually costs":
+// the column-order walk of a row-major matrix (offsets rows*COLS + col, 65536
+// programs of 256 elements over 4096 x 4096, neighbouring programs on
+// neighbouring columns) reads the same 64 MB as the row walk but 2.4x slower
+// on the page's GPU.  "Seeing it in a real kernel": the way out is to load a
+// tile once into fast memory and read it there in any order.
+//
+// Variants:
+//   NAIVE     -- the page's walk: a 256-lane program per (256-row block,
+//                column); lanes step down a column, ld apart.  Kept as the foil.
+//   REGDIRECT -- lanes over columns: a warp reads a contiguous row segment of a
+//                TN-column strip with 16-byte loads and walks down the rows,
+//                accumulating in registers.  No shared-memory staging needed.
+//   STAGED    -- the page's fix on GB300 hardware: the TMA engine copies
+//                TM x TN tiles into a ring of shared-memory stages (mbarrier
+//                completion, bounded waits); threads read the columns back out
+//                of shared memory.  Ragged edges come free: TMA fills
+//                out-of-bounds elements with 0, the masked-load value of
+//                "Slicing, bounds and masking" ("Masking").
+// Every variant writes one partial sum per (row chunk, column) into the
+// caller's workspace; colsum_finish then adds the partials of each column in
+// ascending chunk order.  No atomics: the result is the same run to run.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tm_host.h"
+
+namespace libtm {
+namespace {
+
+constexpr int kNaiveRows = 256;        // the page's program length
+constexpr int64_t kTargetUnits = 1024; // (strip, chunk) work units aimed for
+constexpr int kFinishPG = 8;           // chunk groups per column in the finish pass
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
+
+struct ColPlan {
+    int64_t S;      // column strips: ceil(N / TN)
+    int64_t RT;     // row tiles: ceil(M / TM)
+    int64_t CT;     // row tiles per chunk
+    int64_t P;      // chunks (partials per column)
+    int64_t units;  // S * P
+    int64_t npad;   // partial row length: N rounded up to 4
+};
+
+ColPlan plan_chunks(int64_t M, int64_t N, int64_t TM, int64_t TN)
+{
+    ColPlan pl;
+    pl.S = (N + TN - 1) / TN;
+    pl.RT = (M + TM - 1) / TM;
+    int64_t P = (kTargetUnits + pl.S - 1) / pl.S;
+    if (P > pl.RT) P = pl.RT;
+    if (P < 1) P = 1;
+    pl.CT = (pl.RT + P - 1) / P;
+    pl.P = (pl.RT + pl.CT - 1) / pl.CT;
+    pl.units = pl.S * pl.P;
+    pl.npad = (N + 3) & ~int64_t(3);
+    return pl;
+}
+
+struct ColArgs {
+    const float *X;
+    int64_t ldx, M, N;
+    float *part;    // [P][npad]
+    int64_t npad;
+    int64_t S, RT, CT, units;
+    int TM;
+    unsigned *status;
+};
+
+__device__ __forceinline__ void report(unsigned *status, unsigned bit)
+{
+    atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ NAIVE
+__global__ void __launch_bounds__(kNaiveRows) colsum_naive(const float *__restrict__ X, int64_t ldx, int64_t M,
+                                                           int64_t N, float *__restrict__ part, int64_t npad,
+                                                           int64_t programs)
+{
+    __shared__ float warp_sums[kNaiveRows / 32];
+    for (int64_t pid = blockIdx.x; pid < programs; pid += gridDim.x) {
+        const int64_t col = pid % N;  // neighbouring programs read neighbouring columns
+        const int64_t rb = pid / N;
+        const int64_t row = rb * kNaiveRows + threadIdx.x;
+        float v = row < M ? as_f(ld_nc_b32(X + row * ldx + col)) : 0.0f;  // lane stride: ld words
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = v;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float t = warp_sums[0];
+#pragma unroll
+            for (int w = 1; w < kNaiveRows / 32; ++w) t += warp_sums[w];
+            part[rb * npad + col] = t;
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ finish
+// c[j] = sum over chunks p (ascending) of part[p][j].  A block covers 32
+// columns; its 8 warps each add a contiguous group of chunks, and the groups
+// are added in order.
+__global__ void __launch_bounds__(256) colsum_finish(const float *__restrict__ part, int64_t npad, int64_t P,
+                                                     int64_t N, float *__restrict__ c)
+{
+    __shared__ float grp[kFinishPG][33];
+    const int cx = threadIdx.x & 31, py = threadIdx.x >> 5;
+    const int64_t per = (P + kFinishPG - 1) / kFinishPG;
+    const int64_t p_lo = py * per;
+    const int64_t p_hi = p_lo + per < P ? p_lo + per : P;
+    for (int64_t j0 = (int64_t)blockIdx.x * 32; j0 < N; j0 += (int64_t)gridDim.x * 32) {
+        const int64_t j = j0 + cx;
+        float s = 0.0f;
+        if (j < N) {
+            int64_t p = p_lo;
+            for (; p + 4 <= p_hi; p += 4) {
+                const float a0 = part[(p + 0) * npad + j], a1 = part[(p + 1) * npad + j];
+                const float a2 = part[(p + 2) * npad + j], a3 = part[(p + 3) * npad + j];
+                s += a0;
+                s += a1;
+                s += a2;
+                s += a3;
+            }
+            for (; p < p_hi; ++p) s += part[p * npad + j];
+        }
+        grp[py][cx] = s;
+        __syncthreads();
+        if (py == 0 && j < N) {
+            float t = grp[0][cx];
+#pragma unroll
+            for (int q = 1; q < kFinishPG; ++q) t += grp[q][cx];
+            c[j] = t;
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ REGDIRECT
+template <int TN, bool VEC, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
+{
+    constexpr int EW = VEC ? 4 : 1;
+    constexpr int CL = TN / EW;           // column lanes
+    constexpr int RL = kThreads / CL;     // row lanes
+    constexpr int UNR = 8;                // rows in flight per thread
+    static_assert(CL * RL == kThreads, "strip does not fit the block");
+    __shared__ float red[RL][TN];
+
+    if constexpr (ALIGNED) {
+        const bool whole = (a.M % a.TM == 0) && (a.N % TN == 0);
+        const bool grid_ok = !VEC || ((a.ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(a.X) & 15) == 0);
+        if (!whole || !grid_ok) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            return;
+        }
+    }
+    const int cl = threadIdx.x % CL, rl = threadIdx.x / CL;
+    const int64_t CR = a.CT * a.TM;  // rows per chunk
+    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x) {
+        const int64_t s = u % a.S, p = u / a.S;
+        const int64_t j = s * TN + (int64_t)cl * EW;
+        const bool col_in = ALIGNED || j < a.N;  // column mask of a ragged last strip
+        const int64_t r0 = p * CR;
+        const int64_t r1 = r0 + CR < a.M ? r0 + CR : a.M;  // rows past M are not visited
+        float acc[EW];
+#pragma unroll
+        for (int e = 0; e < EW; ++e) acc[e] = 0.0f;
+        if (col_in) {
+            const float *xp = a.X + j;
+            int64_t row = r0 + rl;
+            for (; row + (UNR - 1) * RL < r1; row += UNR * RL) {
+                uint32_t v[UNR][EW];
+#pragma unroll
+                for (int q = 0; q < UNR; ++q) {
+                    const float *ptr = xp + (row + (int64_t)q * RL) * a.ldx;
+                    if constexpr (VEC) {
+                        u32x4 w = ld_nc_v4(ptr);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[q][e] = w.v[e];
+                    } else {
+                        v[q][0] = ld_nc_b32(ptr);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < UNR; ++q)
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) acc[e] += as_f(v[q][e]);
+            }
+            for (; row < r1; row += RL) {
+                const float *ptr = xp + row * a.ldx;
+                if constexpr (VEC) {
+                    u32x4 w = ld_nc_v4(ptr);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
+                } else {
+                    acc[0] += as_f(ld_nc_b32(ptr));
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < EW; ++e) red[rl][cl * EW + e] = acc[e];
+        __syncthreads();
+        if (rl == 0 && col_in) {
+#pragma unroll
+            for (int e = 0; e < EW; ++e) {
+                float t = red[0][cl * EW + e];
+#pragma unroll
+                for (int q = 1; q < RL; ++q) t += red[q][cl * EW + e];
+                a.part[p * a.npad + j + e] = t;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ STAGED (TMA)
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the mbarrier, giving up after ~1 s.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) return false;
+    }
+    return true;
+}
+
+template <int TM, int TN, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
+                                                          int stages)
+{
+    constexpr int CL = TN / 4;            // column lanes, 4 columns each
+    constexpr int RL = kThreads / CL;     // row lanes
+    constexpr int TILE = TM * TN;         // floats per stage
+    static_assert(TM % RL == 0, "tile height must cover the row lanes");
+    extern __shared__ __align__(128) unsigned char smem[];
+    float *tiles = reinterpret_cast<float *>(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * TILE * sizeof(float));
+    __shared__ float red[RL][TN];
+    __shared__ int abort_flag;
+
+    if constexpr (ALIGNED) {
+        const bool whole = (a.M % TM == 0) && (a.N % TN == 0);
+        if (!whole) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, kStatusBrokenPromise);
+            return;
+        }
+    }
+    if (blockIdx.x >= a.units) return;
+    const int tid = threadIdx.x;
+    const int cl = tid % CL, rl = tid / CL;
+    const int64_t my_units = (a.units - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const int64_t slots = my_units * a.CT;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < stages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[s])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // slot k of this block's tile stream -> (strip, chunk, row tile)
+    auto decode = [&](int64_t k, int64_t &s, int64_t &p, int64_t &rt) {
+        const int64_t u = blockIdx.x + (k / a.CT) * (int64_t)gridDim.x;
+        s = u % a.S;
+        p = u / a.S;
+        rt = p * a.CT + k % a.CT;
+        return rt < a.RT;  // trailing slots of a short last chunk do not exist
+    };
+    auto issue = [&](int64_t k) {
+        if (k >= slots) return;
+        int64_t s, p, rt;
+        if (!decode(k, s, p, rt)) return;
+        const int st = (int)(k % stages);
+        const uint32_t bar = smem_u32(&full[st]);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(TILE * sizeof(float)))
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(tiles + (size_t)st * TILE)),
+            "l"(&tmap), "r"((int)(s * TN)), "r"((int)(rt * TM)), "r"(bar)
+            : "memory");
+    };
+
+    if (tid == 0)
+        for (int k = 0; k < stages; ++k) issue(k);
+
+    uint32_t phase = 0;  // bit s: parity of the next completion of stage s
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    bool aborted = false;
+    for (int64_t k = 0; k < slots; ++k) {
+        int64_t s, p, rt;
+        const bool exists = decode(k, s, p, rt);
+        const int st = (int)(k % stages);
+        if (exists) {
+            if (!mbar_wait_bounded(smem_u32(&full[st]), (phase >> st) & 1u)) {
+                report(a.status, kStatusTimeout);
+                abort_flag = 1;
+            } else {
+                const float *t = tiles + (size_t)st * TILE;
+#pragma unroll
+                for (int rr = rl; rr < TM; rr += RL) {
+                    const float4 v = *reinterpret_cast<const float4 *>(t + rr * TN + cl * 4);
+                    acc[0] += v.x;
+                    acc[1] += v.y;
+                    acc[2] += v.z;
+                    acc[3] += v.w;
+                }
+            }
+            phase ^= 1u << st;
+        }
+        if (k % a.CT == a.CT - 1 || k == slots - 1) {
+            // end of a unit: add the row lanes in order, write this chunk's partial
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                red[rl][cl * 4 + e] = acc[e];
+                acc[e] = 0.0f;
+            }
+            __syncthreads();
+            const int64_t j = s * TN + cl * 4;
+            if (rl == 0 && j < a.N) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float tot = red[0][cl * 4 + e];
+#pragma unroll
+                    for (int q = 1; q < RL; ++q) tot += red[q][cl * 4 + e];
+                    if (j + e < a.N) a.part[p * a.npad + j + e] = tot;
+                }
+            }
+        }
+        __syncthreads();  // every read of stage st (and of red) is done
+        if (abort_flag) {
+            aborted = true;
+            break;
+        }
+        if (tid == 0) issue(k + stages);
+    }
+    if (aborted && tid == 0) {
+        // let copies still in flight land before the block's shared memory goes away
+        for (int st = 0; st < stages; ++st) mbar_wait_bounded(smem_u32(&full[st]), (phase >> st) & 1u);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool staged_tile(int TM, int TN)
+{
+    if (!(TN == 64 || TN == 128 || TN == 256)) return false;
+    if (TM * TN > 8192) return false;
+    return TM >= 1024 / TN && TM <= 256;
+}
+
+int staged_stages(int TM, int TN)
+{
+    const int bytes = TM * TN * 4;
+    int s = (64 * 1024) / bytes;
+    if (s < 2) s = 2;
+    if (s > 8) s = 8;
+    return s;
+}
+
+bool pow2_in(int v, int lo, int hi)
+{
+    return v >= lo && v <= hi && (v & (v - 1)) == 0;
+}
+
+template <int TM, int TN>
+tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, const DevInfo *dev,
+                          cudaStream_t s)
+{
+    const void *k = aligned ? (const void *)colsum_staged<TM, TN, true> : (const void *)colsum_staged<TM, TN, false>;
+    int stages = staged_stages(TM, TN);
+    const size_t smem = (size_t)stages * TM * TN * sizeof(float) + (size_t)stages * sizeof(uint64_t);
+    static std::once_flag attr_once[kMaxDevices][2];
+    int devno = 0;
+    cudaGetDevice(&devno);
+    bool attr_ok = true;
+    std::call_once(attr_once[devno][aligned ? 1 : 0], [&] {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+            cudaGetLastError();
+            attr_ok = false;
+        }
+    });
+    if (!attr_ok) return TM_ERR_CUDA;
+    const int64_t grid = persistent_grid(dev, k, a.units, smem);
+    void *args[] = {const_cast<CUtensorMap *>(&map), const_cast<ColArgs *>(&a), &stages};
+    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(kThreads), args, smem, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
+tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a,
+                        const DevInfo *dev, cudaStream_t s)
+{
+#define TM_STAGED(tm_, tn_) \
+    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, dev, s);
+    TM_STAGED(16, 64)
+    TM_STAGED(32, 64)
+    TM_STAGED(64, 64)
+    TM_STAGED(128, 64)
+    TM_STAGED(8, 128)
+    TM_STAGED(16, 128)
+    TM_STAGED(32, 128)
+    TM_STAGED(64, 128)
+    TM_STAGED(8, 256)
+    TM_STAGED(16, 256)
+    TM_STAGED(32, 256)
+#undef TM_STAGED
+    return TM_ERR_UNSUPPORTED_TILE;
+}
+
+template <int TN>
+tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, const DevInfo *dev, cudaStream_t s)
+{
+    const void *k;
+    if (vec) k = aligned ? (const void *)colsum_regdirect<TN, true, true> : (const void *)colsum_regdirect<TN, true, false>;
+    else k = aligned ? (const void *)colsum_regdirect<TN, false, true> : (const void *)colsum_regdirect<TN, false, false>;
+    const int64_t grid = persistent_grid(dev, k, a.units);
+    void *args[] = {const_cast<ColArgs *>(&a)};
+    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(kThreads), args, 0, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
+tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, float *c, const DevInfo *dev,
+                        cudaStream_t s)
+{
+    const int64_t blocks = (N + 31) / 32;
+    const int64_t grid = persistent_grid(dev, (const void *)colsum_finish, blocks);
+    colsum_finish<<<(unsigned)grid, 256, 0, s>>>(part, npad, P, N, c);
+    return launch_status();
+}
+
+enum class Variant { Naive, RegDirect, Staged };
+
+}  // namespace
+}  // namespace libtm
+
+using namespace libtm;
+
+extern "C" size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, tm_variant variant)
+{
+    if (M <= 0 || N <= 0) return 0;
+    if (variant == TM_VAR_NAIVE) {
+        const int64_t rb = (M + kNaiveRows - 1) / kNaiveRows;
+        return (size_t)(rb * ((N + 3) & ~int64_t(3)) * (int64_t)sizeof(float));
+    }
+    if (variant != TM_VAR_AUTO && variant != TM_VAR_STAGED && variant != TM_VAR_REGDIRECT) return 0;
+    if (!pow2_in(TM, 8, 256) || !(TN == 64 || TN == 128 || TN == 256)) return 0;
+    const ColPlan pl = plan_chunks(M, N, TM, TN);
+    return (size_t)(pl.P * pl.npad * (int64_t)sizeof(float));
+}
+
+extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, void *workspace,
+                               size_t ws_bytes, int32_t TM, int32_t TN, tm_variant variant, uint32_t flags,
+                               tm_stream_t stream)
+{
+    if (!valid2d(X, ldx, M, N)) return TM_ERR_INVALID_ARG;
+    if (N > 0 && c == nullptr) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
+    if (variant != TM_VAR_AUTO && variant != TM_VAR_NAIVE && variant != TM_VAR_STAGED &&
+        variant != TM_VAR_REGDIRECT)
+        return TM_ERR_INVALID_ARG;
+    if (variant != TM_VAR_NAIVE && (!pow2_in(TM, 8, 256) || !(TN == 64 || TN == 128 || TN == 256)))
+        return TM_ERR_UNSUPPORTED_TILE;
+    if (variant == TM_VAR_STAGED && !staged_tile(TM, TN)) return TM_ERR_UNSUPPORTED_TILE;
+    if (N > 0 && !aligned_to(c, 4)) return TM_ERR_MISALIGNED;
+    if (M > 0 && N > 0 && !aligned_to(X, 4)) return TM_ERR_MISALIGNED;
+    const bool aligned = (flags & TM_ALIGNED) != 0;
+    const bool vec16 = aligned_to(X, 16) && ldx % 4 == 0;
+    if (aligned) {
+        if (!vec16) return TM_ERR_MISALIGNED;
+        if (variant == TM_VAR_NAIVE) return TM_ERR_INVALID_ARG;  // the foil has no whole-tile path
+        if (M % TM != 0 || N % TN != 0) return TM_ERR_BROKEN_PROMISE;
+    }
+    if ((flags & TM_PATH_VEC) && !(vec16 && N % 4 == 0)) return TM_ERR_MISALIGNED;
+
+    const bool vec = !(flags & TM_PATH_SCALAR) && vec16 && (aligned || N % 4 == 0);
+
+    // scratch: partial sums per (chunk, column)
+    int64_t P = 0;
+    const int64_t npad = (N + 3) & ~int64_t(3);
+    ColPlan pl{};
+    if (M > 0 && N > 0) {
+        const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant == TM_VAR_NAIVE ? TM_VAR_NAIVE : TM_VAR_AUTO);
+        if (workspace == nullptr || ws_bytes < need || !aligned_to(workspace, 16)) return TM_ERR_WORKSPACE;
+        uintptr_t xlo, xhi, wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+        span2d(X, ldx, M, N, &xlo, &xhi);
+        const uintptr_t clo = reinterpret_cast<uintptr_t>(c), chi = clo + (uintptr_t)N * 4;
+        if (!(xhi <= wlo || whi <= xlo) || !(chi <= wlo || whi <= clo) || !(xhi <= clo || chi <= xlo))
+            return TM_ERR_INVALID_ARG;
+        if (variant == TM_VAR_NAIVE) P = (M + kNaiveRows - 1) / kNaiveRows;
+        else {
+            pl = plan_chunks(M, N, TM, TN);
+            P = pl.P;
+        }
+    }
+    const bool tma_shape = vec16 && M <= INT32_MAX && N <= INT32_MAX && staged_tile(TM, TN) &&
+                           !(flags & (TM_PATH_SCALAR | TM_PATH_VEC));
+    if (variant == TM_VAR_STAGED && !tma_shape) return TM_ERR_MISALIGNED;
+    if (N == 0) return TM_OK;
+
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    float *part = static_cast<float *>(workspace);
+
+    // pick the variant (the TMA encoder comes from the driver on first use)
+    Variant v;
+    if (variant == TM_VAR_NAIVE) v = Variant::Naive;
+    else if (variant == TM_VAR_REGDIRECT) v = Variant::RegDirect;
+    else if (variant == TM_VAR_STAGED) {
+        if (encode_fn() == nullptr) return TM_ERR_CUDA;
+        v = Variant::Staged;
+    } else v = (tma_shape && encode_fn() != nullptr) ? Variant::Staged : Variant::RegDirect;
+
+    if (M > 0) {
+        if (v == Variant::Naive) {
+            const int64_t programs = P * N;
+            const int64_t grid = persistent_grid(dev, (const void *)colsum_naive, programs, 0, kNaiveRows);
+            colsum_naive<<<(unsigned)grid, kNaiveRows, 0, s>>>(X, ldx, M, N, part, npad, programs);
+            st = launch_status();
+        } else {
+            ColArgs a;
+            a.X = X;
+            a.ldx = ldx;
+            a.M = M;
+            a.N = N;
+            a.part = part;
+            a.npad = pl.npad;
+            a.S = pl.S;
+            a.RT = pl.RT;
+            a.CT = pl.CT;
+            a.units = pl.units;
+            a.TM = TM;
+            a.status = dev->status;
+            if (v == Variant::Staged) {
+                CUtensorMap map;
+                const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+                const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
+                const cuuint32_t box[2] = {(cuuint32_t)TN, (cuuint32_t)TM};
+                const cuuint32_t estr[2] = {1, 1};
+                if (encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(X), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                    return TM_ERR_CUDA;
+                st = launch_staged(TM, TN, aligned, map, a, dev, s);
+            } else {
+                switch (TN) {
+                case 64: st = launch_regdirect_t<64>(vec, aligned, a, dev, s); break;
+                case 128: st = launch_regdirect_t<128>(vec, aligned, a, dev, s); break;
+                default: st = launch_regdirect_t<256>(vec, aligned, a, dev, s); break;
+                }
+            }
+        }
+        if (st != TM_OK) return st;
+    }
+    return launch_finish(part, npad, P, N, c, dev, s);
+}

@@ -1,0 +1,149 @@
+// tm_core.cu -- per-device state, status reporting and the diagnostic probes.
+//
+// The pages' broken-promise behaviour is a trap that makes the host's next
+// synchronize fail ("@aligned", "When the promise is broken").  Here the
+// kernel's entry check instead sets a bit in a per-device status word and
+// every block returns before its first access; tm_check is that "next
+// synchronize": it waits on the stream and reports the bit.
+#include <atomic>
+#include <mutex>
+#include <unordered_map>
+
+#include "tm_host.h"
+
+namespace libtm {
+
+// One status word per device (the module is loaded once per device context).
+__device__ unsigned g_status_word;
+
+namespace {
+
+struct DevSlot {
+    std::atomic<bool> ready{false};
+    DevInfo info{};
+};
+
+DevSlot g_slots[kMaxDevices];
+std::mutex g_init_mu;
+
+std::mutex g_occ_mu;
+std::unordered_map<uint64_t, int> g_occ[kMaxDevices];
+
+}  // namespace
+
+tm_status device_info(const DevInfo **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    DevSlot &s = g_slots[dev];
+    if (!s.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_init_mu);
+        if (!s.ready.load(std::memory_order_relaxed)) {
+            int sms = 0;
+            void *addr = nullptr;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess || sms <= 0) {
+                cudaGetLastError();
+                return TM_ERR_CUDA;
+            }
+            s.info.sms = sms;
+            s.info.status = static_cast<unsigned *>(addr);
+            s.ready.store(true, std::memory_order_release);
+        }
+    }
+    *out = &s.info;
+    return TM_OK;
+}
+
+int blocks_per_sm(const void *kernel, int threads, size_t smem)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 1;
+    }
+    uint64_t key = reinterpret_cast<uint64_t>(kernel) ^ ((uint64_t)threads << 48) ^ ((uint64_t)smem << 32);
+    {
+        std::lock_guard<std::mutex> lock(g_occ_mu);
+        auto it = g_occ[dev].find(key);
+        if (it != g_occ[dev].end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = 1;
+    }
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    g_occ[dev][key] = n;
+    return n;
+}
+
+namespace {
+
+__global__ void tile_walk_probe_kernel(int64_t K, int64_t T, int64_t *out4)
+{
+    TileWalk w = tile_walk(K, T);
+    out4[0] = w.whole;
+    out4[1] = w.masked;
+    out4[2] = w.rem;
+    out4[3] = w.iters;
+}
+
+}  // namespace
+}  // namespace libtm
+
+using namespace libtm;
+
+extern "C" const char *tm_status_string(tm_status st)
+{
+    switch (st) {
+    case TM_OK: return "TM_OK";
+    case TM_ERR_INVALID_ARG: return "TM_ERR_INVALID_ARG: invalid argument";
+    case TM_ERR_UNSUPPORTED_TILE: return "TM_ERR_UNSUPPORTED_TILE: tile not positive or not instantiated";
+    case TM_ERR_MISALIGNED: return "TM_ERR_MISALIGNED: pointer or leading dimension breaks vector alignment";
+    case TM_ERR_BROKEN_PROMISE: return "TM_ERR_BROKEN_PROMISE: aligned promise broken (extent not a whole number of tiles)";
+    case TM_ERR_CUDA: return "TM_ERR_CUDA: CUDA runtime error";
+    case TM_ERR_WORKSPACE: return "TM_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case TM_ERR_TIMEOUT: return "TM_ERR_TIMEOUT: a bounded device wait gave up";
+    }
+    return "TM_ERR_UNKNOWN";
+}
+
+extern "C" int tm_version(void) { return 10000; }
+
+extern "C" tm_status tm_check(tm_stream_t stream)
+{
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    unsigned word = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyAsync(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(dev->status, &zero, sizeof zero, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    if (word & kStatusBrokenPromise) return TM_ERR_BROKEN_PROMISE;
+    if (word & kStatusMisaligned) return TM_ERR_MISALIGNED;
+    if (word & kStatusTimeout) return TM_ERR_TIMEOUT;
+    return TM_OK;
+}
+
+extern "C" tm_status tm_tile_walk_probe(int64_t K, int32_t T, int64_t *out4, tm_stream_t stream)
+{
+    if (K < 0 || T <= 0 || out4 == nullptr) return TM_ERR_INVALID_ARG;
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    tile_walk_probe_kernel<<<1, 1, 0, as_stream(stream)>>>(K, T, out4);
+    return launch_status();
+}

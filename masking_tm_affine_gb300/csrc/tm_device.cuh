@@ -1,0 +1,119 @@
+// tm_device.cuh -- device-side building blocks shared by the libtm kernels.
+//
+// Global accesses are written as inline PTX so the instruction each path
+// issues is fixed by the source, not left to the vectoriser: the puzzle
+// "Aligned Load & Store" ("Solution") is exactly about the gap between four
+// scalar `ld.global.nc.f32` and one `ld.global.nc.v4.f32` per 4-element chunk.
+// Loads of read-only inputs use the non-coherent path with L1::no_allocate
+// (each byte is read once); values move as raw 32-bit words so a copy keeps
+// NaN payloads bit for bit.
+#pragma once
+
+#include <cstdint>
+
+namespace libtm {
+
+// Status word bits (one word per device; read and cleared by tm_check).
+enum : unsigned {
+    kStatusBrokenPromise = 1u,  // aligned path entered with M % TM or N % TN != 0
+    kStatusMisaligned = 2u,     // aligned path entered with a pointer or ld off the vector grid
+    kStatusTimeout = 4u,        // a bounded wait gave up
+};
+
+struct u32x4 {
+    uint32_t v[4];
+};
+struct u32x8 {
+    uint32_t v[8];
+};
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ uint32_t ld_nc_b32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ u32x4 ld_nc_v4(const void *p)
+{
+    u32x4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
+                 : "l"(p));
+    return r;
+}
+
+// 32-byte access: sm_100-class GPUs accept .v8 for 32-bit types in .global.
+__device__ __forceinline__ u32x8 ld_nc_v8(const void *p)
+{
+    u32x8 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]),
+                   "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(p));
+    return r;
+}
+
+// ---------------------------------------------------------------- stores
+__device__ __forceinline__ void st_b32(void *p, uint32_t x)
+{
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(p), "r"(x) : "memory");
+}
+
+__device__ __forceinline__ void st_v4(void *p, const u32x4 &x)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(x.v[0]), "r"(x.v[1]),
+                 "r"(x.v[2]), "r"(x.v[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v8(void *p, const u32x8 &x)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(x.v[0]),
+                 "r"(x.v[1]), "r"(x.v[2]), "r"(x.v[3]), "r"(x.v[4]), "r"(x.v[5]), "r"(x.v[6]),
+                 "r"(x.v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t as_u(float f) { return __float_as_uint(f); }
+
+// ---------------------------------------------------------------- tile walk
+// The split of a loop over a runtime extent K in steps of T into whole tiles
+// (no mask) and at most one masked remainder tile ("Slicing, bounds and
+// masking", "Loops over a dynamic extent": K = 1000, T = 16 gives 62 + 1 over
+// 8 columns).  Every kernel that walks a runtime extent takes its bounds from
+// here; tm_tile_walk_probe exposes it to the tests.
+struct TileWalk {
+    int64_t whole;   // tiles that lie entirely inside [0, K)
+    int64_t masked;  // 1 if a partial tile remains, else 0
+    int64_t rem;     // extent of that partial tile (K - whole*T)
+    int64_t iters;   // whole + masked
+};
+
+__host__ __device__ __forceinline__ TileWalk tile_walk(int64_t K, int64_t T)
+{
+    TileWalk w;
+    w.whole = K / T;
+    w.rem = K - w.whole * T;
+    w.masked = w.rem > 0 ? 1 : 0;
+    w.iters = w.whole + w.masked;
+    return w;
+}
+
+// ---------------------------------------------------------------- division
+// n / d for 0 <= n < 2^31 and 1 <= d < 2^31 by multiply-high and shift (the
+// round-up method of Granlund and Montgomery, "Division by invariant integers
+// using multiplication", PLDI 1994).  Built on the host, used per element on
+// the device where a runtime divisor would otherwise cost a division loop.
+struct FastDiv {
+    uint32_t d, mul, shift;
+};
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f)
+{
+    return (__umulhi(n, f.mul) + n) >> f.shift;
+}
+
+}  // namespace libtm

@@ -1,0 +1,107 @@
+// tm_host.h -- host-side internals shared by the libtm translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/tm.h"
+#include "tm_device.cuh"
+
+namespace libtm {
+
+constexpr int kMaxDevices = 64;
+constexpr int kThreads = 256;  // block size of the streaming kernels
+
+// Per-device facts, filled once per device on first use (tm_core.cu).
+struct DevInfo {
+    int sms;           // multiprocessor count
+    unsigned *status;  // device address of this device's status word
+};
+
+// Current device's info; TM_ERR_CUDA if the runtime cannot answer.
+tm_status device_info(const DevInfo **out);
+
+// Resident blocks per SM for `kernel` at `threads` threads and `smem` dynamic
+// shared bytes on the current device (cached per device and kernel).
+int blocks_per_sm(const void *kernel, int threads, size_t smem);
+
+// Persistent grid: enough blocks to fill every SM at full residency, but no
+// more than there are work units.
+inline int64_t persistent_grid(const DevInfo *dev, const void *kernel, int64_t units,
+                               size_t smem = 0, int threads = kThreads)
+{
+    int64_t per_sm = blocks_per_sm(kernel, threads, smem);
+    if (per_sm < 1) per_sm = 1;
+    int64_t g = (int64_t)dev->sms * per_sm;
+    if (units < g) g = units;
+    if (g < 1) g = 1;
+    return g;
+}
+
+// Map the last launch's outcome to a status.
+inline tm_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+}
+
+inline cudaStream_t as_stream(tm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned_to(const void *p, uintptr_t bytes)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+
+// Byte extent [lo, hi) touched by a row-major [M, N] tensor with leading dimension ld.
+inline void span2d(const void *base, int64_t ld, int64_t M, int64_t N, uintptr_t *lo, uintptr_t *hi)
+{
+    *lo = reinterpret_cast<uintptr_t>(base);
+    *hi = *lo + (uintptr_t)(((M - 1) * ld + N) * (int64_t)sizeof(float));
+}
+
+// Shared argument checks of a 2-D [M, N] operand: extents >= 0, ld >= N,
+// no int64 overflow of the addressed span, non-NULL when there is work.
+inline bool valid2d(const void *p, int64_t ld, int64_t M, int64_t N)
+{
+    if (M < 0 || N < 0 || ld < N || ld < 0) return false;
+    if (M == 0 || N == 0) return true;
+    if (p == nullptr) return false;
+    if (ld > 0 && M > (INT64_MAX / 4) / ld) return false;
+    return true;
+}
+
+// Two 2-D operands may alias only exactly (same base, same ld): in-place maps.
+inline bool overlap_ok(const void *a, int64_t lda, const void *b, int64_t ldb, int64_t M, int64_t N)
+{
+    if (M == 0 || N == 0) return true;
+    if (a == b) return lda == ldb;
+    uintptr_t alo, ahi, blo, bhi;
+    span2d(a, lda, M, N, &alo, &ahi);
+    span2d(b, ldb, M, N, &blo, &bhi);
+    return ahi <= blo || bhi <= alo;
+}
+
+// Multiply-high divider for 1 <= d < 2^31 (see FastDiv in tm_device.cuh).
+inline FastDiv make_fastdiv(uint32_t d)
+{
+    FastDiv f;
+    f.d = d;
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    f.shift = l;
+    f.mul = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+    return f;
+}
+
+constexpr uint32_t kPathBits = TM_PATH_SCALAR | TM_PATH_VEC | TM_PATH_TMA;
+
+// At most one path bit, no unknown bits.
+inline bool flags_ok(uint32_t flags, uint32_t allowed)
+{
+    if (flags & ~allowed) return false;
+    uint32_t p = flags & kPathBits;
+    return (p & (p - 1)) == 0;
+}
+
+}  // namespace libtm

@@ -1,0 +1,277 @@
+// tm_map2d.cu -- tiled 2-D maps: Y = alpha*X (tm_scale2d) and B = A (tm_copy2d).
+//
+// Sources: "@aligned" ("A minimal kernel": kernel `scale`, one TM x TN tile per
+// work unit; "What it changes": no masks and 16-byte row access under the
+// promise; "When the promise is broken": the promise is checked once at kernel
+// entry); "Slicing, bounds and masking" ("Masking": loads past the end read 0,
+// stores past the end are skipped; "Promising whole tiles with @aligned":
+// kernel copy2d with 64 x 64 tiles).
+//
+// GB300 design.  The pages launch one CTA per tile.  Here a persistent grid
+// (every SM filled at full residency) walks the tile space in row-major tile
+// order; each iteration takes a group of G consecutive tiles so that every
+// thread has U independent loads in flight (G = 1 for tiles of >= 1024
+// vectors).  Within a group, consecutive threads take consecutive vectors of a
+// tile row, so a warp reads whole 128-byte lines.  Three paths:
+//   Aligned   -- the promise holds: no predicate on any access, 16- or 32-byte
+//                vectors.  Entry check first; on failure no block touches memory.
+//   RaggedVec -- N, ld multiples of 4 and 16-byte bases: 16-byte vectors, one
+//                predicate per vector (a vector is wholly in or wholly out).
+//   Scalar    -- anything else: 4-byte accesses, one predicate per element.
+#include "tm_host.h"
+
+namespace libtm {
+namespace {
+
+enum class Op { Scale, Copy };
+enum class Path { Aligned, RaggedVec, Scalar };
+
+struct Map2dArgs {
+    const float *X;
+    float *Y;
+    int64_t ldx, ldy, M, N;
+    float alpha;
+    uint32_t tiles_n;  // ceil(N / TN)
+    uint32_t ntiles;   // ceil(M / TM) * tiles_n
+    FastDiv div_tiles_n;
+    unsigned *status;
+};
+
+template <Op OP>
+__device__ __forceinline__ uint32_t apply(uint32_t x, float alpha)
+{
+    if (OP == Op::Copy) return x;                 // bitwise: no arithmetic touches the word
+    return as_u(__fmul_rn(alpha, as_f(x)));       // one rounding, like the oracle
+}
+
+template <int EW>
+struct Vec {
+    uint32_t v[EW];
+};
+
+template <int EW>
+__device__ __forceinline__ Vec<EW> load_vec(const float *p)
+{
+    Vec<EW> r;
+    if constexpr (EW == 1) {
+        r.v[0] = ld_nc_b32(p);
+    } else if constexpr (EW == 4) {
+        u32x4 t = ld_nc_v4(p);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r.v[e] = t.v[e];
+    } else {
+        u32x8 t = ld_nc_v8(p);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r.v[e] = t.v[e];
+    }
+    return r;
+}
+
+template <int EW>
+__device__ __forceinline__ void store_vec(float *p, const Vec<EW> &x)
+{
+    if constexpr (EW == 1) {
+        st_b32(p, x.v[0]);
+    } else if constexpr (EW == 4) {
+        u32x4 t;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) t.v[e] = x.v[e];
+        st_v4(p, t);
+    } else {
+        u32x8 t;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t.v[e] = x.v[e];
+        st_v8(p, t);
+    }
+}
+
+template <int TM, int TN, Op OP, Path P, int EW>
+__global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
+{
+    constexpr int VPR = TN / EW;                       // accesses per tile row
+    constexpr int V = TM * VPR;                        // accesses per tile
+    constexpr int G = V >= 4 * kThreads ? 1 : (4 * kThreads) / V;  // tiles per group
+    constexpr int A = G * V;                           // accesses per group
+    constexpr int U = A / kThreads;                    // accesses per thread per group
+    constexpr int UB = U < 4 ? U : 4;                  // accesses in flight per batch
+    static_assert(A % kThreads == 0 && U % UB == 0, "tile shape does not fit the block");
+
+    if constexpr (P == Path::Aligned) {
+        // The promise, checked once at entry ("@aligned", "When the promise is
+        // broken").  A pure function of the arguments, so every block takes the
+        // same branch: on failure nothing is read or written anywhere.
+        const bool whole = (p.M % TM == 0) && (p.N % TN == 0);
+        const bool grid_ok = (p.ldx % EW == 0) && (p.ldy % EW == 0) &&
+                             ((reinterpret_cast<uintptr_t>(p.X) | reinterpret_cast<uintptr_t>(p.Y)) &
+                              (EW * sizeof(float) - 1)) == 0;
+        if (!whole || !grid_ok) {
+            if (blockIdx.x == 0 && threadIdx.x == 0)
+                atomicOr(p.status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            return;
+        }
+    }
+
+    const uint32_t ngroups = (p.ntiles + G - 1) / G;
+    for (uint32_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+#pragma unroll(U / UB <= 4 ? U / UB : 1)
+        for (int b = 0; b < U; b += UB) {
+            Vec<EW> val[UB];
+            int64_t yoff[UB];
+            bool live[UB];
+#pragma unroll
+            for (int u = 0; u < UB; ++u) {
+                const uint32_t k = (uint32_t)(b + u) * kThreads + threadIdx.x;  // access within group
+                const uint32_t tile = g * G + k / V;
+                const uint32_t v = k % V;
+                const uint32_t r = v / VPR;
+                const uint32_t c = (v % VPR) * EW;
+                const uint32_t pm = fdiv(tile, p.div_tiles_n);
+                const uint32_t pn = tile - pm * p.tiles_n;
+                const int64_t i = (int64_t)pm * TM + r;
+                const int64_t j = (int64_t)pn * TN + c;
+                bool in = (G == 1) || (tile < p.ntiles);
+                if constexpr (P != Path::Aligned) in = in && (i < p.M) && (j < p.N);
+                live[u] = in;
+                yoff[u] = i * p.ldy + j;
+                if (in) {
+                    val[u] = load_vec<EW>(p.X + i * p.ldx + j);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) val[u].v[e] = 0u;  // a masked load reads 0
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < UB; ++u) {
+                if (!live[u]) continue;                              // a masked store is skipped
+                Vec<EW> o;
+#pragma unroll
+                for (int e = 0; e < EW; ++e) o.v[e] = apply<OP>(val[u].v[e], p.alpha);
+                store_vec<EW>(p.Y + yoff[u], o);
+            }
+        }
+    }
+}
+
+template <int TM, int TN, Op OP>
+tm_status launch_tile(Path path, int ew, const Map2dArgs &a, const DevInfo *dev, cudaStream_t s)
+{
+    const void *k = nullptr;
+    if (path == Path::Aligned && ew == 8) k = (const void *)map2d_kernel<TM, TN, OP, Path::Aligned, 8>;
+    else if (path == Path::Aligned) k = (const void *)map2d_kernel<TM, TN, OP, Path::Aligned, 4>;
+    else if (path == Path::RaggedVec) k = (const void *)map2d_kernel<TM, TN, OP, Path::RaggedVec, 4>;
+    else k = (const void *)map2d_kernel<TM, TN, OP, Path::Scalar, 1>;
+    const int EW = path == Path::Scalar ? 1 : ew;
+    const int64_t V = (int64_t)TM * TN / EW;
+    const int64_t G = V >= 4 * kThreads ? 1 : (4 * kThreads) / V;
+    const int64_t groups = ((int64_t)a.ntiles + G - 1) / G;
+    const int64_t grid = persistent_grid(dev, k, groups);
+    void *args[] = {const_cast<Map2dArgs *>(&a)};
+    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(kThreads), args, 0, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
+template <Op OP>
+tm_status dispatch(int TM, int TN, Path path, int ew, const Map2dArgs &a, const DevInfo *dev, cudaStream_t s)
+{
+#define TM_TILE(tm_, tn_) \
+    if (TM == tm_ && TN == tn_) return launch_tile<tm_, tn_, OP>(path, ew, a, dev, s);
+    TM_TILE(8, 8)
+    TM_TILE(16, 16)
+    TM_TILE(32, 32)
+    TM_TILE(64, 64)
+    TM_TILE(32, 128)
+    TM_TILE(128, 128)
+#undef TM_TILE
+    return TM_ERR_UNSUPPORTED_TILE;
+}
+
+bool tile_supported(int TM, int TN)
+{
+    return (TM == 8 && TN == 8) || (TM == 16 && TN == 16) || (TM == 32 && TN == 32) ||
+           (TM == 64 && TN == 64) || (TM == 32 && TN == 128) || (TM == 128 && TN == 128);
+}
+
+tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M, int64_t N,
+                float alpha, int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream, bool check_promise)
+{
+    if (!valid2d(X, ldx, M, N) || !valid2d(Y, ldy, M, N)) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | kPathBits)) return TM_ERR_INVALID_ARG;
+    if (TM <= 0 || TN <= 0 || !tile_supported(TM, TN)) return TM_ERR_UNSUPPORTED_TILE;
+    if (!overlap_ok(X, ldx, Y, ldy, M, N)) return TM_ERR_INVALID_ARG;
+    if (M > 0 && N > 0 && (!aligned_to(X, 4) || !aligned_to(Y, 4))) return TM_ERR_MISALIGNED;
+    if (flags & TM_PATH_TMA) return TM_ERR_INVALID_ARG;  // no TMA variant of the 2-D maps yet
+
+    const bool vec16 = aligned_to(X, 16) && aligned_to(Y, 16) && ldx % 4 == 0 && ldy % 4 == 0;
+    const bool vec32 = aligned_to(X, 32) && aligned_to(Y, 32) && ldx % 8 == 0 && ldy % 8 == 0 && TN % 8 == 0;
+    Path path;
+    int ew = 4;
+    if (flags & TM_ALIGNED) {
+        if (check_promise) {
+            if (!vec16) return TM_ERR_MISALIGNED;
+            if (M % TM != 0 || N % TN != 0) return TM_ERR_BROKEN_PROMISE;
+        }
+        if (flags & TM_PATH_SCALAR) {
+            path = Path::Scalar;
+        } else {
+            path = Path::Aligned;
+            ew = (vec32 && !(flags & TM_PATH_VEC) && check_promise) ? 8 : 4;
+        }
+    } else if (flags & TM_PATH_SCALAR) {
+        path = Path::Scalar;
+    } else if (vec16 && N % 4 == 0) {
+        path = Path::RaggedVec;
+    } else if (flags & TM_PATH_VEC) {
+        return TM_ERR_MISALIGNED;
+    } else {
+        path = Path::Scalar;
+    }
+    if (M == 0 || N == 0) return TM_OK;
+
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+
+    const int64_t tiles_m = (M + TM - 1) / TM, tiles_n = (N + TN - 1) / TN;
+    if (tiles_n > INT32_MAX || tiles_m > INT32_MAX / tiles_n) return TM_ERR_INVALID_ARG;
+    Map2dArgs a;
+    a.X = X;
+    a.Y = Y;
+    a.ldx = ldx;
+    a.ldy = ldy;
+    a.M = M;
+    a.N = N;
+    a.alpha = alpha;
+    a.tiles_n = (uint32_t)tiles_n;
+    a.ntiles = (uint32_t)(tiles_m * tiles_n);
+    a.div_tiles_n = make_fastdiv((uint32_t)tiles_n);
+    a.status = dev->status;
+    cudaStream_t s = as_stream(stream);
+    return op == Op::Scale ? dispatch<Op::Scale>(TM, TN, path, ew, a, dev, s)
+                           : dispatch<Op::Copy>(TM, TN, path, ew, a, dev, s);
+}
+
+}  // namespace
+}  // namespace libtm
+
+using namespace libtm;
+
+extern "C" tm_status tm_scale2d(const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M, int64_t N,
+                                float alpha, int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream)
+{
+    return map2d(Op::Scale, X, ldx, Y, ldy, M, N, alpha, TM, TN, flags, stream, true);
+}
+
+extern "C" tm_status tm_copy2d(const float *A, int64_t lda, float *B, int64_t ldb, int64_t M, int64_t N,
+                               int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream)
+{
+    return map2d(Op::Copy, A, lda, B, ldb, M, N, 1.0f, TM, TN, flags, stream, true);
+}
+
+extern "C" tm_status tm_scale2d_unchecked(const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M,
+                                          int64_t N, float alpha, int32_t TM, int32_t TN, tm_stream_t stream)
+{
+    return map2d(Op::Scale, X, ldx, Y, ldy, M, N, alpha, TM, TN, TM_ALIGNED, stream, false);
+}

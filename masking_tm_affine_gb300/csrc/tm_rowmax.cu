@@ -1,0 +1,180 @@
+// tm_rowmax.cu -- m[i] = max_{j < N} S[i, j] over ragged BC-column tiles.
+//
+// Source: "Slicing, bounds and masking", "Reductions over a ragged tile".  A
+// masked load reads 0, which is right for a sum and wrong for a maximum: a row
+// of negative scores padded with zeros has a maximum of 0.  The fix is a
+// second mask written with where and iota: in the column tile starting at kt,
+// the column index iota (0 .. BC-1) is kept where iota < N - kt and replaced
+// by a value no real score reaches otherwise.  That value is -inf here (the
+// page prints -1.0e30; -inf is the same for every finite score above -1e30 and
+// still correct below it).  TM_FILL_ZERO skips the where step: the foil.
+//
+// The row is walked as "Loops over a dynamic extent" splits it: the whole
+// tiles form an unmasked prefix of whole*BC columns, then the one remainder
+// tile takes the masked load and the where.  One warp per row, BR warps per
+// block, persistent grid over row blocks; a shuffle butterfly of fmaxf ends
+// the row.  max is exact and order-free, so the result equals the oracle's
+// bit for bit.
+#include "tm_host.h"
+
+namespace libtm {
+namespace {
+
+template <int BC, bool VEC, bool ALIGNED>
+__global__ void __launch_bounds__(1024, 1) rowmax_kernel(const float *__restrict__ S, int64_t lds, int64_t M,
+                                                      int64_t N, float *__restrict__ m, int BR, int fill_zero,
+                                                      unsigned *status)
+{
+    constexpr int EW = VEC ? 4 : 1;
+    constexpr int U = VEC ? 8 : 16;  // accesses in flight per lane
+    if constexpr (ALIGNED) {
+        const bool whole = (M % BR == 0) && (N % BC == 0);
+        const bool grid_ok = !VEC || ((lds % 4 == 0) && (reinterpret_cast<uintptr_t>(S) & 15) == 0);
+        if (!whole || !grid_ok) {
+            if (blockIdx.x == 0 && threadIdx.x == 0)
+                atomicOr(status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            return;
+        }
+    }
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const TileWalk walk = tile_walk(N, BC);
+    const int64_t prefix = walk.whole * BC / EW;  // accesses in the whole tiles
+    const int64_t row_blocks = (M + BR - 1) / BR;
+
+    for (int64_t rb = blockIdx.x; rb < row_blocks; rb += gridDim.x) {
+        const int64_t row = rb * BR + warp;
+        if (!ALIGNED && row >= M) continue;  // row mask (warp-uniform)
+        const float *sr = S + row * lds;
+        float mx = -INFINITY;
+
+        // whole tiles: no mask
+        int64_t v = lane;
+        for (; v + 32 * (U - 1) < prefix; v += 32 * U) {
+            uint32_t w[U][EW];
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const float *p = sr + (v + 32 * q) * EW;
+                if constexpr (VEC) {
+                    u32x4 t = ld_nc_v4(p);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                } else {
+                    w[q][0] = ld_nc_b32(p);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < U; ++q)
+#pragma unroll
+                for (int e = 0; e < EW; ++e) mx = fmaxf(mx, as_f(w[q][e]));
+        }
+        for (; v < prefix; v += 32) {
+            const float *p = sr + v * EW;
+            if constexpr (VEC) {
+                u32x4 t = ld_nc_v4(p);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx = fmaxf(mx, as_f(t.v[e]));
+            } else {
+                mx = fmaxf(mx, as_f(ld_nc_b32(p)));
+            }
+        }
+
+        // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
+        if (!ALIGNED && walk.masked) {
+            const int64_t kt = walk.whole * BC;
+            for (int iota = lane * EW; iota < BC; iota += 32 * EW) {
+                const int64_t j = kt + iota;
+                float s[EW];
+                if constexpr (VEC) {
+                    u32x4 t = {{0u, 0u, 0u, 0u}};
+                    if (j < N) t = ld_nc_v4(sr + j);  // N % 4 == 0: a vector is wholly in or out
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[e] = as_f(t.v[e]);
+                } else {
+                    s[0] = j < N ? as_f(ld_nc_b32(sr + j)) : 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < EW; ++e) {
+                    if (!fill_zero) s[e] = (iota + e < N - kt) ? s[e] : -INFINITY;
+                    mx = fmaxf(mx, s[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) m[row] = mx;
+    }
+}
+
+template <int BC>
+tm_status launch(bool vec, bool aligned, const float *S, int64_t lds, int64_t M, int64_t N, float *m, int BR,
+                 int fill_zero, const DevInfo *dev, cudaStream_t s)
+{
+    const void *k;
+    if (vec) k = aligned ? (const void *)rowmax_kernel<BC, true, true> : (const void *)rowmax_kernel<BC, true, false>;
+    else k = aligned ? (const void *)rowmax_kernel<BC, false, true> : (const void *)rowmax_kernel<BC, false, false>;
+    const int threads = 32 * BR;
+    const int64_t grid = persistent_grid(dev, k, (M + BR - 1) / BR, 0, threads);
+    unsigned *status = dev->status;
+    void *args[] = {(void *)&S, (void *)&lds, (void *)&M, (void *)&N, (void *)&m,
+                    (void *)&BR, (void *)&fill_zero, (void *)&status};
+    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(threads), args, 0, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
+}  // namespace
+}  // namespace libtm
+
+using namespace libtm;
+
+extern "C" tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N, float *m, int32_t BR,
+                                      int32_t BC, tm_fill fill, uint32_t flags, tm_stream_t stream)
+{
+    if (!valid2d(S, lds, M, N)) return TM_ERR_INVALID_ARG;
+    if (M > 0 && m == nullptr) return TM_ERR_INVALID_ARG;
+    if (fill != TM_FILL_NEG_INF && fill != TM_FILL_ZERO) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
+    if (!(BR == 1 || BR == 2 || BR == 4 || BR == 8 || BR == 16 || BR == 32)) return TM_ERR_UNSUPPORTED_TILE;
+    if (!(BC == 16 || BC == 32 || BC == 64 || BC == 128 || BC == 256 || BC == 512)) return TM_ERR_UNSUPPORTED_TILE;
+    if (M > 0 && !aligned_to(m, 4)) return TM_ERR_MISALIGNED;
+    if (M > 0 && N > 0 && !aligned_to(S, 4)) return TM_ERR_MISALIGNED;
+    if (M > 0 && N > 0) {
+        uintptr_t slo, shi, mlo = reinterpret_cast<uintptr_t>(m), mhi = mlo + (uintptr_t)M * 4;
+        span2d(S, lds, M, N, &slo, &shi);
+        if (!(shi <= mlo || mhi <= slo)) return TM_ERR_INVALID_ARG;
+    }
+    const bool vec16 = aligned_to(S, 16) && lds % 4 == 0;
+    const bool aligned = (flags & TM_ALIGNED) != 0;
+    bool vec;
+    if (aligned) {
+        if (!vec16 && !(flags & TM_PATH_SCALAR)) return TM_ERR_MISALIGNED;
+        if (M % BR != 0 || N % BC != 0) return TM_ERR_BROKEN_PROMISE;
+        vec = !(flags & TM_PATH_SCALAR);
+    } else if (flags & TM_PATH_SCALAR) {
+        vec = false;
+    } else if (vec16 && N % 4 == 0) {
+        vec = true;
+    } else if (flags & TM_PATH_VEC) {
+        return TM_ERR_MISALIGNED;
+    } else {
+        vec = false;
+    }
+    if (M == 0) return TM_OK;
+
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    const int fz = fill == TM_FILL_ZERO ? 1 : 0;
+    switch (BC) {
+    case 16: return launch<16>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    case 32: return launch<32>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    case 64: return launch<64>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    case 128: return launch<128>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    case 256: return launch<256>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    default: return launch<512>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    }
+}

@@ -1,0 +1,176 @@
+"""Thin ctypes binding of ``libtm.so`` (declared in ``include/tm.h``).
+
+Argument marshalling only: every entry point keeps its C name and argument
+order; pointers may be given as integers or as objects with ``data_ptr()``
+(torch tensors); ``stream=None`` means torch's current CUDA stream when torch
+is loaded, else the legacy default stream.  A non-OK status raises
+``TmError`` (its ``.status`` holds the code).  There is no fallback: if the
+library was not built this module raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import sys
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libtm.so")
+
+# status codes (tm_status)
+TM_OK = 0
+TM_ERR_INVALID_ARG = 1
+TM_ERR_UNSUPPORTED_TILE = 2
+TM_ERR_MISALIGNED = 3
+TM_ERR_BROKEN_PROMISE = 4
+TM_ERR_CUDA = 5
+TM_ERR_WORKSPACE = 6
+TM_ERR_TIMEOUT = 7
+
+# flags
+TM_ALIGNED = 0x1
+TM_PATH_SCALAR = 0x10
+TM_PATH_VEC = 0x20
+TM_PATH_TMA = 0x40
+
+# tm_variant
+TM_VAR_AUTO = 0
+TM_VAR_SCALAR = 1
+TM_VAR_VEC_UNALIGNED = 2
+TM_VAR_VEC4 = 3
+TM_VAR_VEC8 = 4
+TM_VAR_NAIVE = 5
+TM_VAR_STAGED = 6
+TM_VAR_REGDIRECT = 7
+
+# tm_fill
+TM_FILL_NEG_INF = 0
+TM_FILL_ZERO = 1
+
+# Every function include/tm.h declares, with its ctypes signature.
+_i64, _i32, _u32, _f32, _vp, _sz = (ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
+                                    ctypes.c_void_p, ctypes.c_size_t)
+_st = ctypes.c_int
+SIGNATURES = {
+    "tm_status_string": (ctypes.c_char_p, [_st]),
+    "tm_version": (ctypes.c_int, []),
+    "tm_affine": (_st, [_vp, _vp, _i64, _st, _vp]),
+    "tm_scale2d": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _u32, _vp]),
+    "tm_copy2d": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _i32, _i32, _u32, _vp]),
+    "tm_rowsum": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _u32, _vp]),
+    "tm_colsum_workspace_bytes": (_sz, [_i64, _i64, _i32, _i32, _st]),
+    "tm_colsum": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _sz, _i32, _i32, _st, _u32, _vp]),
+    "tm_rowmax_masked": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
+    "tm_check": (_st, [_vp]),
+    "tm_tile_walk_probe": (_st, [_i64, _i32, _vp, _vp]),
+    "tm_scale2d_unchecked": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class TmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtm.so (once) and attach the signatures; raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError("libtm.so is not built (%s); run "
+                                   "`python -m masking_tm_affine_gb300.build`" % path)
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        torch = sys.modules.get("torch")
+        if torch is not None and torch.cuda.is_available() and torch.cuda.is_initialized():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _ok(st: int, where: str) -> None:
+    if st != TM_OK:
+        raise TmError(st, where)
+
+
+def status_string(st: int) -> str:
+    return load().tm_status_string(st).decode()
+
+
+def tm_version() -> int:
+    return load().tm_version()
+
+
+def tm_affine(a, out, n: int, variant: int = TM_VAR_AUTO, stream=None) -> None:
+    _ok(load().tm_affine(_ptr(a), _ptr(out), n, variant, _stream(stream)), "tm_affine")
+
+
+def tm_scale2d(X, ldx: int, Y, ldy: int, M: int, N: int, alpha: float, TM: int, TN: int,
+               flags: int = 0, stream=None) -> None:
+    _ok(load().tm_scale2d(_ptr(X), ldx, _ptr(Y), ldy, M, N, alpha, TM, TN, flags, _stream(stream)),
+        "tm_scale2d")
+
+
+def tm_copy2d(A, lda: int, B, ldb: int, M: int, N: int, TM: int, TN: int, flags: int = 0,
+              stream=None) -> None:
+    _ok(load().tm_copy2d(_ptr(A), lda, _ptr(B), ldb, M, N, TM, TN, flags, _stream(stream)), "tm_copy2d")
+
+
+def tm_rowsum(X, ldx: int, M: int, N: int, r, TM: int = 8, TN: int = 512, flags: int = 0,
+              stream=None) -> None:
+    _ok(load().tm_rowsum(_ptr(X), ldx, M, N, _ptr(r), TM, TN, flags, _stream(stream)), "tm_rowsum")
+
+
+def tm_colsum_workspace_bytes(M: int, N: int, TM: int = 32, TN: int = 128,
+                              variant: int = TM_VAR_AUTO) -> int:
+    return int(load().tm_colsum_workspace_bytes(M, N, TM, TN, variant))
+
+
+def tm_colsum(X, ldx: int, M: int, N: int, c, workspace, ws_bytes: int, TM: int = 32, TN: int = 128,
+              variant: int = TM_VAR_AUTO, flags: int = 0, stream=None) -> None:
+    _ok(load().tm_colsum(_ptr(X), ldx, M, N, _ptr(c), _ptr(workspace), ws_bytes, TM, TN, variant, flags,
+                         _stream(stream)), "tm_colsum")
+
+
+def tm_rowmax_masked(S, lds: int, M: int, N: int, m, BR: int = 8, BC: int = 64,
+                     fill: int = TM_FILL_NEG_INF, flags: int = 0, stream=None) -> None:
+    _ok(load().tm_rowmax_masked(_ptr(S), lds, M, N, _ptr(m), BR, BC, fill, flags, _stream(stream)),
+        "tm_rowmax_masked")
+
+
+def tm_check(stream=None) -> None:
+    _ok(load().tm_check(_stream(stream)), "tm_check")
+
+
+def tm_tile_walk_probe(K: int, T: int, out4, stream=None) -> None:
+    _ok(load().tm_tile_walk_probe(K, T, _ptr(out4), _stream(stream)), "tm_tile_walk_probe")
+
+
+def tm_scale2d_unchecked(X, ldx: int, Y, ldy: int, M: int, N: int, alpha: float, TM: int, TN: int,
+                         stream=None) -> None:
+    _ok(load().tm_scale2d_unchecked(_ptr(X), ldx, _ptr(Y), ldy, M, N, alpha, TM, TN, _stream(stream)),
+        "tm_scale2d_unchecked")

@@ -1,0 +1,121 @@
+"""The C-ABI library loads, exports every symbol include/tm.h declares, and
+rejects bad arguments on the host before touching CUDA (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from masking_tm_affine_gb300 import tm
+
+HEADER = os.path.join(ROOT, "include", "tm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tm_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from masking_tm_affine_gb300 import build
+    build.build()
+    return tm.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["tm_affine", "tm_scale2d", "tm_copy2d", "tm_rowsum", "tm_colsum", "tm_colsum_workspace_bytes",
+              "tm_rowmax_masked", "tm_check", "tm_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(tm.SIGNATURES), "binding and header disagree"
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    for code in range(0, 8):
+        s = tm.status_string(code)
+        assert s.startswith("TM_")
+    assert tm.status_string(99) == "TM_ERR_UNKNOWN"
+    assert tm.tm_version() >= 10000
+
+
+# Fake but well-aligned device addresses: every case below must be rejected on
+# the host, before any CUDA call, so nothing ever dereferences them.
+P0, P1 = 0x7F0000000000, 0x7F0100000000
+
+
+def st(fn, *args):
+    return getattr(tm.load(), fn)(*args)
+
+
+def test_affine_host_validation(lib):
+    assert st("tm_affine", P0, P1, -1, 0, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_affine", None, P1, 5, 0, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_affine", P0, P1, 5, 99, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_affine", P0 + 4, P1, 5, tm.TM_VAR_VEC4, None) == tm.TM_ERR_MISALIGNED
+    assert st("tm_affine", P0 + 16, P1, 5, tm.TM_VAR_VEC8, None) == tm.TM_ERR_MISALIGNED
+    assert st("tm_affine", P0 + 2, P1, 5, 0, None) == tm.TM_ERR_MISALIGNED
+    assert st("tm_affine", P0, P0 + 8, 5, 0, None) == tm.TM_ERR_INVALID_ARG  # partial overlap
+    assert st("tm_affine", P0, P1, 0, 0, None) == tm.TM_OK                   # empty: no launch
+
+
+@pytest.mark.parametrize("fn", ["tm_scale2d", "tm_copy2d"])
+def test_map2d_host_validation(lib, fn):
+    def call(X, ldx, Y, ldy, M, N, TM, TN, flags):
+        if fn == "tm_scale2d":
+            return st(fn, X, ldx, Y, ldy, M, N, 1.5, TM, TN, flags, None)
+        return st(fn, X, ldx, Y, ldy, M, N, TM, TN, flags, None)
+    A = tm.TM_ALIGNED
+    assert call(P0, 8, P1, 8, -1, 8, 32, 128, 0) == tm.TM_ERR_INVALID_ARG
+    assert call(P0, 7, P1, 8, 4, 8, 32, 128, 0) == tm.TM_ERR_INVALID_ARG        # ld < N
+    assert call(None, 8, P1, 8, 4, 8, 32, 128, 0) == tm.TM_ERR_INVALID_ARG
+    assert call(P0, 8, P1, 8, 4, 8, 32, 128, 0x8) == tm.TM_ERR_INVALID_ARG      # unknown flag
+    assert call(P0, 8, P1, 8, 4, 8, 32, 128, tm.TM_PATH_SCALAR | tm.TM_PATH_VEC) == tm.TM_ERR_INVALID_ARG
+    assert call(P0, 8, P1, 8, 4, 8, 0, 128, 0) == tm.TM_ERR_UNSUPPORTED_TILE    # divisor must be positive
+    assert call(P0, 8, P1, 8, 4, 8, 32, 64, 0) == tm.TM_ERR_UNSUPPORTED_TILE    # not instantiated
+    assert call(P0, 8192, P1, 8192, 8192, 8100, 32, 128, A) == tm.TM_ERR_BROKEN_PROMISE
+    assert call(P0, 8192, P1, 8192, 8190, 8192, 32, 128, A) == tm.TM_ERR_BROKEN_PROMISE
+    assert call(P0 + 4, 8192, P1, 8192, 8192, 8192, 32, 128, A) == tm.TM_ERR_MISALIGNED
+    assert call(P0, 8190, P1, 8192, 64, 128, 32, 128, A) == tm.TM_ERR_MISALIGNED  # ld % 4 != 0
+    assert call(P0, 8, P0 + 8, 8, 4, 8, 8, 8, 0) == tm.TM_ERR_INVALID_ARG         # partial overlap
+    assert call(P0, 8, P0, 12, 4, 8, 8, 8, 0) == tm.TM_ERR_INVALID_ARG            # same base, other ld
+    assert call(P0, 8, P1, 8, 0, 8, 8, 8, 0) == tm.TM_OK                          # empty
+    assert call(P0, 8, P1, 8, 4, 0, 8, 8, 0) == tm.TM_OK
+
+
+def test_reduction_host_validation(lib):
+    A = tm.TM_ALIGNED
+    assert st("tm_rowsum", P0, 8, 4, 8, P1, 3, 128, 0, None) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert st("tm_rowsum", P0, 8, 4, 8, P1, 8, 100, 0, None) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert st("tm_rowsum", P0, 8, 4, 8, None, 8, 128, 0, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_rowsum", P0, 4096, 4096, 4000, P1, 8, 512, A, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_rowmax_masked", P0, 1000, 8192, 1000, P1, 8, 64, 0, A, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_rowmax_masked", P0, 1000, 8192, 1000, P1, 8, 64, 7, 0, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_rowmax_masked", P0, 1000, 8192, 1000, P1, 8, 48, 0, 0, None) == tm.TM_ERR_UNSUPPORTED_TILE
+    ws = tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128)
+    assert ws > 0 and ws % 16 == 0
+    assert st("tm_colsum", P0, 4096, 4096, 4096, P1, None, ws, 32, 128, 0, 0, None) == tm.TM_ERR_WORKSPACE
+    assert st("tm_colsum", P0, 4096, 4096, 4096, P1, P1 + (1 << 30), ws - 4, 32, 128, 0, 0, None) \
+        == tm.TM_ERR_WORKSPACE
+    assert st("tm_colsum", P0, 4096, 4096, 4096, P1, P1 + (1 << 30), ws, 32, 96, 0, 0, None) \
+        == tm.TM_ERR_UNSUPPORTED_TILE
+    assert st("tm_colsum", P0, 4096, 4096, 4000, P1, P1 + (1 << 30), ws, 32, 128, 0, A, None) \
+        == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_tile_walk_probe", 10, 0, P0, None) == tm.TM_ERR_INVALID_ARG
+
+
+def test_colsum_workspace_plan(lib):
+    # one partial row per chunk; NAIVE: one per 256-row program block
+    assert tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128, tm.TM_VAR_NAIVE) == 16 * 4096 * 4
+    assert tm.tm_colsum_workspace_bytes(0, 4096, 32, 128) == 0
+    assert tm.tm_colsum_workspace_bytes(100, 0, 32, 128) == 0
+    assert tm.tm_colsum_workspace_bytes(100, 10, 33, 128) == 0
+    w = tm.tm_colsum_workspace_bytes(4100, 1001, 32, 128)
+    assert w % (1004 * 4) == 0      # rows padded to a multiple of 4 columns

@@ -1,0 +1,36 @@
+"""The device-side tile-walk planner every kernel uses, read back through
+tm_tile_walk_probe, against the page's worked example and the closed form
+("Slicing, bounds and masking", "Loops over a dynamic extent")."""
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden
+from masking_tm_affine_gb300 import tm
+
+pytestmark = pytest.mark.gpu
+
+
+def probe(K, T):
+    out = torch.zeros(4, dtype=torch.int64, device="cuda")
+    tm.tm_tile_walk_probe(K, T, out)
+    tm.tm_check()
+    return [int(v) for v in out.cpu()]
+
+
+def test_probe_printed_example(cuda):
+    (row,) = read_golden("tile_walk.txt")
+    K, T, whole, masked, rem = map(int, row)
+    assert probe(K, T) == [whole, masked, rem, whole + masked]
+
+
+def test_probe_closed_form_sweep(cuda):
+    for K in list(range(0, 70)) + [1000, 4096, 4100, 2**31 + 5, 2**40 + 3]:
+        for T in [1, 3, 16, 40, 64, 128, 512]:
+            w = probe(K, T)
+            assert w == [K // T, 1 if K % T else 0, K % T, -(-K // T)], (K, T)
+
+
+def test_check_clean(cuda):
+    tm.tm_check()
+    assert np.isfinite(1.0)
