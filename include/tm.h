@@ -211,6 +211,31 @@ tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N, fl
                            int32_t BC, tm_fill fill, uint32_t flags, tm_stream_t stream);
 
 /*
+ * tm_colsum_noalloc -- tm_colsum for callers that cannot allocate device
+ * memory (no counterpart in the pages: a convenience of this library).  Code
+ * running inside another framework that owns all device memory, under a fixed
+ * memory budget, or on a path where cudaMalloc's implicit device-wide
+ * synchronization is not allowed can still take column sums: the partial sums
+ * live in a static device array of TM_NOALLOC_SCRATCH_BYTES that the library
+ * holds on every GPU that loads it, for the life of the process.  This call
+ * allocates nothing and calls no allocating routine.
+ *   Same arguments, variants, flags, results and errors as tm_colsum, minus
+ *   the workspace.  Returns TM_ERR_WORKSPACE (nothing launched) when the
+ *   arguments need more scratch than TM_NOALLOC_SCRATCH_BYTES, i.e. when
+ *   tm_colsum_workspace_bytes(M, N, TM, TN, variant) exceeds it.
+ *   The first call on each device (with M, N > 0) looks up the array's device
+ *   address with cudaGetSymbolAddress while that device is current; make that
+ *   first call before any stream capture.
+ *   All calls share the one array: calls whose kernels may overlap on the GPU
+ *   (different streams, no ordering between them) race and give wrong sums;
+ *   serialize them.  The array keeps the last call's partial sums; every word
+ *   a call reads it wrote first, so no clearing is needed.
+ */
+#define TM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20) /* 4 MiB per device */
+tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, int32_t TM,
+                            int32_t TN, tm_variant variant, uint32_t flags, tm_stream_t stream);
+
+/*
  * tm_check -- synchronize `stream`, then read and clear this device's status
  * word.  Returns TM_ERR_BROKEN_PROMISE if a kernel's entry check found the
  * aligned promise broken (that kernel stored nothing), TM_ERR_MISALIGNED if it

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "tm_host.h"
@@ -602,4 +603,70 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
         if (st != TM_OK) return st;
     }
     return launch_finish(part, npad, P, N, c, dev, s);
+}
+
+// ------------------------------------------------------------------ no-allocation entry point
+// Some callers cannot allocate device memory at the point where they need a
+// column sum: code hosted inside another framework whose allocator owns every
+// device byte, loops with a fixed memory budget that must not fail with
+// out-of-memory halfway through, or latency-critical paths where cudaMalloc
+// (which may synchronize the whole device) is not allowed.  For them
+// tm_colsum_noalloc keeps the partial sums in this file-scope array instead of
+// a caller-provided workspace.  Every GPU that loads the library holds the
+// array until the process exits.
+namespace libtm {
+namespace {
+
+static __device__ __align__(256) float g_colsum_scratch[TM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+struct ScratchSlot {
+    std::atomic<bool> ready{false};
+    void *addr = nullptr;
+};
+ScratchSlot g_scratch_slots[kMaxDevices];
+std::mutex g_scratch_mu;
+
+// Device address of g_colsum_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the real address is asked of
+// the runtime once per device, with that device current.
+tm_status scratch_address(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    ScratchSlot &s = g_scratch_slots[dev];
+    if (!s.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!s.ready.load(std::memory_order_relaxed)) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_colsum_scratch) != cudaSuccess || p == nullptr) {
+                cudaGetLastError();
+                return TM_ERR_CUDA;
+            }
+            s.addr = p;
+            s.ready.store(true, std::memory_order_release);
+        }
+    }
+    *out = s.addr;
+    return TM_OK;
+}
+
+}  // namespace
+}  // namespace libtm
+
+extern "C" tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, int32_t TM,
+                                       int32_t TN, tm_variant variant, uint32_t flags, tm_stream_t stream)
+{
+    const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant == TM_VAR_NAIVE ? TM_VAR_NAIVE : TM_VAR_AUTO);
+    if (need > TM_NOALLOC_SCRATCH_BYTES) return TM_ERR_WORKSPACE;  // beyond the built-in scratch
+    void *scratch = nullptr;
+    if (M > 0 && N > 0) {
+        const tm_status st = scratch_address(&scratch);
+        if (st != TM_OK) return st;
+    }
+    // Every partial-sum word the second pass reads is written earlier in the
+    // same call, so the array's leftover contents never need clearing.
+    return tm_colsum(X, ldx, M, N, c, scratch, TM_NOALLOC_SCRATCH_BYTES, TM, TN, variant, flags, stream);
 }

@@ -61,6 +61,7 @@ SIGNATURES = {
     "tm_colsum_workspace_bytes": (_sz, [_i64, _i64, _i32, _i32, _st]),
     "tm_colsum": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _sz, _i32, _i32, _st, _u32, _vp]),
     "tm_rowmax_masked": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
+    "tm_colsum_noalloc": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
     "tm_check": (_st, [_vp]),
     "tm_tile_walk_probe": (_st, [_i64, _i32, _vp, _vp]),
     "tm_scale2d_unchecked": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
@@ -154,6 +155,17 @@ def tm_colsum(X, ldx: int, M: int, N: int, c, workspace, ws_bytes: int, TM: int 
               variant: int = TM_VAR_AUTO, flags: int = 0, stream=None) -> None:
     _ok(load().tm_colsum(_ptr(X), ldx, M, N, _ptr(c), _ptr(workspace), ws_bytes, TM, TN, variant, flags,
                          _stream(stream)), "tm_colsum")
+
+
+TM_NOALLOC_SCRATCH_BYTES = 4 << 20  # include/tm.h
+
+
+def tm_colsum_noalloc(X, ldx: int, M: int, N: int, c, TM: int = 32, TN: int = 128,
+                      variant: int = TM_VAR_AUTO, flags: int = 0, stream=None) -> None:
+    """tm_colsum without a workspace, for callers that cannot allocate device
+    memory; see include/tm.h for the scratch limit and the concurrency rule."""
+    _ok(load().tm_colsum_noalloc(_ptr(X), ldx, M, N, _ptr(c), TM, TN, variant, flags, _stream(stream)),
+        "tm_colsum_noalloc")
 
 
 def tm_rowmax_masked(S, lds: int, M: int, N: int, m, BR: int = 8, BC: int = 64,
