@@ -7,9 +7,9 @@ One step is one pass of the whole hot path over one batch: the fp32
   affine      out = X*2 + 1 over all 67,108,864 elements (1-D, widest vectors)
   scale2d     Y = 1.5*X, 32 x 128 tiles, aligned promise
   copy2d      B = X, 64 x 64 tiles, aligned promise
-  rowsum      r = sum over each row (8 rows per block, 512-column tiles)
-  colsum      c = sum over each column (32 x 128 strips, AUTO = TMA-staged)
-  rowmax      m = ragged row max, 64-column tiles, -inf fill
+  rowsum      r = sum over each row (a block per row, 1024-column tiles)
+  colsum      c = sum over each column (32 x 128 strips, AUTO variant)
+  rowmax      m = ragged row max (a block per row), 64-column tiles, -inf fill
 
 Metric: achieved HBM GB/s (GB = 1e9 bytes, the pages' convention) over the
 algorithmic bytes (each input byte read once, each output byte written once),
@@ -40,6 +40,9 @@ M = N = 8192
 ALPHA = 1.5
 FALLBACK_HBM_GBS = 6800.0
 STEP_LAUNCHES = 7  # affine, scale2d, copy2d, rowsum, colsum (partials + finish), rowmax
+ROWSUM_TILE = (1, 1024)   # rows per block x columns per tile
+COLSUM_TILE = (32, 128)   # row tile x column strip
+ROWMAX_BR = 1             # rows per block (column tile BC = 64)
 
 
 def gbps(nbytes: int, seconds: float) -> float:
@@ -169,17 +172,39 @@ def make_step(tm, bufs, ws_bytes, stream):
         ("affine", lambda: tm.tm_affine(X, A1, M * N, tm.TM_VAR_AUTO, s)),
         ("scale2d", lambda: tm.tm_scale2d(X, N, Y, N, M, N, ALPHA, 32, 128, tm.TM_ALIGNED, s)),
         ("copy2d", lambda: tm.tm_copy2d(X, N, B, N, M, N, 64, 64, tm.TM_ALIGNED, s)),
-        ("rowsum", lambda: tm.tm_rowsum(X, N, M, N, r, 8, 512, tm.TM_ALIGNED, s)),
-        ("colsum", lambda: tm.tm_colsum(X, N, M, N, c, W, ws_bytes, 32, 128, tm.TM_VAR_AUTO, tm.TM_ALIGNED, s)),
-        ("rowmax_masked", lambda: tm.tm_rowmax_masked(X, N, M, N, m, 8, 64, tm.TM_FILL_NEG_INF, tm.TM_ALIGNED, s)),
+        ("rowsum", lambda: tm.tm_rowsum(X, N, M, N, r, *ROWSUM_TILE, tm.TM_ALIGNED, s)),
+        ("colsum", lambda: tm.tm_colsum(X, N, M, N, c, W, ws_bytes, *COLSUM_TILE, tm.TM_VAR_AUTO, tm.TM_ALIGNED, s)),
+        ("rowmax_masked", lambda: tm.tm_rowmax_masked(X, N, M, N, m, ROWMAX_BR, 64, tm.TM_FILL_NEG_INF,
+                                                      tm.TM_ALIGNED, s)),
     ]
 
 
-def verify_step(bufs, x, oracle):
-    """Sampled parity at full size (the oracle computes the sampled outputs one
-    by one): 64 rows of every output, and every column sum."""
+def make_buffers(tm, x, dev):
+    """Device buffers of one step over the batch x ([M, N] fp32 on the host)."""
+    import torch
+    bufs = {
+        "X": torch.from_numpy(x.reshape(-1)).to(dev),
+        "A1": torch.empty(M * N, dtype=torch.float32, device=dev),
+        "Y": torch.empty(M * N, dtype=torch.float32, device=dev),
+        "B": torch.empty(M * N, dtype=torch.float32, device=dev),
+        "r": torch.empty(M, dtype=torch.float32, device=dev),
+        "c": torch.empty(N, dtype=torch.float32, device=dev),
+        "m": torch.empty(M, dtype=torch.float32, device=dev),
+    }
+    ws_bytes = tm.tm_colsum_workspace_bytes(M, N, *COLSUM_TILE)
+    bufs["W"] = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+    return bufs, ws_bytes
+
+
+def verify_step(bufs, x, oracle, rows=None):
+    """Parity of one step at full size against the oracle: the given rows of
+    every output (default 64 rows spread over the batch; `rows="all"` for
+    every row), and every column sum."""
     import numpy as np
-    rows = np.linspace(0, M - 1, 64).astype(np.int64)
+    if rows is None:
+        rows = np.linspace(0, M - 1, 64).astype(np.int64)
+    elif isinstance(rows, str):
+        rows = np.arange(M, dtype=np.int64)
     xs = x[rows]
     A1 = bufs["A1"].view(M, N)[rows].cpu().numpy()
     Y = bufs["Y"].view(M, N)[rows].cpu().numpy()
@@ -188,7 +213,9 @@ def verify_step(bufs, x, oracle):
     want = np.zeros_like(xs)
     oracle.scale2d(xs, N, want, N, len(rows), N, ALPHA)
     assert np.array_equal(Y.view(np.uint32), want.view(np.uint32)), "scale2d"
-    assert np.array_equal(B.view(np.uint32), xs.view(np.uint32)), "copy2d"
+    want_b = np.zeros(xs.size, dtype=np.uint32)
+    oracle.copy2d(xs, N, want_b, N, len(rows), N)
+    assert np.array_equal(B.view(np.uint32).reshape(-1), want_b), "copy2d"
     r = bufs["r"].cpu().numpy()[rows]
     rw = oracle.rowsum(xs, N, len(rows), N)
     assert np.all(np.abs(r - rw) <= 1e-5 * oracle.rowsum(np.abs(xs), N, len(rows), N)), "rowsum"
@@ -257,17 +284,7 @@ def run_gpu(args):
     tm.load()
 
     x = synth.workload_input(WORKLOAD)
-    bufs = {
-        "X": torch.from_numpy(x.reshape(-1)).to(dev),
-        "A1": torch.empty(M * N, dtype=torch.float32, device=dev),
-        "Y": torch.empty(M * N, dtype=torch.float32, device=dev),
-        "B": torch.empty(M * N, dtype=torch.float32, device=dev),
-        "r": torch.empty(M, dtype=torch.float32, device=dev),
-        "c": torch.empty(N, dtype=torch.float32, device=dev),
-        "m": torch.empty(M, dtype=torch.float32, device=dev),
-    }
-    ws_bytes = tm.tm_colsum_workspace_bytes(M, N, 32, 128)
-    bufs["W"] = torch.empty(max(ws_bytes // 4, 4), dtype=torch.float32, device=dev)
+    bufs, ws_bytes = make_buffers(tm, x, dev)
     stream = torch.cuda.Stream(device=dev)
     step = make_step(tm, bufs, ws_bytes, stream)
     names = [n for n, _ in step]
@@ -313,7 +330,7 @@ def run_gpu(args):
 
     # end to end through the C ABI: pinned host X in, every output back to pinned host memory
     e2e = None
-    if rank == 0:
+    if rank == 0 and args.e2e_steps > 0:
         e2e = run_e2e(tm, bufs, x, step, stream, dev, min(args.steps, args.e2e_steps), step_bytes)
 
     if rank != 0:
@@ -344,8 +361,9 @@ def run_gpu(args):
         "data": "synthetic: numpy PCG64, X ~ N(0,1) seed 1, rounded once to fp32",
         "config": {
             "workload": "scale_8192: fp32 [8192,8192] X~N(0,1) seed 1; one step = affine(1-D, all elements) + "
-                        "scale2d(alpha 1.5, 32x128, aligned) + copy2d(64x64, aligned) + rowsum(8x512) + "
-                        "colsum(32x128, AUTO) + rowmax_masked(8x64, -inf fill)",
+                        "scale2d(alpha 1.5, 32x128, aligned) + copy2d(64x64, aligned) + rowsum(%dx%d) + "
+                        "colsum(%dx%d, AUTO) + rowmax_masked(%dx64, -inf fill)"
+                        % (ROWSUM_TILE + COLSUM_TILE + (ROWMAX_BR,)),
             "M": M, "N": N, "step_bytes": step_bytes,
             "l2": "inputs larger than L2 (X 256 MiB, each output 256 MiB vs 126 MB L2); no flush between steps",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -368,7 +386,6 @@ def run_gpu(args):
 
 def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes):
     import torch
-    steps = max(steps, 3)
     hx = torch.from_numpy(x.reshape(-1)).pin_memory()
     outs = ["A1", "Y", "B", "r", "c", "m"]
     host = {k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs}
@@ -497,6 +514,108 @@ def run_sweep(args):
     return out
 
 
+# --------------------------------------------------------------------- single-workload cases
+CASES = {
+    # name: (workload, kernel, variants) -- variants[0] is the default
+    "affine_1m": ("affine_1m", "affine", ["auto", "scalar", "vec_unaligned", "vec4", "vec8"]),
+    "scale_8192": ("scale_8192", "scale2d", ["aligned", "ragged_vec", "scalar"]),
+    "ragged_copy": ("ragged_4100", "copy2d", ["auto", "scalar"]),
+    "ragged_scale": ("ragged_4100", "scale2d", ["auto", "scalar"]),
+    "rowsum_4096": ("coalesce_4096", "rowsum", ["vec", "scalar"]),
+    "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive"]),
+    "rowmax_8192": ("rowmax_8192", "rowmax_masked", ["neg_inf", "zero", "scalar"]),
+    # the reductions on the [8192, 8192] batch of the step, for tile tuning
+    "rowsum_8192sq": ("scale_8192", "rowsum", ["vec"]),
+    "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect"]),
+    "rowmax_8192sq": ("scale_8192", "rowmax_masked", ["neg_inf"]),
+}
+
+
+def run_cases(args):
+    """Time one kernel on one workload: median of CUDA-event times over
+    --reps launches, L2 flushed (a 512 MiB write) before every launch."""
+    import torch
+
+    from masking_tm_affine_gb300 import synth, tm
+    tm.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, _ = measured_peak()
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    names = list(CASES) if args.case == "all" else [args.case]
+    out = []
+    for name in names:
+        wl, kern, variants = CASES[name]
+        w = synth.WORKLOADS[wl]
+        x = synth.workload_input(wl)
+        X = torch.from_numpy(x.reshape(-1)).to(dev)
+        if kern == "affine":
+            n = x.size
+            O = torch.empty_like(X)
+            vmap = {"auto": tm.TM_VAR_AUTO, "scalar": tm.TM_VAR_SCALAR, "vec_unaligned": tm.TM_VAR_VEC_UNALIGNED,
+                    "vec4": tm.TM_VAR_VEC4, "vec8": tm.TM_VAR_VEC8}
+            nbytes = 8 * n
+            mk = lambda v: (lambda: tm.tm_affine(X, O, n, vmap[v], s))
+        else:
+            Mw, Nw = w["M"], w["N"]
+            tile = tuple(int(t) for t in args.tile.split("x")) if args.tile else None
+            if kern in ("scale2d", "copy2d"):
+                O = torch.empty_like(X)
+                nbytes = 8 * Mw * Nw
+                TM_, TN_ = tile or (w["TM"], w["TN"])
+                fl = {"aligned": tm.TM_ALIGNED, "ragged_vec": 0, "auto": 0, "scalar": tm.TM_PATH_SCALAR}
+                if kern == "scale2d":
+                    mk = lambda v: (lambda: tm.tm_scale2d(X, Nw, O, Nw, Mw, Nw, ALPHA, TM_, TN_, fl[v], s))
+                else:
+                    mk = lambda v: (lambda: tm.tm_copy2d(X, Nw, O, Nw, Mw, Nw, TM_, TN_, fl[v], s))
+            elif kern == "rowsum":
+                O = torch.empty(Mw, dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw + 4 * Mw
+                fl = {"vec": 0, "scalar": tm.TM_PATH_SCALAR}
+                RT_, RN_ = tile or ROWSUM_TILE
+                mk = lambda v: (lambda: tm.tm_rowsum(X, Nw, Mw, Nw, O, RT_, RN_, fl[v], s))
+            elif kern == "colsum":
+                O = torch.empty(Nw, dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw + 4 * Nw
+                vm = {"auto": tm.TM_VAR_AUTO, "staged": tm.TM_VAR_STAGED, "regdirect": tm.TM_VAR_REGDIRECT,
+                      "naive": tm.TM_VAR_NAIVE}
+                CT_, CN_ = tile or COLSUM_TILE
+                ws = max(tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_NAIVE),
+                         tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_AUTO))
+                Wt = torch.empty(ws // 4, dtype=torch.float32, device=dev)
+                mk = lambda v: (lambda: tm.tm_colsum(X, Nw, Mw, Nw, O, Wt, ws, CT_, CN_, vm[v], 0, s))
+            else:
+                O = torch.empty(Mw, dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw + 4 * Mw
+                fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
+                      "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
+                BR_, BC_ = tile or (ROWMAX_BR, w.get("BC", 64))
+                mk = lambda v: (lambda: tm.tm_rowmax_masked(X, Nw, Mw, Nw, O, BR_, BC_, fm[v][0], fm[v][1], s))
+        chosen = variants if args.variant == "all" else [args.variant or variants[0]]
+        for v in chosen:
+            fn = mk(v)
+            ts = []
+            for rep in range(args.reps + 3):
+                if not args.no_flush:
+                    flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                if rep >= 3:
+                    ts.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(ts)
+            out.append({"case": name, "kernel": kern, "variant": v, "tile": args.tile, "bytes": nbytes, "us": round(t * 1e6, 2),
+                        "GBps": round(gbps(nbytes, t), 1), "frac": round(gbps(nbytes, t) / peak, 4),
+                        "reps": args.reps, "l2": "flushed before each launch" if not args.no_flush else "warm"})
+        del X, O
+    tm.tm_check()
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,9 +627,18 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
+    ap.add_argument("--case", help="time one kernel on one workload instead (%s, or all)" % ", ".join(CASES))
+    ap.add_argument("--variant", help="variant of --case (default: the first; 'all' for every one)")
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--tile", help="--case: tile override, e.g. 1x1024 (rows x columns)")
+    ap.add_argument("--no-flush", action="store_true", help="--case: do not flush L2 between launches")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.case:
+        for row in run_cases(args):
+            print(json.dumps(row))
+        return
     if args.impl == "reference":
         line = run_reference(args)
     elif args.sweep:

@@ -182,7 +182,8 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  *   TM, TN      row tile x column strip: TM in 8..256 (powers of two),
  *               TN in 64, 128, 256; TM*TN <= 8192 for STAGED
  *               (NAIVE ignores them: its programs are 256 rows x 1 column)
- *   variant     TM_VAR_AUTO, _NAIVE, _STAGED, _REGDIRECT
+ *   variant     TM_VAR_AUTO (= REGDIRECT, the fastest measured), _NAIVE,
+ *               _STAGED, _REGDIRECT
  *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR
  * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE,
  *         WORKSPACE, CUDA; a stalled TMA pipeline is reported by tm_check as

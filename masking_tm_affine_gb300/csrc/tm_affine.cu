@@ -9,11 +9,11 @@
 // tail writes it, so every variant writes all n elements and all are
 // bit-identical (2a is exact, so 2a + 1 is one rounding, with or without FMA).
 //
-// GB300 design: the fast variants are persistent (every SM filled at full
-// residency) with U independent vector loads in flight per thread; VEC8 uses
-// the 32-byte global access sm_100-class GPUs provide.  SCALAR and
-// VEC_UNALIGNED keep the puzzle's one-unit-per-thread grids: they are the
-// instruction-mix foils.
+// GB300 design: the fast variants give every thread U independent vector
+// loads in flight and run one block per 256*U-vector chunk (a flat grid the
+// block scheduler balances); VEC8 uses the 32-byte global access sm_100-class
+// GPUs provide.  SCALAR and VEC_UNALIGNED keep the puzzle's
+// one-unit-per-thread grids: they are the instruction-mix foils.
 #include "tm_host.h"
 
 namespace libtm {
@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(kThreads) affine_vec_unaligned(const float *a,
     if (blockIdx.x == 0 && t < n) st_b32(out + t, affine1(ld_nc_b32(a + t)));
 }
 
-// VEC4 / VEC8: persistent grid, U vectors of VW elements in flight per thread.
+// VEC4 / VEC8: U vectors of VW elements in flight per thread, one chunk of
+// kThreads*U vectors per block (grid-stride beyond the grid limit).
 // Elements [0, head) are a scalar prologue that brings `a + head` and
 // `out + head` onto the vector grid (both have the same misalignment); the
 // vector body covers [head, head + nvec*VW); the rest is the scalar tail.
@@ -188,12 +189,11 @@ extern "C" tm_status tm_affine(const float *a, float *out, int64_t n, tm_variant
         return launch_status();
     }
     const int64_t nvec = (n - head) / vw;
-    const int64_t units = nvec / (kThreads * (vw == 4 ? kUnroll4 : kUnroll8));
-    const void *k = vw == 4 ? (const void *)affine_vec<4, kUnroll4> : (const void *)affine_vec<8, kUnroll8>;
-    int64_t grid = persistent_grid(dev, k, units > 0 ? units : (nvec + kThreads - 1) / kThreads);
+    const int64_t chunks = nvec / (kThreads * (vw == 4 ? kUnroll4 : kUnroll8));
+    const unsigned grid = flat_grid(chunks > 0 ? chunks : (nvec + kThreads - 1) / kThreads);
     if (vw == 4)
-        affine_vec<4, kUnroll4><<<(unsigned)grid, kThreads, 0, s>>>(a, out, n, head);
+        affine_vec<4, kUnroll4><<<grid, kThreads, 0, s>>>(a, out, n, head);
     else
-        affine_vec<8, kUnroll8><<<(unsigned)grid, kThreads, 0, s>>>(a, out, n, head);
+        affine_vec<8, kUnroll8><<<grid, kThreads, 0, s>>>(a, out, n, head);
     return launch_status();
 }

@@ -12,7 +12,8 @@
 //                column); lanes step down a column, ld apart.  Kept as the foil.
 //   REGDIRECT -- lanes over columns: a warp reads a contiguous row segment of a
 //                TN-column strip with 16-byte loads and walks down the rows,
-//                accumulating in registers.  No shared-memory staging needed.
+//                accumulating in registers.  No shared-memory staging needed;
+//                the fastest variant measured, so AUTO takes it.
 //   STAGED    -- the page's fix on GB300 hardware: the TMA engine copies
 //                TM x TN tiles into a ring of shared-memory stages (mbarrier
 //                completion, bounded waits); threads read the columns back out
@@ -34,7 +35,8 @@ namespace libtm {
 namespace {
 
 constexpr int kNaiveRows = 256;        // the page's program length
-constexpr int64_t kTargetUnits = 1024; // (strip, chunk) work units aimed for
+constexpr int64_t kTargetUnits = 8192; // (strip, chunk) work units aimed for: one block each
+constexpr int64_t kMinChunkRows = 64;  // rows per chunk at least: 8 row lanes x 8 loads in flight
 constexpr int kFinishPG = 8;           // chunk groups per column in the finish pass
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 
@@ -56,6 +58,8 @@ ColPlan plan_chunks(int64_t M, int64_t N, int64_t TM, int64_t TN)
     if (P > pl.RT) P = pl.RT;
     if (P < 1) P = 1;
     pl.CT = (pl.RT + P - 1) / P;
+    const int64_t min_ct = (kMinChunkRows + TM - 1) / TM;
+    if (pl.CT < min_ct) pl.CT = min_ct;
     pl.P = (pl.RT + pl.CT - 1) / pl.CT;
     pl.units = pl.S * pl.P;
     pl.npad = (N + 3) & ~int64_t(3);
@@ -407,37 +411,36 @@ bool pow2_in(int v, int lo, int hi)
 }
 
 template <int TM, int TN>
-tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, const DevInfo *dev,
-                          cudaStream_t s)
+tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, cudaStream_t s)
 {
     const void *k = aligned ? (const void *)colsum_staged<TM, TN, true> : (const void *)colsum_staged<TM, TN, false>;
-    int stages = staged_stages(TM, TN);
+    const int max_stages = staged_stages(TM, TN);
+    int stages = a.CT < max_stages ? (int)a.CT : max_stages;  // a unit holds CT tiles: no deeper ring needed
+    const size_t max_smem = (size_t)max_stages * TM * TN * sizeof(float) + (size_t)max_stages * sizeof(uint64_t);
     const size_t smem = (size_t)stages * TM * TN * sizeof(float) + (size_t)stages * sizeof(uint64_t);
     static std::once_flag attr_once[kMaxDevices][2];
     int devno = 0;
     cudaGetDevice(&devno);
     bool attr_ok = true;
     std::call_once(attr_once[devno][aligned ? 1 : 0], [&] {
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem) != cudaSuccess) {
             cudaGetLastError();
             attr_ok = false;
         }
     });
     if (!attr_ok) return TM_ERR_CUDA;
-    const int64_t grid = persistent_grid(dev, k, a.units, smem);
     void *args[] = {const_cast<CUtensorMap *>(&map), const_cast<ColArgs *>(&a), &stages};
-    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(kThreads), args, smem, s) != cudaSuccess) {
+    if (cudaLaunchKernel(k, dim3(flat_grid(a.units)), dim3(kThreads), args, smem, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
     return TM_OK;
 }
 
-tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a,
-                        const DevInfo *dev, cudaStream_t s)
+tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a, cudaStream_t s)
 {
 #define TM_STAGED(tm_, tn_) \
-    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, dev, s);
+    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, s);
     TM_STAGED(16, 64)
     TM_STAGED(32, 64)
     TM_STAGED(64, 64)
@@ -454,26 +457,22 @@ tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, co
 }
 
 template <int TN>
-tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, const DevInfo *dev, cudaStream_t s)
+tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, cudaStream_t s)
 {
     const void *k;
     if (vec) k = aligned ? (const void *)colsum_regdirect<TN, true, true> : (const void *)colsum_regdirect<TN, true, false>;
     else k = aligned ? (const void *)colsum_regdirect<TN, false, true> : (const void *)colsum_regdirect<TN, false, false>;
-    const int64_t grid = persistent_grid(dev, k, a.units);
     void *args[] = {const_cast<ColArgs *>(&a)};
-    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(kThreads), args, 0, s) != cudaSuccess) {
+    if (cudaLaunchKernel(k, dim3(flat_grid(a.units)), dim3(kThreads), args, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
     return TM_OK;
 }
 
-tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, float *c, const DevInfo *dev,
-                        cudaStream_t s)
+tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, float *c, cudaStream_t s)
 {
-    const int64_t blocks = (N + 31) / 32;
-    const int64_t grid = persistent_grid(dev, (const void *)colsum_finish, blocks);
-    colsum_finish<<<(unsigned)grid, 256, 0, s>>>(part, npad, P, N, c);
+    colsum_finish<<<flat_grid((N + 31) / 32), 256, 0, s>>>(part, npad, P, N, c);
     return launch_status();
 }
 
@@ -559,13 +558,13 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     else if (variant == TM_VAR_STAGED) {
         if (encode_fn() == nullptr) return TM_ERR_CUDA;
         v = Variant::Staged;
-    } else v = (tma_shape && encode_fn() != nullptr) ? Variant::Staged : Variant::RegDirect;
+    } else v = Variant::RegDirect;  // measured faster than STAGED at every tile on GB300 (e.g. 51.9 vs 66.2 us
+                                    // at 8192 x 8192, 32 x 128): lanes over columns already coalesce
 
     if (M > 0) {
         if (v == Variant::Naive) {
             const int64_t programs = P * N;
-            const int64_t grid = persistent_grid(dev, (const void *)colsum_naive, programs, 0, kNaiveRows);
-            colsum_naive<<<(unsigned)grid, kNaiveRows, 0, s>>>(X, ldx, M, N, part, npad, programs);
+            colsum_naive<<<flat_grid(programs), kNaiveRows, 0, s>>>(X, ldx, M, N, part, npad, programs);
             st = launch_status();
         } else {
             ColArgs a;
@@ -591,18 +590,18 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                     return TM_ERR_CUDA;
-                st = launch_staged(TM, TN, aligned, map, a, dev, s);
+                st = launch_staged(TM, TN, aligned, map, a, s);
             } else {
                 switch (TN) {
-                case 64: st = launch_regdirect_t<64>(vec, aligned, a, dev, s); break;
-                case 128: st = launch_regdirect_t<128>(vec, aligned, a, dev, s); break;
-                default: st = launch_regdirect_t<256>(vec, aligned, a, dev, s); break;
+                case 64: st = launch_regdirect_t<64>(vec, aligned, a, s); break;
+                case 128: st = launch_regdirect_t<128>(vec, aligned, a, s); break;
+                default: st = launch_regdirect_t<256>(vec, aligned, a, s); break;
                 }
             }
         }
         if (st != TM_OK) return st;
     }
-    return launch_finish(part, npad, P, N, c, dev, s);
+    return launch_finish(part, npad, P, N, c, s);
 }
 
 // ------------------------------------------------------------------ no-allocation entry point

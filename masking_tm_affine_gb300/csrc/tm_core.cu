@@ -7,7 +7,6 @@
 // synchronize": it waits on the stream and reports the bit.
 #include <atomic>
 #include <mutex>
-#include <unordered_map>
 
 #include "tm_host.h"
 
@@ -25,9 +24,6 @@ struct DevSlot {
 
 DevSlot g_slots[kMaxDevices];
 std::mutex g_init_mu;
-
-std::mutex g_occ_mu;
-std::unordered_map<uint64_t, int> g_occ[kMaxDevices];
 
 }  // namespace
 
@@ -56,29 +52,6 @@ tm_status device_info(const DevInfo **out)
     }
     *out = &s.info;
     return TM_OK;
-}
-
-int blocks_per_sm(const void *kernel, int threads, size_t smem)
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
-        return 1;
-    }
-    uint64_t key = reinterpret_cast<uint64_t>(kernel) ^ ((uint64_t)threads << 48) ^ ((uint64_t)smem << 32);
-    {
-        std::lock_guard<std::mutex> lock(g_occ_mu);
-        auto it = g_occ[dev].find(key);
-        if (it != g_occ[dev].end()) return it->second;
-    }
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = 1;
-    }
-    std::lock_guard<std::mutex> lock(g_occ_mu);
-    g_occ[dev][key] = n;
-    return n;
 }
 
 namespace {

@@ -7,12 +7,13 @@
 // stores past the end are skipped; "Promising whole tiles with @aligned":
 // kernel copy2d with 64 x 64 tiles).
 //
-// GB300 design.  The pages launch one CTA per tile.  Here a persistent grid
-// (every SM filled at full residency) walks the tile space in row-major tile
-// order; each iteration takes a group of G consecutive tiles so that every
-// thread has U independent loads in flight (G = 1 for tiles of >= 1024
-// vectors).  Within a group, consecutive threads take consecutive vectors of a
-// tile row, so a warp reads whole 128-byte lines.  Three paths:
+// GB300 design.  The pages launch one CTA per tile.  Here one block takes a
+// group of G consecutive tiles (row-major tile order) so that every thread has
+// U independent loads in flight (G = 1 for tiles of >= 1024 vectors), and the
+// grid is flat -- one block per group -- so the block scheduler balances the
+// load (a persistent grid-stride loop measured ~9% slower on GB300).  Within a
+// group, consecutive threads take consecutive vectors of a tile row, so a warp
+// reads whole 128-byte lines.  Three paths:
 //   Aligned   -- the promise holds: no predicate on any access, 16- or 32-byte
 //                vectors.  Entry check first; on failure no block touches memory.
 //   RaggedVec -- N, ld multiples of 4 and 16-byte bases: 16-byte vectors, one
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
 }
 
 template <int TM, int TN, Op OP>
-tm_status launch_tile(Path path, int ew, const Map2dArgs &a, const DevInfo *dev, cudaStream_t s)
+tm_status launch_tile(Path path, int ew, const Map2dArgs &a, cudaStream_t s)
 {
     const void *k = nullptr;
     if (path == Path::Aligned && ew == 8) k = (const void *)map2d_kernel<TM, TN, OP, Path::Aligned, 8>;
@@ -164,9 +165,8 @@ tm_status launch_tile(Path path, int ew, const Map2dArgs &a, const DevInfo *dev,
     const int64_t V = (int64_t)TM * TN / EW;
     const int64_t G = V >= 4 * kThreads ? 1 : (4 * kThreads) / V;
     const int64_t groups = ((int64_t)a.ntiles + G - 1) / G;
-    const int64_t grid = persistent_grid(dev, k, groups);
     void *args[] = {const_cast<Map2dArgs *>(&a)};
-    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(kThreads), args, 0, s) != cudaSuccess) {
+    if (cudaLaunchKernel(k, dim3(flat_grid(groups)), dim3(kThreads), args, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
@@ -174,10 +174,10 @@ tm_status launch_tile(Path path, int ew, const Map2dArgs &a, const DevInfo *dev,
 }
 
 template <Op OP>
-tm_status dispatch(int TM, int TN, Path path, int ew, const Map2dArgs &a, const DevInfo *dev, cudaStream_t s)
+tm_status dispatch(int TM, int TN, Path path, int ew, const Map2dArgs &a, cudaStream_t s)
 {
 #define TM_TILE(tm_, tn_) \
-    if (TM == tm_ && TN == tn_) return launch_tile<tm_, tn_, OP>(path, ew, a, dev, s);
+    if (TM == tm_ && TN == tn_) return launch_tile<tm_, tn_, OP>(path, ew, a, s);
     TM_TILE(8, 8)
     TM_TILE(16, 16)
     TM_TILE(32, 32)
@@ -249,8 +249,8 @@ tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64
     a.div_tiles_n = make_fastdiv((uint32_t)tiles_n);
     a.status = dev->status;
     cudaStream_t s = as_stream(stream);
-    return op == Op::Scale ? dispatch<Op::Scale>(TM, TN, path, ew, a, dev, s)
-                           : dispatch<Op::Copy>(TM, TN, path, ew, a, dev, s);
+    return op == Op::Scale ? dispatch<Op::Scale>(TM, TN, path, ew, a, s)
+                           : dispatch<Op::Copy>(TM, TN, path, ew, a, s);
 }
 
 }  // namespace

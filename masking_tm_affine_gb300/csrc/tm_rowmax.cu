@@ -11,22 +11,28 @@
 //
 // The row is walked as "Loops over a dynamic extent" splits it: the whole
 // tiles form an unmasked prefix of whole*BC columns, then the one remainder
-// tile takes the masked load and the where.  One warp per row, BR warps per
-// block, persistent grid over row blocks; a shuffle butterfly of fmaxf ends
-// the row.  max is exact and order-free, so the result equals the oracle's
-// bit for bit.
+// tile takes the masked load and the where.  A block of 256 threads takes BR
+// rows, L = 256/BR lanes per row, flat grid (one block per BR-row band); the
+// row's lanes stride through the prefix with U independent loads in flight,
+// and a shuffle butterfly of fmaxf (plus shared memory when L > 32) ends the
+// row.  max is exact and order-free, so the result equals the oracle's bit
+// for bit.
 #include "tm_host.h"
 
 namespace libtm {
 namespace {
 
-template <int BC, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(1024, 1) rowmax_kernel(const float *__restrict__ S, int64_t lds, int64_t M,
-                                                      int64_t N, float *__restrict__ m, int BR, int fill_zero,
-                                                      unsigned *status)
+template <int BR, bool VEC, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) rowmax_kernel(const float *__restrict__ S, int64_t lds, int64_t M,
+                                                          int64_t N, float *__restrict__ m, int BC, int fill_zero,
+                                                          unsigned *status)
 {
+    constexpr int L = kThreads / BR;   // lanes sharing a row
     constexpr int EW = VEC ? 4 : 1;
-    constexpr int U = VEC ? 8 : 16;  // accesses in flight per lane
+    constexpr int U = VEC ? 8 : 16;    // accesses in flight per lane
+    constexpr int W = L > 32 ? L / 32 : 1;
+    __shared__ float part[BR][W];
+
     if constexpr (ALIGNED) {
         const bool whole = (M % BR == 0) && (N % BC == 0);
         const bool grid_ok = !VEC || ((lds % 4 == 0) && (reinterpret_cast<uintptr_t>(S) & 15) == 0);
@@ -36,94 +42,101 @@ __global__ void __launch_bounds__(1024, 1) rowmax_kernel(const float *__restrict
             return;
         }
     }
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    const int lr = threadIdx.x / L, ln = threadIdx.x % L;
     const TileWalk walk = tile_walk(N, BC);
     const int64_t prefix = walk.whole * BC / EW;  // accesses in the whole tiles
     const int64_t row_blocks = (M + BR - 1) / BR;
 
     for (int64_t rb = blockIdx.x; rb < row_blocks; rb += gridDim.x) {
-        const int64_t row = rb * BR + warp;
-        if (!ALIGNED && row >= M) continue;  // row mask (warp-uniform)
-        const float *sr = S + row * lds;
+        const int64_t row = rb * BR + lr;
+        const bool live = ALIGNED || row < M;  // row mask
         float mx = -INFINITY;
-
-        // whole tiles: no mask
-        int64_t v = lane;
-        for (; v + 32 * (U - 1) < prefix; v += 32 * U) {
-            uint32_t w[U][EW];
+        if (live) {
+            const float *sr = S + row * lds;
+            // whole tiles: no mask
+            int64_t v = ln;
+            for (; v + (int64_t)L * (U - 1) < prefix; v += (int64_t)L * U) {
+                uint32_t w[U][EW];
 #pragma unroll
-            for (int q = 0; q < U; ++q) {
-                const float *p = sr + (v + 32 * q) * EW;
+                for (int q = 0; q < U; ++q) {
+                    const float *p = sr + (v + (int64_t)L * q) * EW;
+                    if constexpr (VEC) {
+                        const u32x4 t = ld_nc_v4(p);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                    } else {
+                        w[q][0] = ld_nc_b32(p);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < U; ++q)
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) mx = fmaxf(mx, as_f(w[q][e]));
+            }
+            for (; v < prefix; v += L) {
+                const float *p = sr + v * EW;
                 if constexpr (VEC) {
-                    u32x4 t = ld_nc_v4(p);
+                    const u32x4 t = ld_nc_v4(p);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                    for (int e = 0; e < 4; ++e) mx = fmaxf(mx, as_f(t.v[e]));
                 } else {
-                    w[q][0] = ld_nc_b32(p);
+                    mx = fmaxf(mx, as_f(ld_nc_b32(p)));
                 }
             }
+            // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
+            if (!ALIGNED && walk.masked) {
+                const int64_t kt = walk.whole * BC;
+                for (int iota = ln * EW; iota < BC; iota += L * EW) {
+                    const int64_t j = kt + iota;
+                    float s[EW];
+                    if constexpr (VEC) {
+                        u32x4 t = {{0u, 0u, 0u, 0u}};
+                        if (j < N) t = ld_nc_v4(sr + j);  // N % 4 == 0: a vector is wholly in or out
 #pragma unroll
-            for (int q = 0; q < U; ++q)
+                        for (int e = 0; e < 4; ++e) s[e] = as_f(t.v[e]);
+                    } else {
+                        s[0] = j < N ? as_f(ld_nc_b32(sr + j)) : 0.0f;
+                    }
 #pragma unroll
-                for (int e = 0; e < EW; ++e) mx = fmaxf(mx, as_f(w[q][e]));
-        }
-        for (; v < prefix; v += 32) {
-            const float *p = sr + v * EW;
-            if constexpr (VEC) {
-                u32x4 t = ld_nc_v4(p);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mx = fmaxf(mx, as_f(t.v[e]));
-            } else {
-                mx = fmaxf(mx, as_f(ld_nc_b32(p)));
-            }
-        }
-
-        // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
-        if (!ALIGNED && walk.masked) {
-            const int64_t kt = walk.whole * BC;
-            for (int iota = lane * EW; iota < BC; iota += 32 * EW) {
-                const int64_t j = kt + iota;
-                float s[EW];
-                if constexpr (VEC) {
-                    u32x4 t = {{0u, 0u, 0u, 0u}};
-                    if (j < N) t = ld_nc_v4(sr + j);  // N % 4 == 0: a vector is wholly in or out
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[e] = as_f(t.v[e]);
-                } else {
-                    s[0] = j < N ? as_f(ld_nc_b32(sr + j)) : 0.0f;
-                }
-#pragma unroll
-                for (int e = 0; e < EW; ++e) {
-                    if (!fill_zero) s[e] = (iota + e < N - kt) ? s[e] : -INFINITY;
-                    mx = fmaxf(mx, s[e]);
+                    for (int e = 0; e < EW; ++e) {
+                        if (!fill_zero) s[e] = (iota + e < N - kt) ? s[e] : -INFINITY;
+                        mx = fmaxf(mx, s[e]);
+                    }
                 }
             }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) m[row] = mx;
+        for (int o = (L < 32 ? L : 32) / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if constexpr (W > 1) {
+            if ((ln & 31) == 0) part[lr][ln >> 5] = mx;
+            __syncthreads();
+            if (ln == 0) {
+#pragma unroll
+                for (int w = 1; w < W; ++w) mx = fmaxf(mx, part[lr][w]);
+            }
+            __syncthreads();
+        }
+        if (ln == 0 && live) m[row] = mx;
     }
 }
 
-template <int BC>
-tm_status launch(bool vec, bool aligned, const float *S, int64_t lds, int64_t M, int64_t N, float *m, int BR,
-                 int fill_zero, const DevInfo *dev, cudaStream_t s)
+template <int BR>
+tm_status launch(bool vec, bool aligned, const float *S, int64_t lds, int64_t M, int64_t N, float *m, int BC,
+                 int fill_zero, unsigned *status, cudaStream_t s)
 {
     const void *k;
-    if (vec) k = aligned ? (const void *)rowmax_kernel<BC, true, true> : (const void *)rowmax_kernel<BC, true, false>;
-    else k = aligned ? (const void *)rowmax_kernel<BC, false, true> : (const void *)rowmax_kernel<BC, false, false>;
-    const int threads = 32 * BR;
-    const int64_t grid = persistent_grid(dev, k, (M + BR - 1) / BR, 0, threads);
-    unsigned *status = dev->status;
+    if (vec) k = aligned ? (const void *)rowmax_kernel<BR, true, true> : (const void *)rowmax_kernel<BR, true, false>;
+    else k = aligned ? (const void *)rowmax_kernel<BR, false, true> : (const void *)rowmax_kernel<BR, false, false>;
     void *args[] = {(void *)&S, (void *)&lds, (void *)&M, (void *)&N, (void *)&m,
-                    (void *)&BR, (void *)&fill_zero, (void *)&status};
-    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(threads), args, 0, s) != cudaSuccess) {
+                    (void *)&BC, (void *)&fill_zero, (void *)&status};
+    if (cudaLaunchKernel(k, dim3(flat_grid((M + BR - 1) / BR)), dim3(kThreads), args, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
     return TM_OK;
 }
+
+bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
 
 }  // namespace
 }  // namespace libtm
@@ -137,8 +150,7 @@ extern "C" tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, in
     if (M > 0 && m == nullptr) return TM_ERR_INVALID_ARG;
     if (fill != TM_FILL_NEG_INF && fill != TM_FILL_ZERO) return TM_ERR_INVALID_ARG;
     if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
-    if (!(BR == 1 || BR == 2 || BR == 4 || BR == 8 || BR == 16 || BR == 32)) return TM_ERR_UNSUPPORTED_TILE;
-    if (!(BC == 16 || BC == 32 || BC == 64 || BC == 128 || BC == 256 || BC == 512)) return TM_ERR_UNSUPPORTED_TILE;
+    if (!pow2_in(BR, 1, 32) || !pow2_in(BC, 16, 4096)) return TM_ERR_UNSUPPORTED_TILE;
     if (M > 0 && !aligned_to(m, 4)) return TM_ERR_MISALIGNED;
     if (M > 0 && N > 0 && !aligned_to(S, 4)) return TM_ERR_MISALIGNED;
     if (M > 0 && N > 0) {
@@ -169,12 +181,12 @@ extern "C" tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, in
     if (st != TM_OK) return st;
     cudaStream_t s = as_stream(stream);
     const int fz = fill == TM_FILL_ZERO ? 1 : 0;
-    switch (BC) {
-    case 16: return launch<16>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
-    case 32: return launch<32>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
-    case 64: return launch<64>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
-    case 128: return launch<128>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
-    case 256: return launch<256>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
-    default: return launch<512>(vec, aligned, S, lds, M, N, m, BR, fz, dev, s);
+    switch (BR) {
+    case 1: return launch<1>(vec, aligned, S, lds, M, N, m, BC, fz, dev->status, s);
+    case 2: return launch<2>(vec, aligned, S, lds, M, N, m, BC, fz, dev->status, s);
+    case 4: return launch<4>(vec, aligned, S, lds, M, N, m, BC, fz, dev->status, s);
+    case 8: return launch<8>(vec, aligned, S, lds, M, N, m, BC, fz, dev->status, s);
+    case 16: return launch<16>(vec, aligned, S, lds, M, N, m, BC, fz, dev->status, s);
+    default: return launch<32>(vec, aligned, S, lds, M, N, m, BC, fz, dev->status, s);
     }
 }

@@ -8,24 +8,28 @@
 // missing columns read 0, the right fill for a sum ("Reductions over a ragged
 // tile").
 //
-// GB300 design: one warp per row, TM warps per block, persistent grid over
-// row blocks.  In the vector path each lane takes TN/128 16-byte vectors per
-// tile and several tiles are in flight per step (8 vectors = 128 bytes per
-// lane); the warp's partial sums meet in a butterfly of shuffles, so the
-// summation order is fixed and the result is identical run to run.
+// GB300 design: a block of 256 threads takes TM rows, L = 256/TM lanes per
+// row.  The whole tiles of a row form one contiguous unmasked prefix, which
+// the row's lanes stride through with U independent 16-byte loads in flight
+// each; then the lanes cover the remainder tile with masked loads.  The L
+// partial sums of a row meet in a shuffle butterfly (plus shared memory when
+// L > 32), so the summation order is fixed and the result identical run to
+// run.  The grid is flat -- one block per TM-row band -- for the block
+// scheduler to balance (TM = 1, a block per row, measured fastest on long rows).
 #include "tm_host.h"
 
 namespace libtm {
 namespace {
 
-template <int TN, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(1024, 1) rowsum_kernel(const float *__restrict__ X, int64_t ldx, int64_t M,
-                                                      int64_t N, float *__restrict__ r, int TM, unsigned *status)
+template <int TM, bool VEC, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) rowsum_kernel(const float *__restrict__ X, int64_t ldx, int64_t M,
+                                                          int64_t N, float *__restrict__ r, int TN, unsigned *status)
 {
-    constexpr int EW = VEC ? 4 : 1;                   // elements per access
-    constexpr int PER_TILE = TN / (32 * EW);          // accesses per lane per tile
-    constexpr int TPS = PER_TILE >= 8 ? 1 : 8 / PER_TILE;  // tiles per unrolled step
-    static_assert(PER_TILE >= 1, "tile narrower than a warp's access");
+    constexpr int L = kThreads / TM;   // lanes sharing a row
+    constexpr int EW = VEC ? 4 : 1;    // elements per access
+    constexpr int U = VEC ? 8 : 16;    // accesses in flight per lane
+    constexpr int W = L > 32 ? L / 32 : 1;  // warps per row
+    __shared__ float part[TM][W];
 
     if constexpr (ALIGNED) {
         const bool whole = (M % TM == 0) && (N % TN == 0);
@@ -36,67 +40,62 @@ __global__ void __launch_bounds__(1024, 1) rowsum_kernel(const float *__restrict
             return;
         }
     }
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    const int lr = threadIdx.x / L, ln = threadIdx.x % L;
     const TileWalk walk = tile_walk(N, TN);
+    const int64_t prefix = walk.whole * TN / EW;  // accesses in the whole tiles
     const int64_t row_blocks = (M + TM - 1) / TM;
 
     for (int64_t rb = blockIdx.x; rb < row_blocks; rb += gridDim.x) {
-        const int64_t row = rb * TM + warp;
-        if (!ALIGNED && row >= M) continue;  // row mask (warp-uniform)
-        const float *xr = X + row * ldx;
+        const int64_t row = rb * TM + lr;
+        const bool live = ALIGNED || row < M;  // row mask
         float acc[EW];
 #pragma unroll
         for (int e = 0; e < EW; ++e) acc[e] = 0.0f;
-
-        // whole tiles, TPS at a time, no mask
-        int64_t t = 0;
-        for (; t + TPS <= walk.whole; t += TPS) {
-            uint32_t v[TPS * PER_TILE][EW];
+        if (live) {
+            const float *xr = X + row * ldx;
+            // whole tiles: no mask
+            int64_t v = ln;
+            for (; v + (int64_t)L * (U - 1) < prefix; v += (int64_t)L * U) {
+                uint32_t w[U][EW];
 #pragma unroll
-            for (int q = 0; q < TPS * PER_TILE; ++q) {
-                const float *p = xr + t * TN + ((int64_t)q * 32 + lane) * EW;
-                if constexpr (VEC) {
-                    u32x4 w = ld_nc_v4(p);
+                for (int q = 0; q < U; ++q) {
+                    const float *p = xr + (v + (int64_t)L * q) * EW;
+                    if constexpr (VEC) {
+                        const u32x4 t = ld_nc_v4(p);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) v[q][e] = w.v[e];
-                } else {
-                    v[q][0] = ld_nc_b32(p);
+                        for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                    } else {
+                        w[q][0] = ld_nc_b32(p);
+                    }
                 }
+#pragma unroll
+                for (int q = 0; q < U; ++q)
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) acc[e] += as_f(w[q][e]);
             }
-#pragma unroll
-            for (int q = 0; q < TPS * PER_TILE; ++q)
-#pragma unroll
-                for (int e = 0; e < EW; ++e) acc[e] += as_f(v[q][e]);
-        }
-        // leftover whole tiles, one at a time, no mask
-        for (; t < walk.whole; ++t) {
-#pragma unroll
-            for (int q = 0; q < PER_TILE; ++q) {
-                const float *p = xr + t * TN + ((int64_t)q * 32 + lane) * EW;
+            for (; v < prefix; v += L) {
+                const float *p = xr + v * EW;
                 if constexpr (VEC) {
-                    u32x4 w = ld_nc_v4(p);
+                    const u32x4 t = ld_nc_v4(p);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
+                    for (int e = 0; e < 4; ++e) acc[e] += as_f(t.v[e]);
                 } else {
                     acc[0] += as_f(ld_nc_b32(p));
                 }
             }
-        }
-        // the masked remainder tile: columns past N read as 0
-        if (!ALIGNED && walk.masked) {
-            const int64_t kt = walk.whole * TN;
+            // the masked remainder tile: columns past N read as 0
+            if (!ALIGNED && walk.masked) {
+                const int64_t kt = walk.whole * TN;
+                for (int iota = ln * EW; iota < TN; iota += L * EW) {
+                    const int64_t j = kt + iota;
+                    if constexpr (VEC) {
+                        u32x4 t = {{0u, 0u, 0u, 0u}};
+                        if (j < N) t = ld_nc_v4(xr + j);  // N % 4 == 0: a vector is wholly in or out
 #pragma unroll
-            for (int q = 0; q < PER_TILE; ++q) {
-                const int64_t j = kt + ((int64_t)q * 32 + lane) * EW;
-                if constexpr (VEC) {
-                    u32x4 w = {{0u, 0u, 0u, 0u}};
-                    if (j < N) w = ld_nc_v4(xr + j);  // N % 4 == 0: a vector is wholly in or out
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
-                } else {
-                    acc[0] += j < N ? as_f(ld_nc_b32(xr + j)) : 0.0f;
+                        for (int e = 0; e < 4; ++e) acc[e] += as_f(t.v[e]);
+                    } else {
+                        acc[0] += j < N ? as_f(ld_nc_b32(xr + j)) : 0.0f;
+                    }
                 }
             }
         }
@@ -104,28 +103,37 @@ __global__ void __launch_bounds__(1024, 1) rowsum_kernel(const float *__restrict
 #pragma unroll
         for (int e = 1; e < EW; ++e) s += acc[e];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) r[row] = s;
+        for (int o = (L < 32 ? L : 32) / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if constexpr (W > 1) {
+            if ((ln & 31) == 0) part[lr][ln >> 5] = s;
+            __syncthreads();
+            if (ln == 0) {
+                s = part[lr][0];
+#pragma unroll
+                for (int w = 1; w < W; ++w) s += part[lr][w];
+            }
+            __syncthreads();
+        }
+        if (ln == 0 && live) r[row] = s;
     }
 }
 
-template <int TN>
-tm_status launch(bool vec, bool aligned, const float *X, int64_t ldx, int64_t M, int64_t N, float *r, int TM,
-                 const DevInfo *dev, cudaStream_t s)
+template <int TM>
+tm_status launch(bool vec, bool aligned, const float *X, int64_t ldx, int64_t M, int64_t N, float *r, int TN,
+                 unsigned *status, cudaStream_t s)
 {
     const void *k;
-    if (vec) k = aligned ? (const void *)rowsum_kernel<TN, true, true> : (const void *)rowsum_kernel<TN, true, false>;
-    else k = aligned ? (const void *)rowsum_kernel<TN, false, true> : (const void *)rowsum_kernel<TN, false, false>;
-    const int threads = 32 * TM;
-    const int64_t grid = persistent_grid(dev, k, (M + TM - 1) / TM, 0, threads);
-    unsigned *status = dev->status;
-    void *args[] = {(void *)&X, (void *)&ldx, (void *)&M, (void *)&N, (void *)&r, (void *)&TM, (void *)&status};
-    if (cudaLaunchKernel(k, dim3((unsigned)grid), dim3(threads), args, 0, s) != cudaSuccess) {
+    if (vec) k = aligned ? (const void *)rowsum_kernel<TM, true, true> : (const void *)rowsum_kernel<TM, true, false>;
+    else k = aligned ? (const void *)rowsum_kernel<TM, false, true> : (const void *)rowsum_kernel<TM, false, false>;
+    void *args[] = {(void *)&X, (void *)&ldx, (void *)&M, (void *)&N, (void *)&r, (void *)&TN, (void *)&status};
+    if (cudaLaunchKernel(k, dim3(flat_grid((M + TM - 1) / TM)), dim3(kThreads), args, 0, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
     return TM_OK;
 }
+
+bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
 
 }  // namespace
 }  // namespace libtm
@@ -138,8 +146,7 @@ extern "C" tm_status tm_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N
     if (!valid2d(X, ldx, M, N)) return TM_ERR_INVALID_ARG;
     if (M > 0 && r == nullptr) return TM_ERR_INVALID_ARG;
     if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
-    if (!(TM == 1 || TM == 2 || TM == 4 || TM == 8 || TM == 16 || TM == 32)) return TM_ERR_UNSUPPORTED_TILE;
-    if (!(TN == 128 || TN == 256 || TN == 512 || TN == 1024)) return TM_ERR_UNSUPPORTED_TILE;
+    if (!pow2_in(TM, 1, 32) || !pow2_in(TN, 16, 4096)) return TM_ERR_UNSUPPORTED_TILE;
     if (M > 0 && !aligned_to(r, 4)) return TM_ERR_MISALIGNED;
     if (M > 0 && N > 0 && !aligned_to(X, 4)) return TM_ERR_MISALIGNED;
     if (M > 0 && N > 0) {
@@ -169,10 +176,12 @@ extern "C" tm_status tm_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N
     tm_status st = device_info(&dev);
     if (st != TM_OK) return st;
     cudaStream_t s = as_stream(stream);
-    switch (TN) {
-    case 128: return launch<128>(vec, aligned, X, ldx, M, N, r, TM, dev, s);
-    case 256: return launch<256>(vec, aligned, X, ldx, M, N, r, TM, dev, s);
-    case 512: return launch<512>(vec, aligned, X, ldx, M, N, r, TM, dev, s);
-    default: return launch<1024>(vec, aligned, X, ldx, M, N, r, TM, dev, s);
+    switch (TM) {
+    case 1: return launch<1>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
+    case 2: return launch<2>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
+    case 4: return launch<4>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
+    case 8: return launch<8>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
+    case 16: return launch<16>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
+    default: return launch<32>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
     }
 }
