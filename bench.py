@@ -432,10 +432,13 @@ def run_reference(args):
     if prev:
         os.sched_setaffinity(0, {min(prev)})
 
+    Yall = np.empty_like(x)
+    Ball = np.empty(x.size, dtype=np.uint32)
+
     def one_pass(R):
         xs = x[:R]
-        Yw = np.empty_like(xs)
-        Bw = np.empty(xs.size, dtype=np.uint32)
+        Yw = Yall[:R]
+        Bw = Ball[:R * N]
         oracle.affine(xs)
         oracle.scale2d(xs, N, Yw, N, R, N, ALPHA)
         oracle.copy2d(xs, N, Bw, N, R, N)

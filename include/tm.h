@@ -34,7 +34,7 @@
  * Errors.   No call prints, aborts or throws.  A call that returns anything but
  *           TM_OK has launched nothing and written nothing.  A promise broken
  *           on the device side is reported by the next tm_check, mirroring
- *           "the next synchronize on the host fails" ("@aligned", "When the
+ *           the page's failing host synchronize ("@aligned", "When the
  *           promise is broken").
  * Empty.    M == 0, N == 0 or n == 0 is legal.  Maps then do nothing; a
  *           reduction still writes its outputs (sum of nothing = 0, max of
@@ -172,7 +172,8 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
 /*
  * tm_colsum -- c[j] = sum_i X[i, j] (fp32 accumulation), the stride-COLS walk
  * of "Memory Coalescing and Tensor Layout", "What it actually costs", and its
- * fix from "Seeing it in a real kernel" (load a tile once into fast memory).
+ * fix from "Seeing it in a real kernel" (stage a tile in fast on-chip memory
+ * and read it there in any order).
  * Row chunks write partial sums to `workspace`; a second pass adds them in a
  * fixed order, so the result is deterministic run to run.
  *   X, ldx      device input [M, ldx]        c   device output, N floats
@@ -198,7 +199,7 @@ tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c,
  * "Slicing, bounds and masking", "Reductions over a ragged tile": whole tiles
  * are read unmasked; the remainder tile's missing columns read 0 and are then
  * replaced by where(iota < N - kt, s, fill).  fill = TM_FILL_NEG_INF gives the
- * true row maximum (a value no real score reaches); TM_FILL_ZERO skips the
+ * true row maximum (the fill can never win); TM_FILL_ZERO skips the
  * where step and reproduces the pitfall (max(0, true max) when N % BC != 0).
  * N == 0 gives -inf.  max ignores a NaN operand unless both are NaN.
  *   S, lds   device input [M, lds]     m   device output, M floats

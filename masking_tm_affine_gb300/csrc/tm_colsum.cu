@@ -3,7 +3,7 @@
 // Source: "Memory Coalescing and Tensor Layout".  "What it actually costs":
 // the column-order walk of a row-major matrix (offsets rows*COLS + col, 65536
 // programs of 256 elements over 4096 x 4096, neighbouring programs on
-// neighbouring columns) reads the same 64 MB as the row walk but 2.4x slower
+// neighbouring columns) moves the row walk's bytes yet ran 2.4x slower
 // on the page's GPU.  "Seeing it in a real kernel": the way out is to load a
 // tile once into fast memory and read it there in any order.
 //

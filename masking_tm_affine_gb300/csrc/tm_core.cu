@@ -77,7 +77,7 @@ extern "C" const char *tm_status_string(tm_status st)
     case TM_ERR_INVALID_ARG: return "TM_ERR_INVALID_ARG: invalid argument";
     case TM_ERR_UNSUPPORTED_TILE: return "TM_ERR_UNSUPPORTED_TILE: tile not positive or not instantiated";
     case TM_ERR_MISALIGNED: return "TM_ERR_MISALIGNED: pointer or leading dimension breaks vector alignment";
-    case TM_ERR_BROKEN_PROMISE: return "TM_ERR_BROKEN_PROMISE: aligned promise broken (extent not a whole number of tiles)";
+    case TM_ERR_BROKEN_PROMISE: return "TM_ERR_BROKEN_PROMISE: aligned promise broken (an extent is not a multiple of its tile)";
     case TM_ERR_CUDA: return "TM_ERR_CUDA: CUDA runtime error";
     case TM_ERR_WORKSPACE: return "TM_ERR_WORKSPACE: workspace missing, too small or misaligned";
     case TM_ERR_TIMEOUT: return "TM_ERR_TIMEOUT: a bounded device wait gave up";

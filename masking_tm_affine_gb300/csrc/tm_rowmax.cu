@@ -5,7 +5,7 @@
 // of negative scores padded with zeros has a maximum of 0.  The fix is a
 // second mask written with where and iota: in the column tile starting at kt,
 // the column index iota (0 .. BC-1) is kept where iota < N - kt and replaced
-// by a value no real score reaches otherwise.  That value is -inf here (the
+// otherwise by a fill that can never be a row's maximum.  That fill is -inf (the
 // page prints -1.0e30; -inf is the same for every finite score above -1e30 and
 // still correct below it).  TM_FILL_ZERO skips the where step: the foil.
 //

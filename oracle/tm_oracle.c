@@ -153,8 +153,8 @@ void oracle_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N, double *r)
 
 /* ------------------------------------------------------------------------ */
 /* a6: per-column sums -- the stride-COLS walk of [MC] "What it actually      */
-/* costs", same bytes, same arithmetic: c[j] = sum_i X[i, j] in fp64, rows    */
-/* added in ascending order.                                                  */
+/* costs", the row walk's data read in column order: c[j] = sum_i X[i, j] in  */
+/* fp64, rows added in ascending order.                                       */
 /* ------------------------------------------------------------------------ */
 void oracle_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, double *c)
 {
@@ -173,7 +173,7 @@ void oracle_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, double *c)
 /*     s[c] = S[i, kt + c] when kt + c < N, else 0  (a masked load reads 0,   */
 /*            [SB] "Masking")                                                 */
 /*     fill_mode 0: s[c] = (c < N - kt) ? s[c] : -inf  (the where/iota mask;  */
-/*            -inf is the value no real score reaches)                        */
+/*            -inf can never be a row's maximum)                             */
 /*     fill_mode 1: no where step -- the zero-fill pitfall the page warns of  */
 /*     m = max(m, max_c s[c])                                                 */
 /* m starts at -inf, the identity of max, so N = 0 gives -inf.  max follows   */
