@@ -331,7 +331,8 @@ def run_gpu(args):
     # end to end through the C ABI: pinned host X in, every output back to pinned host memory
     e2e = None
     if rank == 0 and args.e2e_steps > 0:
-        e2e = run_e2e(tm, bufs, x, step, stream, dev, min(args.steps, args.e2e_steps), step_bytes)
+        e2e = run_e2e(tm, bufs, x, step, stream, dev, min(args.steps, args.e2e_steps), step_bytes, ws_bytes,
+                      args.e2e_mode)
 
     if rank != 0:
         if world > 1:
@@ -384,36 +385,88 @@ def run_gpu(args):
     return line
 
 
-def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes):
+def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="pipelined"):
+    """The step end to end through the C ABI: every step copies its input X from
+    pinned host memory and every output back to pinned host memory.
+
+    mode "serial": copy in, six calls, copy out, one stream.
+    mode "pipelined": two device buffer sets; step k's copy-in, kernels and
+    copy-out run on three streams ordered by events, so step k+1's upload and
+    step k-1's download overlap step k's kernels (copies of opposite directions
+    also overlap on the link).  Each step still moves all of its own data."""
     import torch
-    hx = torch.from_numpy(x.reshape(-1)).pin_memory()
     outs = ["A1", "Y", "B", "r", "c", "m"]
-    host = {k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs}
+    hx = torch.from_numpy(x.reshape(-1)).pin_memory()
     h2d = hx.numel() * 4
     d2h = sum(bufs[k].numel() * 4 for k in outs)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
+    if mode == "serial":
+        host = {k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs}
+
+        def one(k):
             bufs["X"].copy_(hx, non_blocking=True)
             for _, fn in step:
                 fn()
-            for k in outs:
-                host[k].copy_(bufs[k], non_blocking=True)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            bufs["X"].copy_(hx, non_blocking=True)
-            for _, fn in step:
-                fn()
-            for k in outs:
-                host[k].copy_(bufs[k], non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    t = e0.elapsed_time(e1) * 1e-3
+            for o in outs:
+                host[o].copy_(bufs[o], non_blocking=True)
+        with torch.cuda.stream(stream):
+            for k in range(2):
+                one(k)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in range(steps):
+                one(k)
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) * 1e-3
+    else:
+        sets = [bufs, make_buffers(tm, x, dev)[0]]
+        steps_of = [step, make_step(tm, sets[1], ws_bytes, stream)]
+        hosts = [{k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs} for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev = lambda: torch.cuda.Event()
+        loaded = [ev(), ev()]
+        computed = [ev(), ev()]
+        drained = [ev(), ev()]
+        first = [True, True]
+
+        def one(k):
+            b = k % 2
+            with torch.cuda.stream(s_in):
+                if not first[b]:
+                    s_in.wait_event(computed[b])       # the kernels of step k-2 are done with X[b]
+                sets[b]["X"].copy_(hx, non_blocking=True)
+                loaded[b].record(s_in)
+            with torch.cuda.stream(stream):
+                stream.wait_event(loaded[b])
+                if not first[b]:
+                    stream.wait_event(drained[b])      # the outputs of step k-2 have left the device
+                for _, fn in steps_of[b]:
+                    fn()
+                computed[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[b])
+                for o in outs:
+                    hosts[b][o].copy_(sets[b][o], non_blocking=True)
+                drained[b].record(s_out)
+            first[b] = False
+        for k in range(2):
+            one(k)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for k in range(steps):
+            one(k)
+        s_in.wait_stream(s_out)
+        e1.record(s_in)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) * 1e-3
     return {"value": round(gbps(step_bytes * steps, t), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3),
-            "path": "pinned host X -> device, six C-ABI calls, every output -> pinned host, one stream"}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3), "mode": mode,
+            "path": "pinned host X -> device, the six C-ABI calls, every output -> pinned host"
+                    + (", one stream" if mode == "serial" else
+                       "; copy-in, kernels and copy-out of consecutive steps overlap on three streams")}
 
 
 # --------------------------------------------------------------------- reference arm
@@ -628,6 +681,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="print the 1 KB..1 GB size sweep instead")
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-mode", choices=["pipelined", "serial"], default="pipelined")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-verify", action="store_true")
     ap.add_argument("--case", help="time one kernel on one workload instead (%s, or all)" % ", ".join(CASES))

@@ -1,9 +1,11 @@
 """Build ``libtm.so`` in-tree with nvcc for sm_103a (GB300).
 
 Each ``csrc/*.cu`` translation unit compiles in parallel into ``_build/``;
-they link into ``masking_tm_affine_gb300/lib/libtm.so`` with the CUDA runtime
-linked statically (the library shares the device's primary context with
-whoever loads it).  No fast-math and no flush-to-zero: the maps must match the
+they link into ``masking_tm_affine_gb300/lib/libtm.so`` against the shared CUDA
+runtime (``libcudart.so.13``).  A process that already loaded the runtime --
+torch does at import -- shares that one instance with libtm, so the current
+device, streams and contexts are the caller's; otherwise the RUNPATH to the
+toolkit's lib64 finds it.  No fast-math and no flush-to-zero: the maps must match the
 oracle bit for bit.  ``ptxas -v`` reports (registers, spills, shared memory)
 land in ``_build/*.ptxas.txt``.
 
@@ -81,7 +83,8 @@ def build(force: bool = False) -> str:
         objs = list(ex.map(_compile, srcs))
     if force or _stale(LIB, objs):
         tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+        libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
+        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath," + libdir, "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link of libtm.so failed:\n%s" % r.stderr[-6000:])

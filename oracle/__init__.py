@@ -66,6 +66,8 @@ def _load():
         lib.oracle_colsum.restype = None
         lib.oracle_rowmax_masked.argtypes = [vp, i64, i64, i64, i64, i32, vp]
         lib.oracle_rowmax_masked.restype = i32
+        lib.oracle_softmax_rowstats.argtypes = [vp, i64, i64, i64, i64, i32, vp, vp]
+        lib.oracle_softmax_rowstats.restype = i32
         _lib = lib
         return lib
 
@@ -168,3 +170,16 @@ def rowmax_masked(S, lds: int, M: int, N: int, BC: int, fill: int = FILL_NEG_INF
     if _load().oracle_rowmax_masked(_ptr(S), lds, M, N, BC, fill, _ptr(m)) != 0:
         raise ValueError("rowmax needs BC > 0 and a known fill")
     return m
+
+
+def softmax_rowstats(S, lds: int, M: int, N: int, BC: int, fill: int = FILL_NEG_INF):
+    """Row maximum m (float32) and normaliser l = sum exp(s - m) (float64) over
+    BC-wide ragged column tiles ("Slicing, bounds and masking", "Reductions over
+    a ragged tile": the softmax needs the same -inf fill as the maximum)."""
+    S = _as_f32_flat(S)
+    _check_2d(S, lds, M, N, "S")
+    m = np.empty(M, dtype=np.float32)
+    l = np.empty(M, dtype=np.float64)
+    if _load().oracle_softmax_rowstats(_ptr(S), lds, M, N, BC, fill, _ptr(m), _ptr(l)) != 0:
+        raise ValueError("softmax row statistics need BC > 0 and a known fill")
+    return m, l

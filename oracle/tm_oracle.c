@@ -200,3 +200,48 @@ int oracle_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* f1: softmax row statistics over ragged column tiles.  [SB] "Reductions    */
+/* over a ragged tile" names the softmax as the second reduction the zero    */
+/* fill breaks; its statistics are the row maximum m and the normaliser      */
+/* l = sum_j exp(s_j - m).  Per row i, over the tile walk of the row-max     */
+/* oracle above (masked load reading 0, then the where step unless           */
+/* fill_mode == 1), every tile value v enters the definition:                */
+/*   m = max over all tile values (fmaxf; starts at -inf)                    */
+/*   l = sum over all tile values of exp(v - m), in fp64; a value of -inf    */
+/*       contributes exp(-inf) = 0; when m = -inf the sum is empty: l = 0.   */
+/* With fill -inf this is the plain definition over the N real scores.       */
+/* ------------------------------------------------------------------------ */
+int oracle_softmax_rowstats(const float *S, int64_t lds, int64_t M, int64_t N,
+                            int64_t BC, int fill_mode, float *m, double *l)
+{
+    int64_t i, kt, c;
+    if (BC <= 0 || (fill_mode != 0 && fill_mode != 1))
+        return -1;
+    for (i = 0; i < M; ++i) {
+        float mi = -INFINITY;
+        double li = 0.0;
+        /* first pass: the maximum over the masked tiles */
+        for (kt = 0; kt < N; kt += BC)
+            for (c = 0; c < BC; ++c) {
+                float s = (kt + c < N) ? S[i * lds + kt + c] : 0.0f;
+                if (fill_mode == 0)
+                    s = (c < N - kt) ? s : -INFINITY;
+                mi = fmaxf(mi, s);
+            }
+        /* second pass: the sum of exponentials relative to it */
+        if (mi != -INFINITY)
+            for (kt = 0; kt < N; kt += BC)
+                for (c = 0; c < BC; ++c) {
+                    float s = (kt + c < N) ? S[i * lds + kt + c] : 0.0f;
+                    if (fill_mode == 0)
+                        s = (c < N - kt) ? s : -INFINITY;
+                    if (s != -INFINITY)
+                        li += exp((double)s - (double)mi);
+                }
+        m[i] = mi;
+        l[i] = li;
+    }
+    return 0;
+}

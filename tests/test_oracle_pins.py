@@ -383,3 +383,58 @@ def test_bandwidth_units_match_page_table():
     for access, rows, cols, nbytes, t_us, bw in read_golden("coalescing_table.txt"):
         assert int(nbytes) == int(rows) * int(cols) * 4 == 2**26
         assert abs(gbps(int(nbytes), float(t_us) * 1e-6) - float(bw)) / float(bw) < 1e-3
+
+
+# --------------------------------------------------------------------------
+# Softmax row statistics (the softmax of "Reductions over a ragged tile")
+# --------------------------------------------------------------------------
+def test_softmax_stats_constant_rows(oracle):
+    # s = c everywhere: m = c and every term is exp(0) = 1, so l = N exactly
+    for N, BC in [(1, 64), (40, 64), (64, 64), (1000, 64), (7, 16)]:
+        s = np.full((3, N), -7.25, dtype=np.float32)
+        m, l = oracle.softmax_rowstats(s, N, 3, N, BC)
+        assert np.all(m == np.float32(-7.25)) and np.all(l == float(N))
+
+
+def test_softmax_stats_match_scipy_logsumexp(oracle):
+    from scipy.special import logsumexp
+    s = synth.uniform((20, 1000), -30.0, -1.0, 4)
+    m, l = oracle.softmax_rowstats(s, 1000, 20, 1000, 64)
+    assert np.array_equal(m, s.max(axis=1))
+    lse = logsumexp(s.astype(np.float64), axis=1)
+    assert np.allclose(m.astype(np.float64) + np.log(l), lse, rtol=0, atol=1e-12)
+
+
+def test_softmax_stats_two_values_by_hand(oracle):
+    # scores {2, 2 - ln 3}: m = 2 and l = 1 + e^(-ln 3) = 4/3, up to the float32
+    # rounding of the second score (exactly 1 + exp(s1 - 2) with math.exp)
+    s = np.array([[2.0, 2.0 - np.log(3.0)]], dtype=np.float32)
+    m, l = oracle.softmax_rowstats(s, 2, 1, 2, 64)
+    assert m[0] == np.float32(2.0)
+    assert abs(l[0] - (1.0 + math.exp(float(s[0, 1]) - 2.0))) < 1e-15
+    assert abs(l[0] - 4.0 / 3.0) < 1e-7
+
+
+def test_softmax_stats_zero_fill_pitfall(oracle):
+    # negative scores, ragged last tile, no where step: padding zeros win the max
+    # and each padded column adds exp(0 - 0) = 1 to l
+    N, BC = 1000, 64
+    s = synth.uniform((5, N), -30.0, -1.0, 8)
+    m0, l0 = oracle.softmax_rowstats(s, N, 5, N, BC, oracle.FILL_ZERO)
+    pad = BC - N % BC
+    assert np.all(m0 == 0.0)
+    want = np.exp(s.astype(np.float64)).sum(axis=1) + pad
+    assert np.allclose(l0, want, rtol=1e-13, atol=0)
+    mi, li = oracle.softmax_rowstats(s, N, 5, N, BC, oracle.FILL_NEG_INF)
+    assert np.all(mi < 0) and np.all(li >= 1.0) and np.all(li < N)
+
+
+def test_softmax_stats_empty_and_infinite(oracle):
+    m, l = oracle.softmax_rowstats(np.zeros(4, np.float32), 1, 4, 0, 64)
+    assert np.all(m == -np.inf) and np.all(l == 0.0)
+    s = np.full((1, 10), -np.inf, dtype=np.float32)
+    m, l = oracle.softmax_rowstats(s, 10, 1, 10, 16)
+    assert m[0] == -np.inf and l[0] == 0.0
+    s[0, 3] = -5.0
+    m, l = oracle.softmax_rowstats(s, 10, 1, 10, 16)
+    assert m[0] == np.float32(-5.0) and l[0] == 1.0
