@@ -580,7 +580,9 @@ CASES = {
     "rowsum_4096": ("coalesce_4096", "rowsum", ["vec", "scalar"]),
     "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive"]),
     "rowmax_8192": ("rowmax_8192", "rowmax_masked", ["neg_inf", "zero", "scalar"]),
+    "softmax_8192": ("rowmax_8192", "softmax_rowstats", ["neg_inf", "zero", "scalar"]),
     # the reductions on the [8192, 8192] batch of the step, for tile tuning
+    "softmax_8192sq": ("scale_8192", "softmax_rowstats", ["neg_inf"]),
     "rowsum_8192sq": ("scale_8192", "rowsum", ["vec"]),
     "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect"]),
     "rowmax_8192sq": ("scale_8192", "rowmax_masked", ["neg_inf"]),
@@ -642,12 +644,20 @@ def run_cases(args):
                          tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_AUTO))
                 Wt = torch.empty(ws // 4, dtype=torch.float32, device=dev)
                 mk = lambda v: (lambda: tm.tm_colsum(X, Nw, Mw, Nw, O, Wt, ws, CT_, CN_, vm[v], 0, s))
+            elif kern == "softmax_rowstats":
+                O = torch.empty(Mw, dtype=torch.float32, device=dev)
+                O2 = torch.empty(Mw, dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw + 8 * Mw
+                fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
+                      "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
+                SB_, SC_ = tile or (4 if Nw < 4096 else 1, w.get("BC", 64))
+                mk = lambda v: (lambda: tm.tm_softmax_rowstats(X, Nw, Mw, Nw, O, O2, SB_, SC_, fm[v][0], fm[v][1], s))
             else:
                 O = torch.empty(Mw, dtype=torch.float32, device=dev)
                 nbytes = 4 * Mw * Nw + 4 * Mw
                 fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
                       "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
-                BR_, BC_ = tile or (ROWMAX_BR, w.get("BC", 64))
+                BR_, BC_ = tile or (4 if Nw < 4096 else ROWMAX_BR, w.get("BC", 64))
                 mk = lambda v: (lambda: tm.tm_rowmax_masked(X, Nw, Mw, Nw, O, BR_, BC_, fm[v][0], fm[v][1], s))
         chosen = variants if args.variant == "all" else [args.variant or variants[0]]
         for v in chosen:

@@ -213,6 +213,23 @@ tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N, fl
                            int32_t BC, tm_fill fill, uint32_t flags, tm_stream_t stream);
 
 /*
+ * tm_softmax_rowstats -- the softmax row statistics over ragged BC-column
+ * tiles: m[i] = max_{j < N} S[i, j] and l[i] = sum_{j < N} exp(S[i, j] - m[i]).
+ * "Slicing, bounds and masking", "Reductions over a ragged tile": the softmax
+ * is the second reduction a zero fill breaks; the remainder tile takes the
+ * masked load and the where(iota < N - kt, s, -inf) step, so padding is never
+ * the maximum and adds exp(-inf) = 0 to l.  TM_FILL_ZERO skips the where step
+ * (the pitfall: padding zeros enter both m and l).  N == 0 gives m = -inf and
+ * l = 0.  fp32 with CUDA's expf; l is within 1e-5 relative of the exact sum,
+ * m is exact.
+ *   S, lds   device input [M, lds]     m, l   device outputs, M floats each
+ *   BR, BC, flags   as tm_rowmax_masked
+ * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
+ */
+tm_status tm_softmax_rowstats(const float *S, int64_t lds, int64_t M, int64_t N, float *m, float *l,
+                              int32_t BR, int32_t BC, tm_fill fill, uint32_t flags, tm_stream_t stream);
+
+/*
  * tm_colsum_noalloc -- tm_colsum for callers that cannot allocate device
  * memory (no counterpart in the pages: a convenience of this library).  Code
  * running inside another framework that owns all device memory, under a fixed

@@ -61,6 +61,7 @@ SIGNATURES = {
     "tm_colsum_workspace_bytes": (_sz, [_i64, _i64, _i32, _i32, _st]),
     "tm_colsum": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _sz, _i32, _i32, _st, _u32, _vp]),
     "tm_rowmax_masked": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
+    "tm_softmax_rowstats": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _i32, _i32, _st, _u32, _vp]),
     "tm_colsum_noalloc": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
     "tm_check": (_st, [_vp]),
     "tm_tile_walk_probe": (_st, [_i64, _i32, _vp, _vp]),
@@ -172,6 +173,12 @@ def tm_rowmax_masked(S, lds: int, M: int, N: int, m, BR: int = 8, BC: int = 64,
                      fill: int = TM_FILL_NEG_INF, flags: int = 0, stream=None) -> None:
     _ok(load().tm_rowmax_masked(_ptr(S), lds, M, N, _ptr(m), BR, BC, fill, flags, _stream(stream)),
         "tm_rowmax_masked")
+
+
+def tm_softmax_rowstats(S, lds: int, M: int, N: int, m, l, BR: int = 8, BC: int = 64,
+                        fill: int = TM_FILL_NEG_INF, flags: int = 0, stream=None) -> None:
+    _ok(load().tm_softmax_rowstats(_ptr(S), lds, M, N, _ptr(m), _ptr(l), BR, BC, fill, flags, _stream(stream)),
+        "tm_softmax_rowstats")
 
 
 def tm_check(stream=None) -> None:
