@@ -650,14 +650,14 @@ def run_cases(args):
                 nbytes = 4 * Mw * Nw + 8 * Mw
                 fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
                       "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
-                SB_, SC_ = tile or (4 if Nw < 4096 else 1, w.get("BC", 64))
+                SB_, SC_ = tile or (16 if Nw < 4096 else 4, w.get("BC", 64))
                 mk = lambda v: (lambda: tm.tm_softmax_rowstats(X, Nw, Mw, Nw, O, O2, SB_, SC_, fm[v][0], fm[v][1], s))
             else:
                 O = torch.empty(Mw, dtype=torch.float32, device=dev)
                 nbytes = 4 * Mw * Nw + 4 * Mw
                 fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
                       "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
-                BR_, BC_ = tile or (4 if Nw < 4096 else ROWMAX_BR, w.get("BC", 64))
+                BR_, BC_ = tile or (16 if Nw < 4096 else ROWMAX_BR, w.get("BC", 64))
                 mk = lambda v: (lambda: tm.tm_rowmax_masked(X, Nw, Mw, Nw, O, BR_, BC_, fm[v][0], fm[v][1], s))
         chosen = variants if args.variant == "all" else [args.variant or variants[0]]
         for v in chosen:

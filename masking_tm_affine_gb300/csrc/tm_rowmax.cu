@@ -53,35 +53,30 @@ __global__ void __launch_bounds__(kThreads) rowmax_kernel(const float *__restric
         float mx = -INFINITY;
         if (live) {
             const float *sr = S + row * lds;
-            // whole tiles: no mask
-            int64_t v = ln;
-            for (; v + (int64_t)L * (U - 1) < prefix; v += (int64_t)L * U) {
+            // whole tiles: no mask.  U loads in flight per lane; in a partial
+            // last batch the lanes past the prefix hold -inf, the max identity
+            for (int64_t v = ln; v < prefix; v += (int64_t)L * U) {
+                const bool full = v + (int64_t)L * (U - 1) < prefix;
                 uint32_t w[U][EW];
 #pragma unroll
                 for (int q = 0; q < U; ++q) {
                     const float *p = sr + (v + (int64_t)L * q) * EW;
-                    if constexpr (VEC) {
-                        const u32x4 t = ld_nc_v4(p);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
-                    } else {
-                        w[q][0] = ld_nc_b32(p);
+                    for (int e = 0; e < EW; ++e) w[q][e] = as_u(-INFINITY);
+                    if (full || v + (int64_t)L * q < prefix) {
+                        if constexpr (VEC) {
+                            const u32x4 t = ld_nc_v4(p);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                        } else {
+                            w[q][0] = ld_nc_b32(p);
+                        }
                     }
                 }
 #pragma unroll
                 for (int q = 0; q < U; ++q)
 #pragma unroll
                     for (int e = 0; e < EW; ++e) mx = fmaxf(mx, as_f(w[q][e]));
-            }
-            for (; v < prefix; v += L) {
-                const float *p = sr + v * EW;
-                if constexpr (VEC) {
-                    const u32x4 t = ld_nc_v4(p);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) mx = fmaxf(mx, as_f(t.v[e]));
-                } else {
-                    mx = fmaxf(mx, as_f(ld_nc_b32(p)));
-                }
             }
             // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
             if (!ALIGNED && walk.masked) {

@@ -53,35 +53,31 @@ __global__ void __launch_bounds__(kThreads) rowsum_kernel(const float *__restric
         for (int e = 0; e < EW; ++e) acc[e] = 0.0f;
         if (live) {
             const float *xr = X + row * ldx;
-            // whole tiles: no mask
-            int64_t v = ln;
-            for (; v + (int64_t)L * (U - 1) < prefix; v += (int64_t)L * U) {
+            // whole tiles: no mask.  U loads in flight per lane; the last batch
+            // of a row may be partial (lanes past the prefix add nothing), but
+            // it still issues all its loads before the first add
+            for (int64_t v = ln; v < prefix; v += (int64_t)L * U) {
+                const bool full = v + (int64_t)L * (U - 1) < prefix;
                 uint32_t w[U][EW];
 #pragma unroll
                 for (int q = 0; q < U; ++q) {
                     const float *p = xr + (v + (int64_t)L * q) * EW;
-                    if constexpr (VEC) {
-                        const u32x4 t = ld_nc_v4(p);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
-                    } else {
-                        w[q][0] = ld_nc_b32(p);
+                    for (int e = 0; e < EW; ++e) w[q][e] = 0u;
+                    if (full || v + (int64_t)L * q < prefix) {
+                        if constexpr (VEC) {
+                            const u32x4 t = ld_nc_v4(p);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                        } else {
+                            w[q][0] = ld_nc_b32(p);
+                        }
                     }
                 }
 #pragma unroll
                 for (int q = 0; q < U; ++q)
 #pragma unroll
                     for (int e = 0; e < EW; ++e) acc[e] += as_f(w[q][e]);
-            }
-            for (; v < prefix; v += L) {
-                const float *p = xr + v * EW;
-                if constexpr (VEC) {
-                    const u32x4 t = ld_nc_v4(p);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[e] += as_f(t.v[e]);
-                } else {
-                    acc[0] += as_f(ld_nc_b32(p));
-                }
             }
             // the masked remainder tile: columns past N read as 0
             if (!ALIGNED && walk.masked) {

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
 {
     constexpr int L = kThreads / BR;   // lanes sharing a row
     constexpr int EW = VEC ? 4 : 1;
-    constexpr int U = VEC ? 8 : 16;    // accesses in flight per lane
+    constexpr int U = VEC ? 4 : 16;    // accesses in flight per lane (16 values per batch: fewer registers)
     constexpr int W = L > 32 ? L / 32 : 1;
     __shared__ float part_m[BR][W], part_l[BR][W];
 
@@ -86,19 +86,25 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
         float mx = -INFINITY, sum = 0.0f;
         if (live) {
             const float *sr = S + row * lds;
-            // whole tiles: no mask
-            int64_t v = ln;
-            for (; v + (int64_t)L * (U - 1) < prefix; v += (int64_t)L * U) {
+            // whole tiles: no mask.  U loads in flight per lane; in a partial
+            // last batch the lanes past the prefix hold -inf, which is never the
+            // maximum and adds exp(-inf) = 0
+            for (int64_t v = ln; v < prefix; v += (int64_t)L * U) {
+                const bool full = v + (int64_t)L * (U - 1) < prefix;
                 uint32_t w[U][EW];
 #pragma unroll
                 for (int q = 0; q < U; ++q) {
                     const float *p = sr + (v + (int64_t)L * q) * EW;
-                    if constexpr (VEC) {
-                        const u32x4 t = ld_nc_v4(p);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
-                    } else {
-                        w[q][0] = ld_nc_b32(p);
+                    for (int e = 0; e < EW; ++e) w[q][e] = as_u(-INFINITY);
+                    if (full || v + (int64_t)L * q < prefix) {
+                        if constexpr (VEC) {
+                            const u32x4 t = ld_nc_v4(p);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) w[q][e] = t.v[e];
+                        } else {
+                            w[q][0] = ld_nc_b32(p);
+                        }
                     }
                 }
                 float vals[U * EW];
@@ -106,18 +112,6 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
                 for (int q = 0; q < U; ++q)
 #pragma unroll
                     for (int e = 0; e < EW; ++e) vals[q * EW + e] = as_f(w[q][e]);
-                absorb(mx, sum, vals);
-            }
-            for (; v < prefix; v += L) {
-                const float *p = sr + v * EW;
-                float vals[EW];
-                if constexpr (VEC) {
-                    const u32x4 t = ld_nc_v4(p);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) vals[e] = as_f(t.v[e]);
-                } else {
-                    vals[0] = as_f(ld_nc_b32(p));
-                }
                 absorb(mx, sum, vals);
             }
             // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
