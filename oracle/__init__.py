@@ -68,6 +68,8 @@ def _load():
         lib.oracle_rowmax_masked.restype = i32
         lib.oracle_softmax_rowstats.argtypes = [vp, i64, i64, i64, i64, i32, vp, vp]
         lib.oracle_softmax_rowstats.restype = i32
+        lib.oracle_channel_affine.argtypes = [vp, i64, i64, i64, vp, vp, i64, i32, vp, i64]
+        lib.oracle_channel_affine.restype = i32
         _lib = lib
         return lib
 
@@ -183,3 +185,25 @@ def softmax_rowstats(S, lds: int, M: int, N: int, BC: int, fill: int = FILL_NEG_
     if _load().oracle_softmax_rowstats(_ptr(S), lds, M, N, BC, fill, _ptr(m), _ptr(l)) != 0:
         raise ValueError("softmax row statistics need BC > 0 and a known fill")
     return m, l
+
+
+CHANNELS_LAST = 0   # [N, C] view of [B, C, H, W]: channel = column
+CHANNELS_FIRST = 1  # [B*C, H*W] view: channel = row mod C
+
+
+def channel_affine(X, ldx: int, R: int, K: int, scale, bias, C: int, layout: int, Y: np.ndarray, ldy: int) -> None:
+    """In place on ``Y``: Y = X*scale[ch] + bias[ch] per channel, one rounding
+    ("Memory Coalescing and Tensor Layout", "NCHW versus NHWC")."""
+    X = _as_f32_flat(X)
+    if Y.dtype != np.float32 or not Y.flags.c_contiguous:
+        raise TypeError("Y must be a contiguous float32 array")
+    _check_2d(X, ldx, R, K, "X")
+    _check_2d(Y.reshape(-1), ldy, R, K, "Y")
+    sp = None if scale is None else _as_f32_flat(scale)
+    bp = None if bias is None else _as_f32_flat(bias)
+    for v in (sp, bp):
+        if v is not None and v.size < C:
+            raise ValueError("parameter vector shorter than C")
+    if _load().oracle_channel_affine(_ptr(X), ldx, R, K, None if sp is None else _ptr(sp),
+                                     None if bp is None else _ptr(bp), C, layout, _ptr(Y), ldy) != 0:
+        raise ValueError("channel affine needs C > 0, a known layout, and K <= C for channels last")

@@ -245,3 +245,37 @@ int oracle_softmax_rowstats(const float *S, int64_t lds, int64_t M, int64_t N,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* f3: per-channel scale and bias.  [MC] "NCHW versus NHWC": a per-channel   */
+/* scale and bias wants the channel to be the fast dimension, which a         */
+/* [B, C, H, W] tensor reinterpreted as [N, C] with N = B*H*W gives without  */
+/* moving data (channels last, layout 0: channel = column j); with channels  */
+/* first the same tensor is [B*C, H*W] and the channel of row i is i mod C   */
+/* (layout 1).  Y[i, j] = X[i, j] * scale[ch] + bias[ch], rounded once (a    */
+/* fused multiply-add, C's fmaf); a NULL scale means x + bias and a NULL     */
+/* bias x * scale, each rounded once.  In-bounds elements only.              */
+/* ------------------------------------------------------------------------ */
+int oracle_channel_affine(const float *X, int64_t ldx, int64_t R, int64_t K,
+                          const float *scale, const float *bias, int64_t C,
+                          int layout, float *Y, int64_t ldy)
+{
+    int64_t i, j;
+    if (C <= 0 || (layout != 0 && layout != 1) || (layout == 0 && K > C))
+        return -1;
+    for (i = 0; i < R; ++i)
+        for (j = 0; j < K; ++j) {
+            int64_t ch = layout == 0 ? j : i % C;
+            float x = X[i * ldx + j], y;
+            if (scale != NULL && bias != NULL)
+                y = fmaf(x, scale[ch], bias[ch]);
+            else if (scale != NULL)
+                y = x * scale[ch];
+            else if (bias != NULL)
+                y = x + bias[ch];
+            else
+                y = x;
+            Y[i * ldy + j] = y;
+        }
+    return 0;
+}

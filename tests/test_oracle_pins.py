@@ -438,3 +438,63 @@ def test_softmax_stats_empty_and_infinite(oracle):
     s[0, 3] = -5.0
     m, l = oracle.softmax_rowstats(s, 10, 1, 10, 16)
     assert m[0] == np.float32(-5.0) and l[0] == 1.0
+
+
+# --------------------------------------------------------------------------
+# Per-channel scale and bias ("Memory Coalescing and Tensor Layout", "NCHW versus NHWC")
+# --------------------------------------------------------------------------
+def _fma_exact(x, s, b):
+    """fl(x*s + b) with one rounding: the exact rational, rounded to float32."""
+    return _round_exact_to_f32(Fraction(float(x)) * Fraction(float(s)) + Fraction(float(b)))
+
+
+def test_channel_affine_single_rounding(oracle):
+    g = synth.rng(31)
+    R, C = 40, 12
+    x = synth.normal((R, C), 32)
+    sc = synth.uniform((C,), 0.25, 4.0, 33)
+    bi = synth.normal((C,), 34)
+    Y = np.zeros(R * C, np.float32)
+    oracle.channel_affine(x, C, R, C, sc, bi, C, oracle.CHANNELS_LAST, Y, C)
+    Yv = Y.reshape(R, C)
+    for i in range(0, R, 3):
+        for j in range(C):
+            assert f32_bits(Yv[i, j]) == f32_bits(_fma_exact(x[i, j], sc[j], bi[j]))
+
+
+def test_channel_affine_layouts_agree_with_4d_broadcast(oracle):
+    # the same [B, C, H, W] tensor through both views equals numpy's fp64
+    # broadcast rounded to fp32 (that double rounding could differ from one
+    # rounding at rare ties -- none occurs for these seeded values; the exact
+    # rational test above pins the single rounding itself)
+    B, C, H, W = 3, 5, 4, 6
+    t = synth.normal((B, C, H, W), 35)
+    sc = synth.uniform((C,), 0.5, 2.0, 36)
+    bi = synth.uniform((C,), -1.0, 1.0, 37)
+    want = (t.astype(np.float64) * sc[None, :, None, None] + bi[None, :, None, None]).astype(np.float32)
+    # channels first: rows b*C + c of length H*W
+    Y1 = np.zeros(t.size, np.float32)
+    oracle.channel_affine(t.reshape(-1), H * W, B * C, H * W, sc, bi, C, oracle.CHANNELS_FIRST, Y1, H * W)
+    assert np.array_equal(Y1.reshape(B, C, H, W), want)
+    # channels last: the NHWC copy as [B*H*W, C]
+    nhwc = np.ascontiguousarray(t.transpose(0, 2, 3, 1))
+    Y2 = np.zeros(t.size, np.float32)
+    oracle.channel_affine(nhwc.reshape(-1), C, B * H * W, C, sc, bi, C, oracle.CHANNELS_LAST, Y2, C)
+    assert np.array_equal(Y2.reshape(B, H, W, C).transpose(0, 3, 1, 2), want)
+
+
+def test_channel_affine_bias_only_scale_only_and_gaps(oracle):
+    R, K, ld = 7, 9, 13
+    x = synth.normal((R, K), 38)
+    X = synth.pad_rows(x, ld)
+    bi = synth.normal((K,), 39)
+    sc = synth.normal((K,), 40)
+    Y = np.full(R * ld, synth.CANARY_U32, np.uint32).view(np.float32)
+    oracle.channel_affine(X, ld, R, K, None, bi, K, oracle.CHANNELS_LAST, Y, ld)
+    Yv = Y.reshape(R, ld)
+    assert np.array_equal(Yv[:, :K], x + bi[None, :])            # one rounding of x + b
+    assert np.all(f32_bits(Yv[:, K:]) == synth.CANARY_U32)
+    oracle.channel_affine(X, ld, R, K, sc, None, K, oracle.CHANNELS_LAST, Y, ld)
+    assert np.array_equal(Yv[:, :K], x * sc[None, :])            # one rounding of x * s
+    with pytest.raises(ValueError):
+        oracle.channel_affine(X, ld, R, K, sc, bi, K - 1, oracle.CHANNELS_LAST, Y, ld)
