@@ -581,6 +581,8 @@ CASES = {
     "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive"]),
     "rowmax_8192": ("rowmax_8192", "rowmax_masked", ["neg_inf", "zero", "scalar"]),
     "softmax_8192": ("rowmax_8192", "softmax_rowstats", ["neg_inf", "zero", "scalar"]),
+    "channel_nhwc": ("channel_nhwc", "channel_affine", ["auto", "scalar"]),
+    "channel_nchw": ("channel_nchw", "channel_affine", ["auto", "scalar"]),
     # the reductions on the [8192, 8192] batch of the step, for tile tuning
     "softmax_8192sq": ("scale_8192", "softmax_rowstats", ["neg_inf"]),
     "rowsum_8192sq": ("scale_8192", "rowsum", ["vec"]),
@@ -644,6 +646,16 @@ def run_cases(args):
                          tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_AUTO))
                 Wt = torch.empty(ws // 4, dtype=torch.float32, device=dev)
                 mk = lambda v: (lambda: tm.tm_colsum(X, Nw, Mw, Nw, O, Wt, ws, CT_, CN_, vm[v], 0, s))
+            elif kern == "channel_affine":
+                O = torch.empty_like(X)
+                nbytes = 8 * Mw * Nw + 8 * w["C"]
+                scv, biv = synth.channel_params(w["C"])
+                SC = torch.from_numpy(scv).to(dev)
+                BI = torch.from_numpy(biv).to(dev)
+                TM_, TN_ = tile or (w["TM"], w["TN"])
+                fl = {"auto": 0, "scalar": tm.TM_PATH_SCALAR}
+                mk = lambda v: (lambda: tm.tm_channel_affine(X, Nw, Mw, Nw, SC, BI, w["C"], w["layout"], O, Nw,
+                                                             TM_, TN_, fl[v], s))
             elif kern == "softmax_rowstats":
                 O = torch.empty(Mw, dtype=torch.float32, device=dev)
                 O2 = torch.empty(Mw, dtype=torch.float32, device=dev)

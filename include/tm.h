@@ -148,6 +148,30 @@ tm_status tm_copy2d(const float *A, int64_t lda, float *B, int64_t ldb, int64_t 
                     int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream);
 
 /*
+ * tm_channel_affine -- per-channel scale and bias over a [B, C, H, W] tensor,
+ * Y = X * scale[ch] + bias[ch] rounded once (fused multiply-add); a NULL scale
+ * gives X + bias, a NULL bias X * scale (each rounded once).  "Memory
+ * Coalescing and Tensor Layout", "NCHW versus NHWC": the operation wants the
+ * channel as the fast dimension, which reinterpreting the tensor (no data
+ * moved) provides:
+ *   layout TM_CHANNELS_LAST  -- X is [R, K] = [B*H*W, C]: channel = column j
+ *                               (requires K <= C);
+ *   layout TM_CHANNELS_FIRST -- X is [R, K] = [B*C, H*W]: channel = i mod C
+ *                               (requires R < 2^31).
+ * Same tiles, flags, paths, masking and in-place rule as tm_scale2d.
+ *   scale, bias   device vectors of C floats, or NULL; never overlapping Y.
+ *                 With channels last, the vector paths need 16-byte aligned
+ *                 parameter vectors (otherwise the scalar path is taken).
+ * Errors: INVALID_ARG (also C <= 0, unknown layout), UNSUPPORTED_TILE,
+ *         MISALIGNED, BROKEN_PROMISE, CUDA.
+ */
+#define TM_CHANNELS_LAST 0
+#define TM_CHANNELS_FIRST 1
+tm_status tm_channel_affine(const float *X, int64_t ldx, int64_t R, int64_t K, const float *scale,
+                            const float *bias, int64_t C, int32_t layout, float *Y, int64_t ldy, int32_t TM,
+                            int32_t TN, uint32_t flags, tm_stream_t stream);
+
+/*
  * tm_rowsum -- r[i] = sum_j X[i, j] (fp32 accumulation), the stride-1 walk of
  * "Memory Coalescing and Tensor Layout", "What it actually costs".  Each row
  * is walked in TN-column tiles: the whole tiles unmasked, then one masked

@@ -55,6 +55,24 @@ __device__ __forceinline__ u32x8 ld_nc_v8(const void *p)
     return r;
 }
 
+// Cached read-only loads for small vectors every row reuses (per-channel
+// parameters): these keep the default L1 allocation.
+__device__ __forceinline__ uint32_t ldg_b32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ u32x4 ldg_v4(const void *p)
+{
+    u32x4 r;
+    asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
+                 : "l"(p));
+    return r;
+}
+
 // ---------------------------------------------------------------- stores
 __device__ __forceinline__ void st_b32(void *p, uint32_t x)
 {

@@ -24,7 +24,7 @@
 namespace libtm {
 namespace {
 
-enum class Op { Scale, Copy };
+enum class Op { Scale, Copy, Channel };
 enum class Path { Aligned, RaggedVec, Scalar };
 
 struct Map2dArgs {
@@ -36,6 +36,11 @@ struct Map2dArgs {
     uint32_t ntiles;   // ceil(M / TM) * tiles_n
     FastDiv div_tiles_n;
     unsigned *status;
+    // Op::Channel only: per-channel parameters (either may be NULL)
+    const float *scale, *bias;
+    int layout;       // 0: channel = column j; 1: channel = row i mod C
+    uint32_t C;
+    FastDiv div_C;
 };
 
 template <Op OP>
@@ -43,6 +48,32 @@ __device__ __forceinline__ uint32_t apply(uint32_t x, float alpha)
 {
     if (OP == Op::Copy) return x;                 // bitwise: no arithmetic touches the word
     return as_u(__fmul_rn(alpha, as_f(x)));       // one rounding, like the oracle
+}
+
+// y = x*s + b rounded once (fused), or x*s / x + b when a vector is absent.
+__device__ __forceinline__ uint32_t apply_channel(uint32_t x, float s, float b, bool has_s, bool has_b)
+{
+    if (has_s && has_b) return as_u(__fmaf_rn(as_f(x), s, b));
+    if (has_s) return as_u(__fmul_rn(as_f(x), s));
+    if (has_b) return as_u(__fadd_rn(as_f(x), b));
+    return x;
+}
+
+// EW consecutive per-channel parameters starting at channel ch (16-byte
+// aligned when EW >= 4: the host picks a scalar path otherwise).
+template <int EW>
+__device__ __forceinline__ void load_params(const float *v, uint32_t ch, float (&out)[EW])
+{
+    if constexpr (EW == 1) {
+        out[0] = as_f(ldg_b32(v + ch));
+    } else {
+#pragma unroll
+        for (int h = 0; h < EW; h += 4) {
+            const u32x4 t = ldg_v4(v + ch + h);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) out[h + e] = as_f(t.v[e]);
+        }
+    }
 }
 
 template <int EW>
@@ -118,6 +149,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
         for (int b = 0; b < U; b += UB) {
             Vec<EW> val[UB];
             int64_t yoff[UB];
+            uint32_t chan[UB];  // Op::Channel: the first element's channel (C < 2^31)
             bool live[UB];
 #pragma unroll
             for (int u = 0; u < UB; ++u) {
@@ -134,6 +166,8 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
                 if constexpr (P != Path::Aligned) in = in && (i < p.M) && (j < p.N);
                 live[u] = in;
                 yoff[u] = i * p.ldy + j;
+                if constexpr (OP == Op::Channel)
+                    chan[u] = p.layout == 0 ? (uint32_t)j : (uint32_t)i - fdiv((uint32_t)i, p.div_C) * p.C;
                 if (in) {
                     val[u] = load_vec<EW>(p.X + i * p.ldx + j);
                 } else {
@@ -145,8 +179,29 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
             for (int u = 0; u < UB; ++u) {
                 if (!live[u]) continue;                              // a masked store is skipped
                 Vec<EW> o;
+                if constexpr (OP == Op::Channel) {
+                    // per-channel scale and bias: along the row (channels last)
+                    // or one pair per row (channels first)
+                    const bool hs = p.scale != nullptr, hb = p.bias != nullptr;
+                    float sv[EW], bv[EW];
+                    if (p.layout == 0) {
+                        if (hs) load_params<EW>(p.scale, chan[u], sv);
+                        if (hb) load_params<EW>(p.bias, chan[u], bv);
+                    } else {
+                        const float s1 = hs ? as_f(ldg_b32(p.scale + chan[u])) : 0.0f;
+                        const float b1 = hb ? as_f(ldg_b32(p.bias + chan[u])) : 0.0f;
 #pragma unroll
-                for (int e = 0; e < EW; ++e) o.v[e] = apply<OP>(val[u].v[e], p.alpha);
+                        for (int e = 0; e < EW; ++e) {
+                            sv[e] = s1;
+                            bv[e] = b1;
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) o.v[e] = apply_channel(val[u].v[e], sv[e], bv[e], hs, hb);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) o.v[e] = apply<OP>(val[u].v[e], p.alpha);
+                }
                 store_vec<EW>(p.Y + yoff[u], o);
             }
         }
@@ -194,10 +249,35 @@ bool tile_supported(int TM, int TN)
            (TM == 64 && TN == 64) || (TM == 32 && TN == 128) || (TM == 128 && TN == 128);
 }
 
+// Per-channel parameters of Op::Channel (see tm_channel_affine).
+struct ChannelParams {
+    const float *scale, *bias;
+    int64_t C;
+    int layout;
+};
+
 tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M, int64_t N,
-                float alpha, int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream, bool check_promise)
+                float alpha, int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream, bool check_promise,
+                const ChannelParams *ch = nullptr)
 {
     if (!valid2d(X, ldx, M, N) || !valid2d(Y, ldy, M, N)) return TM_ERR_INVALID_ARG;
+    bool params16 = true;  // every present parameter vector is 16-byte aligned
+    if (op == Op::Channel) {
+        if (ch->C <= 0 || ch->C > INT32_MAX || (ch->layout != 0 && ch->layout != 1)) return TM_ERR_INVALID_ARG;
+        if (ch->layout == 0 && N > ch->C) return TM_ERR_INVALID_ARG;
+        if (ch->layout == 1 && M > INT32_MAX) return TM_ERR_INVALID_ARG;
+        for (const float *v : {ch->scale, ch->bias}) {
+            if (v == nullptr) continue;
+            if (!aligned_to(v, 4)) return TM_ERR_MISALIGNED;
+            params16 = params16 && aligned_to(v, 16);
+            if (M > 0 && N > 0) {
+                uintptr_t ylo, yhi, vlo = reinterpret_cast<uintptr_t>(v), vhi = vlo + (uintptr_t)ch->C * 4;
+                span2d(Y, ldy, M, N, &ylo, &yhi);
+                if (!(yhi <= vlo || vhi <= ylo)) return TM_ERR_INVALID_ARG;
+            }
+        }
+        if (ch->layout == 1) params16 = true;  // one scalar parameter per row: no vector loads
+    }
     if (!flags_ok(flags, TM_ALIGNED | kPathBits)) return TM_ERR_INVALID_ARG;
     if (TM <= 0 || TN <= 0 || !tile_supported(TM, TN)) return TM_ERR_UNSUPPORTED_TILE;
     if (!overlap_ok(X, ldx, Y, ldy, M, N)) return TM_ERR_INVALID_ARG;
@@ -206,6 +286,7 @@ tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64
 
     const bool vec16 = aligned_to(X, 16) && aligned_to(Y, 16) && ldx % 4 == 0 && ldy % 4 == 0;
     const bool vec32 = aligned_to(X, 32) && aligned_to(Y, 32) && ldx % 8 == 0 && ldy % 8 == 0 && TN % 8 == 0;
+    if (!params16) flags |= TM_PATH_SCALAR;  // parameters read per element
     Path path;
     int ew = 4;
     if (flags & TM_ALIGNED) {
@@ -214,12 +295,14 @@ tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64
             if (M % TM != 0 || N % TN != 0) return TM_ERR_BROKEN_PROMISE;
         }
         if (flags & TM_PATH_SCALAR) {
+            if (flags & TM_PATH_VEC) return TM_ERR_MISALIGNED;
             path = Path::Scalar;
         } else {
             path = Path::Aligned;
             ew = (vec32 && !(flags & TM_PATH_VEC) && check_promise) ? 8 : 4;
         }
     } else if (flags & TM_PATH_SCALAR) {
+        if (flags & TM_PATH_VEC) return TM_ERR_MISALIGNED;
         path = Path::Scalar;
     } else if (vec16 && N % 4 == 0) {
         path = Path::RaggedVec;
@@ -248,7 +331,13 @@ tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64
     a.ntiles = (uint32_t)(tiles_m * tiles_n);
     a.div_tiles_n = make_fastdiv((uint32_t)tiles_n);
     a.status = dev->status;
+    a.scale = op == Op::Channel ? ch->scale : nullptr;
+    a.bias = op == Op::Channel ? ch->bias : nullptr;
+    a.layout = op == Op::Channel ? ch->layout : 0;
+    a.C = op == Op::Channel ? (uint32_t)ch->C : 1u;
+    a.div_C = make_fastdiv(a.C);
     cudaStream_t s = as_stream(stream);
+    if (op == Op::Channel) return dispatch<Op::Channel>(TM, TN, path, ew, a, s);
     return op == Op::Scale ? dispatch<Op::Scale>(TM, TN, path, ew, a, s)
                            : dispatch<Op::Copy>(TM, TN, path, ew, a, s);
 }
@@ -274,4 +363,12 @@ extern "C" tm_status tm_scale2d_unchecked(const float *X, int64_t ldx, float *Y,
                                           int64_t N, float alpha, int32_t TM, int32_t TN, tm_stream_t stream)
 {
     return map2d(Op::Scale, X, ldx, Y, ldy, M, N, alpha, TM, TN, TM_ALIGNED, stream, false);
+}
+
+extern "C" tm_status tm_channel_affine(const float *X, int64_t ldx, int64_t R, int64_t K, const float *scale,
+                                       const float *bias, int64_t C, int32_t layout, float *Y, int64_t ldy,
+                                       int32_t TM, int32_t TN, uint32_t flags, tm_stream_t stream)
+{
+    const ChannelParams ch{scale, bias, C, layout};
+    return map2d(Op::Channel, X, ldx, Y, ldy, R, K, 0.0f, TM, TN, flags, stream, true, &ch);
 }

@@ -68,7 +68,19 @@ WORKLOADS = {
     "coalesce_4096": dict(kind="sums", M=4096, N=4096, dist=("uniform", 0.0, 1.0), seed=3),
     "rowmax_8192": dict(kind="rowmax", M=8192, N=1000, dist=("uniform", -30.0, -1.0), seed=4,
                         BC=64),
+    # per-channel scale and bias ("Memory Coalescing and Tensor Layout", "NCHW versus
+    # NHWC"): an activation-shaped [B, C, H, W] = [32, 256, 56, 56] fp32 tensor
+    # (25.7M elements, 103 MB) read as [B*H*W, C] (channels last) or [B*C, H*W]
+    "channel_nhwc": dict(kind="channel", M=32 * 56 * 56, N=256, C=256, layout=0,
+                         dist=("normal",), seed=5, TM=32, TN=128),
+    "channel_nchw": dict(kind="channel", M=32 * 256, N=56 * 56, C=256, layout=1,
+                         dist=("normal",), seed=5, TM=32, TN=128),
 }
+
+
+def channel_params(C: int, seed: int = 6):
+    """Per-channel scale in [0.5, 2) and bias ~ N(0, 1)."""
+    return uniform((C,), 0.5, 2.0, seed), normal((C,), seed + 1)
 
 
 def draw(dist, shape, seed: int) -> np.ndarray:

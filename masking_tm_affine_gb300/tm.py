@@ -57,6 +57,7 @@ SIGNATURES = {
     "tm_affine": (_st, [_vp, _vp, _i64, _st, _vp]),
     "tm_scale2d": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _u32, _vp]),
     "tm_copy2d": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _i32, _i32, _u32, _vp]),
+    "tm_channel_affine": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _i32, _u32, _vp]),
     "tm_rowsum": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _u32, _vp]),
     "tm_colsum_workspace_bytes": (_sz, [_i64, _i64, _i32, _i32, _st]),
     "tm_colsum": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _sz, _i32, _i32, _st, _u32, _vp]),
@@ -140,6 +141,16 @@ def tm_scale2d(X, ldx: int, Y, ldy: int, M: int, N: int, alpha: float, TM: int, 
 def tm_copy2d(A, lda: int, B, ldb: int, M: int, N: int, TM: int, TN: int, flags: int = 0,
               stream=None) -> None:
     _ok(load().tm_copy2d(_ptr(A), lda, _ptr(B), ldb, M, N, TM, TN, flags, _stream(stream)), "tm_copy2d")
+
+
+TM_CHANNELS_LAST = 0
+TM_CHANNELS_FIRST = 1
+
+
+def tm_channel_affine(X, ldx: int, R: int, K: int, scale, bias, C: int, layout: int, Y, ldy: int,
+                      TM: int = 32, TN: int = 128, flags: int = 0, stream=None) -> None:
+    _ok(load().tm_channel_affine(_ptr(X), ldx, R, K, _ptr(scale), _ptr(bias), C, layout, _ptr(Y), ldy, TM, TN,
+                                 flags, _stream(stream)), "tm_channel_affine")
 
 
 def tm_rowsum(X, ldx: int, M: int, N: int, r, TM: int = 8, TN: int = 512, flags: int = 0,
