@@ -70,6 +70,12 @@ def _load():
         lib.oracle_softmax_rowstats.restype = i32
         lib.oracle_channel_affine.argtypes = [vp, i64, i64, i64, vp, vp, i64, i32, vp, i64]
         lib.oracle_channel_affine.restype = i32
+        lib.oracle_padded_extent.argtypes = [i64, vp, i32]
+        lib.oracle_padded_extent.restype = i64
+        lib.oracle_row_stride.argtypes = [i64, i32]
+        lib.oracle_row_stride.restype = i64
+        lib.oracle_pad2d.argtypes = [vp, i64, i64, i64, vp, i64, i64, i64]
+        lib.oracle_pad2d.restype = None
         _lib = lib
         return lib
 
@@ -207,3 +213,34 @@ def channel_affine(X, ldx: int, R: int, K: int, scale, bias, C: int, layout: int
     if _load().oracle_channel_affine(_ptr(X), ldx, R, K, None if sp is None else _ptr(sp),
                                      None if bp is None else _ptr(bp), C, layout, _ptr(Y), ldy) != 0:
         raise ValueError("channel affine needs C > 0, a known layout, and K <= C for channels last")
+
+
+def padded_extent(extent: int, tiles) -> int:
+    """Smallest extent >= the given one that every candidate tile divides
+    ("@aligned", "Interactions")."""
+    t = np.ascontiguousarray(tiles, dtype=np.int32)
+    r = _load().oracle_padded_extent(extent, _ptr(t), t.size)
+    if r < 0:
+        raise ValueError("bad extent or tiles")
+    return int(r)
+
+
+def row_stride(N: int, align_bytes: int = 16) -> int:
+    """Smallest row stride >= N whose rows are whole multiples of align_bytes
+    ("Memory Coalescing and Tensor Layout", "The alignment constraint")."""
+    r = _load().oracle_row_stride(N, align_bytes)
+    if r < 0:
+        raise ValueError("bad N or alignment")
+    return int(r)
+
+
+def pad2d(A, lda: int, M: int, N: int, B: np.ndarray, ldb: int, Mp: int, Np: int) -> None:
+    """In place on ``B``: A inside [M, N], zeros in the rest of [Mp, Np]."""
+    A = np.ascontiguousarray(A).reshape(-1).view(np.uint32)
+    if B.dtype.itemsize != 4 or not B.flags.c_contiguous:
+        raise TypeError("B must be a contiguous 4-byte array")
+    if Mp < M or Np < N:
+        raise ValueError("padded extents must cover the source")
+    _check_2d(A, lda, M, N, "A")
+    _check_2d(B.reshape(-1), ldb, Mp, Np, "B")
+    _load().oracle_pad2d(_ptr(A), lda, M, N, _ptr(B), ldb, Mp, Np)

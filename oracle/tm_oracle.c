@@ -279,3 +279,54 @@ int oracle_channel_affine(const float *X, int64_t ldx, int64_t R, int64_t K,
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* f2: keeping the promise by padding.  [AL] "Interactions": when the tile   */
+/* sizes come from a tuner, the promise has to hold for every candidate, so  */
+/* the host pads (or picks) extents that every candidate divides.  [MC] "The  */
+/* alignment constraint": rows that must start on 16 bytes get a padded row  */
+/* stride, and kernels use that stride.  Written as the searches they are.   */
+/* ------------------------------------------------------------------------ */
+
+/* Smallest e >= extent that every tile divides; -1 on bad input. */
+int64_t oracle_padded_extent(int64_t extent, const int32_t *tiles, int32_t ntiles)
+{
+    int64_t e;
+    int32_t k;
+    if (extent < 0 || ntiles <= 0)
+        return -1;
+    for (k = 0; k < ntiles; ++k)
+        if (tiles[k] <= 0)
+            return -1;
+    for (e = extent;; ++e) {
+        int ok = 1;
+        for (k = 0; k < ntiles && ok; ++k)
+            if (e % tiles[k] != 0)
+                ok = 0;
+        if (ok)
+            return e;
+    }
+}
+
+/* Smallest row stride ld >= N (in floats) whose byte length is a multiple */
+/* of align_bytes; -1 on bad input.                                         */
+int64_t oracle_row_stride(int64_t N, int32_t align_bytes)
+{
+    int64_t ld;
+    if (N < 0 || align_bytes <= 0 || align_bytes % 4 != 0)
+        return -1;
+    for (ld = N;; ++ld)
+        if ((ld * 4) % align_bytes == 0)
+            return ld;
+}
+
+/* B[i, j] = A[i, j] inside [M, N], 0 in the rest of [Mp, Np] (the value a   */
+/* masked load reads); words of B outside [Mp, Np] are not written.          */
+void oracle_pad2d(const uint32_t *A, int64_t lda, int64_t M, int64_t N,
+                  uint32_t *B, int64_t ldb, int64_t Mp, int64_t Np)
+{
+    int64_t i, j;
+    for (i = 0; i < Mp; ++i)
+        for (j = 0; j < Np; ++j)
+            B[i * ldb + j] = (i < M && j < N) ? A[i * lda + j] : 0u;
+}

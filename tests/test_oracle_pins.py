@@ -498,3 +498,56 @@ def test_channel_affine_bias_only_scale_only_and_gaps(oracle):
     assert np.array_equal(Yv[:, :K], x * sc[None, :])            # one rounding of x * s
     with pytest.raises(ValueError):
         oracle.channel_affine(X, ld, R, K, sc, bi, K - 1, oracle.CHANNELS_LAST, Y, ld)
+
+
+# --------------------------------------------------------------------------
+# Keeping the promise by padding ("@aligned", "Interactions";
+# "Memory Coalescing and Tensor Layout", "The alignment constraint")
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("extent", [0, 1, 31, 32, 33, 255, 256, 1000, 4100, 8192, 8193])
+@pytest.mark.parametrize("tiles", [[32], [64], [32, 256], [4, 16], [64, 128, 256], [3, 5]])
+def test_padded_extent_is_lcm_multiple(oracle, extent, tiles):
+    L = math.lcm(*tiles)
+    got = oracle.padded_extent(extent, tiles)
+    assert got == -(-extent // L) * L                      # round up to the lcm (math.lcm as reference)
+    assert all(oracle.promise_kept(got, got, t, t) for t in tiles)
+
+
+def test_padded_extent_autotune_pairing(oracle):
+    # the gemm's tuner picks TILE_M from {32, 256}: the host must pad M to a
+    # multiple of 256 so that whichever it picks, the promise holds
+    assert oracle.padded_extent(1000, [32, 256]) == 1024
+    assert oracle.padded_extent(4100, [32, 256]) == 4352
+    assert oracle.padded_extent(4100, [64]) == 4160
+    with pytest.raises(ValueError):
+        oracle.padded_extent(10, [0])
+
+
+def test_row_stride_16_byte_rows(oracle):
+    # 16-byte rows are four fp32 elements: N rounds up to a multiple of 4
+    for N in range(0, 40):
+        assert oracle.row_stride(N, 16) == -(-N // 4) * 4
+        assert oracle.row_stride(N, 32) == -(-N // 8) * 8
+    assert oracle.row_stride(1000, 16) == 1000 and oracle.row_stride(1001, 16) == 1004
+    with pytest.raises(ValueError):
+        oracle.row_stride(10, 6)
+
+
+@pytest.mark.parametrize("M,N,Mp,Np,lda,ldb", [(5, 7, 8, 8, 7, 8), (0, 3, 4, 4, 3, 4), (3, 0, 4, 4, 1, 6),
+                                               (20, 28, 32, 32, 28, 36), (4100, 1000, 4160, 1024, 1000, 1024)])
+def test_pad2d_definition_and_sum_invariance(oracle, M, N, Mp, Np, lda, ldb):
+    x = synth.normal((max(M, 1), max(N, 1)), 60)[:M, :N]
+    A = synth.pad_rows(x, lda) if M and N else np.zeros(max(M * lda, 1), np.float32)
+    B = np.full(Mp * ldb + 16, synth.CANARY_U32, np.uint32)
+    oracle.pad2d(A, lda, M, N, B, ldb, Mp, Np)
+    Bv = B[:Mp * ldb].reshape(Mp, ldb)
+    want = np.zeros((Mp, Np), np.float32)
+    want[:M, :N] = x                                        # numpy slicing as the reference
+    assert np.array_equal(Bv[:, :Np].view(np.float32), want)
+    assert np.all(Bv[:, Np:] == synth.CANARY_U32) and np.all(B[Mp * ldb:] == synth.CANARY_U32)
+    if M and N:
+        # zero padding is the masked-load value: sums over the padded tensor are
+        # the sums over the original, exactly
+        Bf = Bv.view(np.float32).reshape(-1)
+        assert np.array_equal(oracle.rowsum(Bf, ldb, Mp, Np)[:M], oracle.rowsum(A, lda, M, N))
+        assert np.array_equal(oracle.colsum(Bf, ldb, Mp, Np)[:N], oracle.colsum(A, lda, M, N))
