@@ -581,6 +581,7 @@ CASES = {
     "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive"]),
     "rowmax_8192": ("rowmax_8192", "rowmax_masked", ["neg_inf", "zero", "scalar"]),
     "softmax_8192": ("rowmax_8192", "softmax_rowstats", ["neg_inf", "zero", "scalar"]),
+    "pad_ragged": ("ragged_4100", "pad2d", ["auto"]),
     "channel_nhwc": ("channel_nhwc", "channel_affine", ["auto", "scalar"]),
     "channel_nchw": ("channel_nchw", "channel_affine", ["auto", "scalar"]),
     # the reductions on the [8192, 8192] batch of the step, for tile tuning
@@ -646,6 +647,12 @@ def run_cases(args):
                          tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_AUTO))
                 Wt = torch.empty(ws // 4, dtype=torch.float32, device=dev)
                 mk = lambda v: (lambda: tm.tm_colsum(X, Nw, Mw, Nw, O, Wt, ws, CT_, CN_, vm[v], 0, s))
+            elif kern == "pad2d":
+                Mp_, Np_ = tm.tm_padded_extent(Mw, [w["TM"]]), tm.tm_padded_extent(Nw, [w["TN"]])
+                ldp = tm.tm_row_stride(Np_, 16)
+                O = torch.empty(Mp_ * ldp, dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw + 4 * Mp_ * Np_
+                mk = lambda v: (lambda: tm.tm_pad2d(X, Nw, Mw, Nw, O, ldp, Mp_, Np_, s))
             elif kern == "channel_affine":
                 O = torch.empty_like(X)
                 nbytes = 8 * Mw * Nw + 8 * w["C"]

@@ -172,6 +172,34 @@ tm_status tm_channel_affine(const float *X, int64_t ldx, int64_t R, int64_t K, c
                             int32_t TN, uint32_t flags, tm_stream_t stream);
 
 /*
+ * Keeping the promise by padding.  "@aligned", "Interactions": when tiles come
+ * from a tuner the promise must hold for every candidate, so the host pads the
+ * extents; "Memory Coalescing and Tensor Layout", "The alignment constraint":
+ * rows that must start on 16 bytes get a padded stride, and that stride -- not
+ * the shape -- is what kernels are given.
+ *
+ * tm_padded_extent -- the smallest extent >= `extent` that every one of the
+ * ntiles candidate tiles (a HOST array of positive ints) divides: `extent`
+ * rounded up to their least common multiple.  -1 on bad input or overflow.
+ * Host only, no CUDA call.
+ *
+ * tm_row_stride -- the smallest row stride >= N (in floats) whose rows are a
+ * whole multiple of align_bytes (a power of two, >= 4): 16 gives N rounded up
+ * to a multiple of 4.  -1 on bad input.  Host only.
+ *
+ * tm_pad2d -- B[i, j] = A[i, j] for i < M, j < N and B[i, j] = 0 for the rest
+ * of [Mp, Np] (the value a masked load reads, so sums over B equal sums over A
+ * and the aligned path can run on B).  Words of B outside [Mp, Np] are not
+ * written.  A and B must not overlap.  Requires Mp >= M, Np >= N, lda >= N,
+ * ldb >= Np.  16-byte vectors when B, ldb, Np (and A, lda, N) allow.
+ * Errors: INVALID_ARG, MISALIGNED (a pointer not 4-byte aligned), CUDA.
+ */
+int64_t tm_padded_extent(int64_t extent, const int32_t *tiles, int32_t ntiles);
+int64_t tm_row_stride(int64_t N, int32_t align_bytes);
+tm_status tm_pad2d(const float *A, int64_t lda, int64_t M, int64_t N, float *B, int64_t ldb, int64_t Mp,
+                   int64_t Np, tm_stream_t stream);
+
+/*
  * tm_rowsum -- r[i] = sum_j X[i, j] (fp32 accumulation), the stride-1 walk of
  * "Memory Coalescing and Tensor Layout", "What it actually costs".  Each row
  * is walked in TN-column tiles: the whole tiles unmasked, then one masked

@@ -24,7 +24,7 @@
 namespace libtm {
 namespace {
 
-enum class Op { Scale, Copy, Channel };
+enum class Op { Scale, Copy, Channel, Pad };
 enum class Path { Aligned, RaggedVec, Scalar };
 
 struct Map2dArgs {
@@ -41,12 +41,14 @@ struct Map2dArgs {
     int layout;       // 0: channel = column j; 1: channel = row i mod C
     uint32_t C;
     FastDiv div_C;
+    // Op::Pad only: the source extents inside the padded [M, N]
+    int64_t Msrc, Nsrc;
 };
 
 template <Op OP>
 __device__ __forceinline__ uint32_t apply(uint32_t x, float alpha)
 {
-    if (OP == Op::Copy) return x;                 // bitwise: no arithmetic touches the word
+    if (OP == Op::Copy || OP == Op::Pad) return x;  // bitwise: no arithmetic touches the word
     return as_u(__fmul_rn(alpha, as_f(x)));       // one rounding, like the oracle
 }
 
@@ -168,7 +170,10 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
                 yoff[u] = i * p.ldy + j;
                 if constexpr (OP == Op::Channel)
                     chan[u] = p.layout == 0 ? (uint32_t)j : (uint32_t)i - fdiv((uint32_t)i, p.div_C) * p.C;
-                if (in) {
+                // Op::Pad: the walk covers the padded extents; the source is read
+                // only inside [Msrc, Nsrc] (vectors there are whole: Nsrc % EW == 0)
+                const bool src = OP != Op::Pad || (i < p.Msrc && j < p.Nsrc);
+                if (in && src) {
                     val[u] = load_vec<EW>(p.X + i * p.ldx + j);
                 } else {
 #pragma unroll
@@ -371,4 +376,73 @@ extern "C" tm_status tm_channel_affine(const float *X, int64_t ldx, int64_t R, i
 {
     const ChannelParams ch{scale, bias, C, layout};
     return map2d(Op::Channel, X, ldx, Y, ldy, R, K, 0.0f, TM, TN, flags, stream, true, &ch);
+}
+
+extern "C" tm_status tm_pad2d(const float *A, int64_t lda, int64_t M, int64_t N, float *B, int64_t ldb, int64_t Mp,
+                              int64_t Np, tm_stream_t stream)
+{
+    if (M < 0 || N < 0 || Mp < M || Np < N) return TM_ERR_INVALID_ARG;
+    if (!valid2d(A, lda, M, N) || !valid2d(B, ldb, Mp, Np)) return TM_ERR_INVALID_ARG;
+    if (Mp == 0 || Np == 0) return TM_OK;
+    if (M > 0 && N > 0) {
+        uintptr_t alo, ahi, blo, bhi;
+        span2d(A, lda, M, N, &alo, &ahi);
+        span2d(B, ldb, Mp, Np, &blo, &bhi);
+        if (!(ahi <= blo || bhi <= alo)) return TM_ERR_INVALID_ARG;  // no in-place padding
+        if (!aligned_to(A, 4)) return TM_ERR_MISALIGNED;
+    }
+    if (!aligned_to(B, 4)) return TM_ERR_MISALIGNED;
+    const bool vec = aligned_to(B, 16) && ldb % 4 == 0 && Np % 4 == 0 &&
+                     (M == 0 || N == 0 || (aligned_to(A, 16) && lda % 4 == 0 && N % 4 == 0));
+    constexpr int TM = 32, TN = 128;
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    const int64_t tiles_m = (Mp + TM - 1) / TM, tiles_n = (Np + TN - 1) / TN;
+    if (tiles_n > INT32_MAX || tiles_m > INT32_MAX / tiles_n) return TM_ERR_INVALID_ARG;
+    Map2dArgs a{};
+    a.X = A;
+    a.Y = B;
+    a.ldx = lda;
+    a.ldy = ldb;
+    a.M = Mp;
+    a.N = Np;
+    a.tiles_n = (uint32_t)tiles_n;
+    a.ntiles = (uint32_t)(tiles_m * tiles_n);
+    a.div_tiles_n = make_fastdiv((uint32_t)tiles_n);
+    a.status = dev->status;
+    a.C = 1u;
+    a.div_C = make_fastdiv(1u);
+    a.Msrc = M;
+    a.Nsrc = N;
+    return launch_tile<TM, TN, Op::Pad>(vec ? Path::RaggedVec : Path::Scalar, 4, a, as_stream(stream));
+}
+
+extern "C" int64_t tm_padded_extent(int64_t extent, const int32_t *tiles, int32_t ntiles)
+{
+    if (extent < 0 || ntiles <= 0 || tiles == nullptr) return -1;
+    int64_t L = 1;
+    for (int32_t k = 0; k < ntiles; ++k) {
+        const int64_t t = tiles[k];
+        if (t <= 0) return -1;
+        int64_t a = L, b = t;  // L = lcm(L, t)
+        while (b) {
+            const int64_t r = a % b;
+            a = b;
+            b = r;
+        }
+        if (L / a > INT64_MAX / t) return -1;
+        L = L / a * t;
+    }
+    const int64_t q = extent / L + (extent % L ? 1 : 0);
+    if (q > INT64_MAX / L) return -1;
+    return q * L;
+}
+
+extern "C" int64_t tm_row_stride(int64_t N, int32_t align_bytes)
+{
+    if (N < 0 || align_bytes <= 0 || align_bytes % 4 != 0 || (align_bytes & (align_bytes - 1)) != 0) return -1;
+    const int64_t q = align_bytes / 4;  // elements per aligned unit
+    if (N > INT64_MAX - q) return -1;
+    return (N + q - 1) / q * q;
 }

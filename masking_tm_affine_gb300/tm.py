@@ -58,6 +58,9 @@ SIGNATURES = {
     "tm_scale2d": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _u32, _vp]),
     "tm_copy2d": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _i32, _i32, _u32, _vp]),
     "tm_channel_affine": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _i32, _vp, _i64, _i32, _i32, _u32, _vp]),
+    "tm_padded_extent": (_i64, [_i64, _vp, _i32]),
+    "tm_row_stride": (_i64, [_i64, _i32]),
+    "tm_pad2d": (_st, [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _i64, _vp]),
     "tm_rowsum": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _u32, _vp]),
     "tm_colsum_workspace_bytes": (_sz, [_i64, _i64, _i32, _i32, _st]),
     "tm_colsum": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _sz, _i32, _i32, _st, _u32, _vp]),
@@ -151,6 +154,19 @@ def tm_channel_affine(X, ldx: int, R: int, K: int, scale, bias, C: int, layout: 
                       TM: int = 32, TN: int = 128, flags: int = 0, stream=None) -> None:
     _ok(load().tm_channel_affine(_ptr(X), ldx, R, K, _ptr(scale), _ptr(bias), C, layout, _ptr(Y), ldy, TM, TN,
                                  flags, _stream(stream)), "tm_channel_affine")
+
+
+def tm_padded_extent(extent: int, tiles) -> int:
+    arr = (ctypes.c_int32 * len(tiles))(*tiles)
+    return int(load().tm_padded_extent(extent, ctypes.cast(arr, ctypes.c_void_p), len(tiles)))
+
+
+def tm_row_stride(N: int, align_bytes: int = 16) -> int:
+    return int(load().tm_row_stride(N, align_bytes))
+
+
+def tm_pad2d(A, lda: int, M: int, N: int, B, ldb: int, Mp: int, Np: int, stream=None) -> None:
+    _ok(load().tm_pad2d(_ptr(A), lda, M, N, _ptr(B), ldb, Mp, Np, _stream(stream)), "tm_pad2d")
 
 
 def tm_rowsum(X, ldx: int, M: int, N: int, r, TM: int = 8, TN: int = 512, flags: int = 0,

@@ -119,3 +119,21 @@ def test_colsum_workspace_plan(lib):
     assert tm.tm_colsum_workspace_bytes(100, 10, 33, 128) == 0
     w = tm.tm_colsum_workspace_bytes(4100, 1001, 32, 128)
     assert w % (1004 * 4) == 0      # rows padded to a multiple of 4 columns
+
+
+def test_padding_helpers_match_oracle(lib, oracle):
+    # host-only entry points (no CUDA call): against the oracle's search definitions
+    for tiles in ([32], [64], [32, 256], [4, 16], [64, 128, 256], [3, 5], [1]):
+        for extent in list(range(0, 70)) + [1000, 4100, 8192, 8193, 10**9 + 7]:
+            if extent > 10**6 and max(tiles) < 32:
+                continue  # the oracle's search is linear in the gap
+            assert tm.tm_padded_extent(extent, tiles) == oracle.padded_extent(extent, tiles), (extent, tiles)
+    for N in list(range(0, 100)) + [1000, 1001, 4099, 10**9 + 3]:
+        for align in (4, 16, 32, 128):
+            assert tm.tm_row_stride(N, align) == oracle.row_stride(N, align), (N, align)
+    assert tm.tm_padded_extent(10, [0]) == -1
+    assert tm.tm_padded_extent(-1, [4]) == -1
+    assert tm.tm_padded_extent(10, []) == -1
+    assert tm.tm_row_stride(10, 6) == -1 and tm.tm_row_stride(10, 12) == -1
+    assert tm.tm_padded_extent(2**63 - 1, [2]) == -1       # the next multiple of 2 overflows int64
+    assert tm.tm_padded_extent(2**62, [3, 5, 7]) == -(-2**62 // 105) * 105
