@@ -1,0 +1,90 @@
+"""Maximum sizes: tensors past 2^31 elements (8.6 - 9.6 GB each), where any
+32-bit element offset would wrap.  Inputs are a seeded integer pattern built
+on the device; sampled rows (including the last ones) are checked against the
+oracle, which computes them one by one."""
+import numpy as np
+import pytest
+import torch
+
+from masking_tm_affine_gb300 import tm
+
+pytestmark = pytest.mark.gpu
+
+
+def pattern(rows, cols, seed):
+    """fp32 values k/64 for small integers k from a seeded hash of the
+    position: exact in fp32 and cheap to rebuild on the host."""
+    i = torch.arange(rows, device="cuda", dtype=torch.int64)[:, None]
+    j = torch.arange(cols, device="cuda", dtype=torch.int64)[None, :]
+    h = (i * 1000003 + j * 7919 + seed * 104729) % 2039
+    return ((h - 1019).to(torch.float32) / 64.0)
+
+
+def pattern_host(rows_idx, cols, seed):
+    i = np.asarray(rows_idx, dtype=np.int64)[:, None]
+    j = np.arange(cols, dtype=np.int64)[None, :]
+    h = (i * 1000003 + j * 7919 + seed * 104729) % 2039
+    return ((h - 1019).astype(np.float32) / np.float32(64.0))
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.empty_cache()
+
+
+def test_affine_past_2_31_elements(cuda, oracle):
+    n = (1 << 31) + 5
+    a = pattern(1, n, 1).reshape(-1)
+    out = torch.empty_like(a)
+    tm.tm_affine(a, out, n)
+    tm.tm_check()
+    for start in (0, (1 << 31) - 64, n - 64):
+        seg = a[start:start + 64].cpu().numpy()
+        assert np.array_equal(out[start:start + 64].cpu().numpy().view(np.uint32), oracle.affine(seg).view(np.uint32))
+    del a, out
+
+
+def test_scale2d_and_copy2d_past_2_31_elements(cuda, oracle):
+    M, N = 40001, 60000                           # 2.4e9 elements, ragged for 32 x 128 tiles
+    X = pattern(M, N, 2)
+    Y = torch.empty_like(X)
+    rows = [0, 17, M // 2, M - 2, M - 1]
+    tm.tm_scale2d(X, N, Y, N, M, N, 1.5, 32, 128)
+    tm.tm_check()
+    xs = pattern_host(rows, N, 2)
+    want = np.zeros_like(xs)
+    oracle.scale2d(xs, N, want, N, len(rows), N, 1.5)
+    assert np.array_equal(Y[rows].cpu().numpy(), want)
+    tm.tm_copy2d(X, N, Y, N, M, N, 64, 64)
+    tm.tm_check()
+    assert np.array_equal(Y[rows].cpu().numpy(), xs)
+    del X, Y
+
+
+def test_reductions_past_2_31_elements(cuda, oracle):
+    M, N = 70001, 32768                           # 2.3e9 elements
+    X = pattern(M, N, 3)
+    rows = [0, 1, M // 3, M - 1]
+    xs = pattern_host(rows, N, 3)
+    r = torch.empty(M, device="cuda")
+    tm.tm_rowsum(X, N, M, N, r, 1, 1024)
+    m = torch.empty(M, device="cuda")
+    tm.tm_rowmax_masked(X, N, M, N, m, 1, 64)
+    c = torch.empty(N, device="cuda")
+    ws = tm.tm_colsum_workspace_bytes(M, N, 32, 128)
+    W = torch.empty(ws // 4, device="cuda")
+    tm.tm_colsum(X, N, M, N, c, W, ws, 32, 128)
+    tm.tm_check()
+    # values are k/64 with |k| <= 1019: every partial sum is exact in fp32 while
+    # below 2^24/64, so row sums (|sum| < 2^14) must match exactly
+    assert np.array_equal(r[rows].cpu().numpy(), oracle.rowsum(xs, N, len(rows), N).astype(np.float32))
+    assert np.array_equal(m[rows].cpu().numpy(), oracle.rowmax_masked(xs, N, len(rows), N, 64))
+    # column sums: checked against an exact integer column sum of the pattern
+    cols = np.array([0, 1, N // 2, N - 1])
+    i = np.arange(M, dtype=np.int64)[:, None]
+    h = (i * 1000003 + cols[None, :] * 7919 + 3 * 104729) % 2039
+    exact = (h - 1019).sum(axis=0) / 64.0
+    got = c.cpu().numpy()[cols].astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 1e-5 * (np.abs(h - 1019).sum(axis=0) / 64.0))
+    del X, W
