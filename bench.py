@@ -592,6 +592,65 @@ CASES = {
 }
 
 
+def time_oracle_case(kern, w, x, budget_s: float = 1.5) -> dict:
+    """The oracle on one host core for the same kernel and workload, over a row
+    slice sized to about budget_s (whole workload when it fits)."""
+    import numpy as np
+    import oracle
+    from masking_tm_affine_gb300 import synth
+    oracle.build()
+    flat = kern == "affine"
+    rows = x.size if flat else x.shape[0]
+    cols = 1 if flat else x.shape[1]
+
+    def call(R):
+        if flat:
+            oracle.affine(x[:R])
+            return 8 * R
+        xs = np.ascontiguousarray(x[:R])
+        if kern in ("scale2d", "copy2d"):
+            Y = np.empty(R * cols, dtype=np.float32)
+            if kern == "scale2d":
+                oracle.scale2d(xs, cols, Y, cols, R, cols, ALPHA)
+            else:
+                oracle.copy2d(xs, cols, Y.view(np.uint32), cols, R, cols)
+            return 8 * R * cols
+        if kern == "rowsum":
+            oracle.rowsum(xs, cols, R, cols)
+            return 4 * R * cols + 4 * R
+        if kern == "colsum":
+            oracle.colsum(xs, cols, R, cols)
+            return 4 * R * cols + 4 * cols
+        if kern == "rowmax_masked":
+            oracle.rowmax_masked(xs, cols, R, cols, w.get("BC", 64))
+            return 4 * R * cols + 4 * R
+        if kern == "softmax_rowstats":
+            oracle.softmax_rowstats(xs, cols, R, cols, w.get("BC", 64))
+            return 4 * R * cols + 8 * R
+        if kern == "channel_affine":
+            sc, bi = synth.channel_params(w["C"])
+            Y = np.empty(R * cols, dtype=np.float32)
+            oracle.channel_affine(xs, cols, R, cols, sc, bi, w["C"], w["layout"], Y, cols)
+            return 8 * R * cols + 8 * w["C"]
+        if kern == "pad2d":
+            Np = -(-cols // w["TN"]) * w["TN"]
+            Rp = -(-R // w["TM"]) * w["TM"]
+            B = np.empty(Rp * Np, dtype=np.uint32)
+            oracle.pad2d(xs, cols, R, cols, B, Np, Rp, Np)
+            return 4 * R * cols + 4 * Rp * Np
+        raise ValueError(kern)
+
+    probe = max(1, min(rows, 64 if not flat else 1 << 16))
+    t0 = time.perf_counter()
+    call(probe)
+    per = (time.perf_counter() - t0) / probe
+    R = int(max(1, min(rows, budget_s / max(per, 1e-12))))
+    t0 = time.perf_counter()
+    nb = call(R)
+    el = time.perf_counter() - t0
+    return {"GBps": round(gbps(nb, el), 3), "sample": "%d of %d %s, one host thread" % (R, rows, "elements" if flat else "rows")}
+
+
 def run_cases(args):
     """Time one kernel on one workload: median of CUDA-event times over
     --reps launches, L2 flushed (a 512 MiB write) before every launch."""
@@ -693,9 +752,12 @@ def run_cases(args):
                 if rep >= 3:
                     ts.append(e0.elapsed_time(e1) * 1e-3)
             t = statistics.median(ts)
-            out.append({"case": name, "kernel": kern, "variant": v, "tile": args.tile, "bytes": nbytes, "us": round(t * 1e6, 2),
+            row = {"case": name, "kernel": kern, "variant": v, "tile": args.tile, "bytes": nbytes, "us": round(t * 1e6, 2),
                         "GBps": round(gbps(nbytes, t), 1), "frac": round(gbps(nbytes, t) / peak, 4),
-                        "reps": args.reps, "l2": "flushed before each launch" if not args.no_flush else "warm"})
+                        "reps": args.reps, "l2": "flushed before each launch" if not args.no_flush else "warm"}
+            if args.oracle:
+                row["oracle"] = time_oracle_case(kern, w, x)
+            out.append(row)
         del X, O
     tm.tm_check()
     return out
@@ -718,6 +780,7 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--tile", help="--case: tile override, e.g. 1x1024 (rows x columns)")
     ap.add_argument("--no-flush", action="store_true", help="--case: do not flush L2 between launches")
+    ap.add_argument("--oracle", action="store_true", help="--case: also time the oracle on the same workload")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -76,6 +76,8 @@ def _load():
         lib.oracle_row_stride.restype = i64
         lib.oracle_pad2d.argtypes = [vp, i64, i64, i64, vp, i64, i64, i64]
         lib.oracle_pad2d.restype = None
+        lib.oracle_gemm_rows.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, f32, f32, vp]
+        lib.oracle_gemm_rows.restype = None
         _lib = lib
         return lib
 
@@ -244,3 +246,30 @@ def pad2d(A, lda: int, M: int, N: int, B: np.ndarray, ldb: int, Mp: int, Np: int
     _check_2d(A, lda, M, N, "A")
     _check_2d(B.reshape(-1), ldb, Mp, Np, "B")
     _load().oracle_pad2d(_ptr(A), lda, M, N, _ptr(B), ldb, Mp, Np)
+
+
+def gemm_rows(A, lda: int, B, ldb: int, Cin, ldc: int, rows, N: int, K: int, alpha: float = 1.0,
+              beta: float = 0.0) -> np.ndarray:
+    """Rows ``rows`` of alpha*(A B) + beta*Cin, fp64 then rounded once to fp32
+    ("@aligned", the gemm example; "Slicing, bounds and masking", "Loops over a
+    dynamic extent").  A [*, lda] rows hold K used columns, B [K, ldb] rows N."""
+    A = _as_f32_flat(A)
+    B = _as_f32_flat(B)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    if K > 0 and (lda < K or ldb < N):
+        raise ValueError("leading dimensions too small")
+    if B.size < max(0, (K - 1) * ldb + N) and K > 0 and N > 0:
+        raise ValueError("B too small")
+    if rows.size and A.size < (int(rows.max()) * lda + K):
+        raise ValueError("A too small for the requested rows")
+    if beta != 0.0:
+        Cin = _as_f32_flat(Cin)
+        if rows.size and Cin.size < int(rows.max()) * ldc + N:
+            raise ValueError("C too small for the requested rows")
+        cptr = _ptr(Cin)
+    else:
+        cptr = None
+    out = np.empty((rows.size, N), dtype=np.float32)
+    _load().oracle_gemm_rows(_ptr(A), lda, _ptr(B), ldb, cptr, ldc, _ptr(rows), rows.size, N, K,
+                             float(alpha), float(beta), _ptr(out))
+    return out

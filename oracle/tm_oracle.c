@@ -330,3 +330,31 @@ void oracle_pad2d(const uint32_t *A, int64_t lda, int64_t M, int64_t N,
         for (j = 0; j < Np; ++j)
             B[i * ldb + j] = (i < M && j < N) ? A[i * lda + j] : 0u;
 }
+
+/* ------------------------------------------------------------------------ */
+/* f4: the gemm of [AL] "A minimal kernel"'s companion example (kernel gemm, */
+/* "without @aligned" / "with @aligned"): C = alpha * (A B) + beta * C_old   */
+/* over row-major A [M, K], B [K, N], C [M, N].  The tiled kernel walks K in */
+/* whole tiles plus one masked remainder whose missing columns read 0 ([SB]  */
+/* "Loops over a dynamic extent"), and masks its M and N edges; both leave   */
+/* the plain definition, computed here in fp64 and rounded once to fp32,     */
+/* for the rows listed in rows[0 .. nrows) (out is [nrows, N], ld = N).      */
+/* ------------------------------------------------------------------------ */
+void oracle_gemm_rows(const float *A, int64_t lda, const float *B, int64_t ldb,
+                      const float *Cin, int64_t ldc, const int64_t *rows, int64_t nrows,
+                      int64_t N, int64_t K, float alpha, float beta, float *out)
+{
+    int64_t r, j, k;
+    for (r = 0; r < nrows; ++r) {
+        const int64_t i = rows[r];
+        for (j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (k = 0; k < K; ++k)
+                acc += (double)A[i * lda + k] * (double)B[k * ldb + j];
+            acc = (double)alpha * acc;
+            if (beta != 0.0f)
+                acc += (double)beta * (double)Cin[i * ldc + j];
+            out[r * N + j] = (float)acc;
+        }
+    }
+}

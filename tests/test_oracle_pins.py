@@ -551,3 +551,46 @@ def test_pad2d_definition_and_sum_invariance(oracle, M, N, Mp, Np, lda, ldb):
         Bf = Bv.view(np.float32).reshape(-1)
         assert np.array_equal(oracle.rowsum(Bf, ldb, Mp, Np)[:M], oracle.rowsum(A, lda, M, N))
         assert np.array_equal(oracle.colsum(Bf, ldb, Mp, Np)[:N], oracle.colsum(A, lda, M, N))
+
+
+# --------------------------------------------------------------------------
+# The gemm ("@aligned" gemm example; "Loops over a dynamic extent")
+# --------------------------------------------------------------------------
+def test_gemm_rows_matches_numpy_float64(oracle):
+    M, N, K = 37, 29, 1000                               # K = 1000: the page's ragged K
+    A = synth.normal((M, K), 70)
+    B = synth.normal((K, N), 71)
+    C = synth.normal((M, N), 72)
+    rows = np.arange(M)
+    got = oracle.gemm_rows(A, K, B, N, C, N, rows, N, K, 1.25, -0.5)
+    want = (1.25 * (A.astype(np.float64) @ B.astype(np.float64)) - 0.5 * C.astype(np.float64)).astype(np.float32)
+    # fp64 sums in different orders: equal after rounding to fp32 except at rare ties
+    assert np.mean(got == want) > 0.999
+    assert np.allclose(got, want, rtol=1e-6, atol=1e-6)
+
+
+def test_gemm_rows_closed_forms(oracle):
+    # identity B: A @ I = A exactly; all-ones: every entry is the row sum of A
+    M, K = 5, 12
+    A = synth.uniform((M, K), -4.0, 4.0, 73)
+    I = np.eye(K, dtype=np.float32)
+    assert np.array_equal(oracle.gemm_rows(A, K, I, K, None, 0, np.arange(M), K, K), A)
+    ones = np.ones((K, 3), np.float32)
+    got = oracle.gemm_rows(A, K, ones, 3, None, 0, np.arange(M), 3, K)
+    rs = A.astype(np.float64).sum(axis=1).astype(np.float32)
+    assert np.array_equal(got, np.repeat(rs[:, None], 3, axis=1))
+    # beta only (K = 0): C_out = beta * C_in, one rounding
+    C = synth.normal((M, 4), 74)
+    got = oracle.gemm_rows(A, K, ones, 3, C, 4, np.arange(M), 4, 0, 2.0, 0.75)
+    assert np.array_equal(got, (0.75 * C.astype(np.float64)).astype(np.float32))
+
+
+def test_gemm_rows_row_subset_and_lds(oracle):
+    M, N, K, lda, ldb = 50, 20, 33, 40, 24
+    A = synth.pad_rows(synth.normal((M, K), 75), lda)
+    B = synth.pad_rows(synth.normal((K, N), 76), ldb)          # gaps hold 3e38 poison
+    rows = np.array([0, 7, 49])
+    got = oracle.gemm_rows(A, lda, B, ldb, None, 0, rows, N, K)
+    Af = A.reshape(M, lda)[:, :K].astype(np.float64)
+    Bf = B.reshape(K, ldb)[:, :N].astype(np.float64)
+    assert np.allclose(got, (Af @ Bf)[rows].astype(np.float32), rtol=1e-6, atol=1e-6)
