@@ -589,7 +589,90 @@ CASES = {
     "rowsum_8192sq": ("scale_8192", "rowsum", ["vec"]),
     "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect"]),
     "rowmax_8192sq": ("scale_8192", "rowmax_masked", ["neg_inf"]),
+    # the tensor-core gemm (3xTF32 by default; tf32 = one pass)
+    "gemm_4100": ("gemm_4100", "gemm", ["3xtf32", "tf32"]),
+    "gemm_8192": ("gemm_8192", "gemm", ["3xtf32", "tf32"]),
 }
+
+# nominal tf32 / bf16 dense tensor rates of GB300 (1.1 and 2.25 PFLOP/s): the
+# tf32 peak is the measured bf16 peak times this ratio
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def tf32_peak(sustained: bool = False):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(path) as f:
+            v = float(json.load(f)[key])
+        return v * TF32_PER_BF16, "measured (MEASURED_PEAKS.json %s x 1.1/2.25 nominal tf32/bf16)" % key
+    except Exception:
+        return 1900.0 * TF32_PER_BF16, "fallback (1.9 PFLOP/s bf16 x 1.1/2.25)"
+
+
+def time_oracle_gemm(w, a, b, c, budget_s: float = 1.5) -> dict:
+    """The oracle's row-by-row fp64 gemm on one host thread, rows sized to about budget_s."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    M, N, K = w["M"], w["N"], w["K"]
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, K, b, N, c, N, np.arange(1), N, K, w["alpha"], w["beta"])
+    per = time.perf_counter() - t0
+    R = int(max(1, min(M, budget_s / max(per, 1e-9))))
+    t0 = time.perf_counter()
+    oracle.gemm_rows(a, K, b, N, c, N, np.arange(R), N, K, w["alpha"], w["beta"])
+    el = time.perf_counter() - t0
+    return {"TFLOPs": round(2.0 * R * N * K / el / 1e12, 6), "sample": "%d of %d rows, one host thread" % (R, M)}
+
+
+def run_gemm_case(name, args, dev, stream, flush):
+    import torch
+
+    from masking_tm_affine_gb300 import synth, tm
+    wl, _, variants = CASES[name]
+    w = synth.WORKLOADS[wl]
+    M, N, K = w["M"], w["N"], w["K"]
+    a, b, c = synth.gemm_inputs(wl)
+    A, B = torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)
+    C0 = torch.from_numpy(c).to(dev)
+    C = C0.clone()
+    TN_ = int(args.tile.split("x")[1]) if args.tile else w["TN"]
+    wsb = tm.tm_gemm_workspace_bytes(M, N, K, TN_)
+    raw = torch.empty(wsb + 1024, dtype=torch.uint8, device=dev)
+    ws = (raw.data_ptr() + 1023) // 1024 * 1024
+    aligned = M % 128 == 0 and N % TN_ == 0 and K % 32 == 0
+    peak, peak_src = tf32_peak()
+    s = stream.cuda_stream
+    out = []
+    chosen = variants if args.variant == "all" else [args.variant or variants[0]]
+    for v in chosen:
+        fl = (tm.TM_ALIGNED if aligned else 0) | (tm.TM_GEMM_TF32 if v == "tf32" else 0)
+        ts = []
+        for rep in range(args.reps + 3):
+            C.copy_(C0)
+            if not args.no_flush:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            tm.tm_gemm(A, K, B, N, C, N, M, N, K, w["alpha"], w["beta"], ws, wsb, 128, TN_, 32, fl, s)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        t = statistics.median(ts)
+        flops = 2.0 * M * N * K
+        passes = 3 if v == "3xtf32" else 1
+        row = {"case": name, "kernel": "gemm", "variant": v, "tile": "128x%dx32" % TN_, "M": M, "N": N, "K": K,
+               "us": round(t * 1e6, 2), "TFLOPs": round(flops / t / 1e12, 2),
+               "tensor_TFLOPs": round(passes * flops / t / 1e12, 2),
+               "frac_of_tf32_peak": round(passes * flops / t / 1e12 / peak, 4), "tf32_peak": round(peak, 1),
+               "peak_source": peak_src, "reps": args.reps,
+               "l2": "flushed before each launch" if not args.no_flush else "warm"}
+        if args.oracle:
+            row["oracle"] = time_oracle_gemm(w, a, b, c)
+        out.append(row)
+    return out
 
 
 def time_oracle_case(kern, w, x, budget_s: float = 1.5) -> dict:
@@ -668,6 +751,9 @@ def run_cases(args):
     out = []
     for name in names:
         wl, kern, variants = CASES[name]
+        if kern == "gemm":
+            out.extend(run_gemm_case(name, args, dev, stream, flush))
+            continue
         w = synth.WORKLOADS[wl]
         x = synth.workload_input(wl)
         X = torch.from_numpy(x.reshape(-1)).to(dev)

@@ -307,6 +307,47 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
                             int32_t TN, tm_variant variant, uint32_t flags, tm_stream_t stream);
 
 /*
+ * tm_gemm -- the fp32 gemm of the pages' @aligned example:
+ *   C = alpha * (A B) + beta * C     A [M, K], B [K, N], C [M, N], row-major.
+ * "@aligned", the gemm example (acc += dot(a, b) over TILE_K-wide tiles of K,
+ * then alpha * acc + beta * c_old per TILE_M x TILE_N output tile, with and
+ * without the promise); "Slicing, bounds and masking", "Loops over a dynamic
+ * extent" (K known only at run time: whole tiles plus one masked remainder
+ * whose missing columns read 0).
+ * On GB300 the contraction runs on the tensor cores (tcgen05, tf32 inputs,
+ * fp32 accumulation in tensor memory).  By default each operand is split as
+ * x = hi + lo (both tf32) and the product takes hi*hi + hi*lo + lo*hi, which
+ * keeps fp32-level accuracy; TM_GEMM_TF32 keeps only hi*hi (tf32 accuracy,
+ * about 3x the speed).  A first pass writes the split operands, K-major and
+ * zero-padded to whole tiles, into the caller's workspace; the zero padding
+ * is the masked remainder tile's fill, so the tensor-core loop itself runs
+ * over whole tiles only.  beta == 0 does not read C (NaN in C stays out).
+ * K == 0 gives C = beta * C.
+ *   A, lda   device input [M, lda]    B, ldb   device input [K, ldb]
+ *   C, ldc   device in/out [M, ldc]; C must not overlap A, B or the workspace
+ *   TM, TN, TK   the output tile and K tile: TM = 128, TK = 32, TN = 128 or 256
+ *   flags    TM_ALIGNED (M % TM == 0, N % TN == 0, K % TK == 0: the output
+ *            tiles store without masks), TM_GEMM_TF32
+ *   workspace, ws_bytes   device scratch of at least
+ *            tm_gemm_workspace_bytes(M, N, K, TN) bytes, 1024-byte aligned,
+ *            overlapping no operand; contents on entry do not matter.
+ * Accuracy: |C - exact| <= (3*2^-22 + 3*K*2^-23) * |alpha| * sum_k |a_ik||b_kj|
+ *   + 2^-23 * (|alpha * (A B)_ij| + |beta c_ij|) (3xTF32; tensor-core
+ *   accumulation is taken as fp32 with truncation).  Integer-valued inputs
+ *   whose partial sums stay below 2^24 give exact results.
+ * Errors: INVALID_ARG (extents, NULL, ld, overlap, unknown flag, N beyond
+ *   TN * 65535 or a padded extent beyond 2^31 - 1), UNSUPPORTED_TILE, MISALIGNED (a pointer not 4-byte
+ *   aligned), BROKEN_PROMISE (host check of TM_ALIGNED), WORKSPACE, CUDA;
+ *   TIMEOUT through tm_check if the tensor-core pipeline stalls (its waits
+ *   are bounded; C is then left partly written).
+ */
+#define TM_GEMM_TF32 0x100u
+size_t tm_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t TN);
+tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                  int64_t M, int64_t N, int64_t K, float alpha, float beta, int32_t TM, int32_t TN,
+                  int32_t TK, uint32_t flags, void *workspace, size_t ws_bytes, tm_stream_t stream);
+
+/*
  * tm_check -- synchronize `stream`, then read and clear this device's status
  * word.  Returns TM_ERR_BROKEN_PROMISE if a kernel's entry check found the
  * aligned promise broken (that kernel stored nothing), TM_ERR_MISALIGNED if it

@@ -1,0 +1,482 @@
+// tm_gemm.cu -- the ragged fp32 gemm: C = alpha * (A B) + beta * C on tcgen05.
+//
+// Source: "@aligned" -- the gemm example (C = alpha * acc + beta * c_old over
+// TILE_M x TILE_N output tiles, acc += dot(a, b) over K tiles), shown with and
+// without the promise; "Slicing, bounds and masking", "Loops over a dynamic
+// extent": a K loop over a runtime extent is whole tiles plus one masked
+// remainder whose missing columns read 0.
+//
+// GB300 design.  A dense contraction, so it runs on the 5th-generation tensor
+// cores: tcgen05.mma kind::tf32 from shared-memory operands into a TMEM
+// accumulator.  fp32 accuracy comes from the 3xTF32 split: each operand x is
+// hi + lo with hi = x rounded to tf32 and lo = (x - hi) rounded to tf32, and
+// the product is hi*hi + hi*lo + lo*hi (the lo*lo term is below fp32
+// resolution); TM_GEMM_TF32 keeps the single hi*hi pass instead.
+//   1. split pass (memory-bound): A [M, K] and B [K, N] become K-major hi/lo
+//      operands zero-padded to whole tiles -- the zero padding is exactly the
+//      masked remainder tile's fill -- with B transposed on the way.
+//   2. gemm: one 128 x BN output tile per CTA, flat grid.  One thread issues
+//      TMA copies (128-byte swizzle, K-major) into a ring of STAGES shared-
+//      memory stages; one thread issues the MMAs (K = 8 per instruction, four
+//      per 32-wide K tile, three passes each) and commits each stage back to
+//      the producer through an mbarrier; the four warps then read the
+//      accumulator rows out of TMEM (32x32b loads) and write
+//      alpha * acc + beta * C, masking the M and N edges unless the promise
+//      holds.  Every wait is bounded; a stalled pipeline sets the status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tm_host.h"
+
+namespace libtm {
+namespace {
+
+constexpr int GBM = 128;  // UMMA M (one CTA)
+constexpr int GBK = 32;   // K per stage: one 128-byte swizzle row of fp32
+constexpr long long kGemmWait = 2000000000LL;
+
+// ------------------------------------------------------------------ split pass
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// A: hi/lo [Mp, Kp] row-major (K-major operand), zero outside [M, K].  Blocks
+// over rows, threads over k: both sides coalesced.
+__global__ void __launch_bounds__(256) split_rows(const float *__restrict__ A, int64_t lda, int64_t M, int64_t K,
+                                                  float *__restrict__ hi, float *__restrict__ lo, int64_t Mp,
+                                                  int64_t Kp)
+{
+    for (int64_t i = blockIdx.x; i < Mp; i += gridDim.x) {
+        for (int64_t k = threadIdx.x; k < Kp; k += blockDim.x) {
+            const float x = (i < M && k < K) ? as_f(ld_nc_b32(A + i * lda + k)) : 0.0f;
+            const uint32_t h = to_tf32(x);
+            hi[i * Kp + k] = as_f(h);
+            lo[i * Kp + k] = as_f(to_tf32(x - as_f(h)));
+        }
+    }
+}
+
+// B [K, N] -> hi/lo [Np, Kp] (transposed, K-major), zero outside; 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) split_transpose(const float *__restrict__ B, int64_t ldb, int64_t K,
+                                                       int64_t N, float *__restrict__ hi, float *__restrict__ lo,
+                                                       int64_t Np, int64_t Kp)
+{
+    __shared__ float t[32][33];
+    const int64_t tiles_k = Kp / 32, tiles_n = Np / 32;
+    for (int64_t tile = blockIdx.x; tile < tiles_k * tiles_n; tile += gridDim.x) {
+        const int64_t k0 = (tile / tiles_n) * 32, n0 = (tile % tiles_n) * 32;
+        const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+#pragma unroll
+        for (int r = ty; r < 32; r += 8) {
+            const int64_t k = k0 + r, n = n0 + tx;
+            t[r][tx] = (k < K && n < N) ? as_f(ld_nc_b32(B + k * ldb + n)) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = ty; r < 32; r += 8) {
+            const int64_t n = n0 + r, k = k0 + tx;
+            const float x = t[tx][r];
+            const uint32_t h = to_tf32(x);
+            hi[n * Kp + k] = as_f(h);
+            lo[n * Kp + k] = as_f(to_tf32(x - as_f(h)));
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ gemm
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity))
+        if (clock64() - t0 > kGemmWait) return false;
+    return true;
+}
+
+// Shared-memory matrix descriptor: start >> 4 in [0, 14), leading byte offset
+// >> 4 in [16, 30), stride byte offset >> 4 in [32, 46), descriptor version 1
+// at bit 46, layout 2 (128-byte swizzle) in [61, 64).  K-major with 128-byte
+// rows: consecutive 8-row groups are 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B tf32
+// (bits 7-9, 10-12 = 2), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t tmem, uint64_t da, uint64_t db, uint32_t id, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+        "l"(da), "l"(db), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+struct GemmArgs {
+    float *C;
+    int64_t ldc, M, N;
+    float alpha, beta;
+    int KT;  // whole K tiles (of 32) after padding
+    unsigned *status;
+};
+
+template <int BN, int STAGES>
+struct GemmSmem {
+    struct Stage {
+        alignas(1024) float a_hi[GBM * GBK];
+        alignas(1024) float a_lo[GBM * GBK];
+        alignas(1024) float b_hi[BN * GBK];
+        alignas(1024) float b_lo[BN * GBK];
+    };
+    Stage st[STAGES];
+    alignas(8) uint64_t full[STAGES];
+    alignas(8) uint64_t empty[STAGES];
+    alignas(8) uint64_t done;
+    uint32_t tmem;
+    int abort;
+};
+
+template <int BN, int STAGES, bool THREE, bool ALIGNED>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tf32_kernel(const __grid_constant__ CUtensorMap m_ahi, const __grid_constant__ CUtensorMap m_alo,
+                     const __grid_constant__ CUtensorMap m_bhi, const __grid_constant__ CUtensorMap m_blo,
+                     const GemmArgs g)
+{
+    using Smem = GemmSmem<BN, STAGES>;
+    extern __shared__ __align__(1024) unsigned char raw[];
+    Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * GBM, n0 = blockIdx.y * BN;  // pm = block.x, pn = block.y as on the page
+    constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BN) * GBK * sizeof(float));
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s.tmem)),
+                     "r"(BN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (threadIdx.x == 32) {
+        for (int i = 0; i < STAGES; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.empty[i])));
+        }
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.done)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s.abort = 0;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s.tmem;
+
+    int issued = 0;  // producer: stages loaded
+    if (threadIdx.x == 0) {
+        // ---------------- producer: TMA copies of the four operand tiles
+        for (int kt = 0; kt < g.KT; ++kt) {
+            const int st = kt % STAGES;
+            if (kt >= STAGES && !mbar_wait(su32(&s.empty[st]), (uint32_t)((kt / STAGES) + 1) & 1u)) {
+                atomicOr(g.status, kStatusTimeout);
+                s.abort = 1;
+                break;
+            }
+            const uint32_t bar = su32(&s.full[st]);
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kStageBytes)
+                         : "memory");
+            const int kx = kt * GBK;
+            tma_load(su32(s.st[st].a_hi), &m_ahi, kx, m0, bar);
+            tma_load(su32(s.st[st].b_hi), &m_bhi, kx, n0, bar);
+            if (THREE) {
+                tma_load(su32(s.st[st].a_lo), &m_alo, kx, m0, bar);
+                tma_load(su32(s.st[st].b_lo), &m_blo, kx, n0, bar);
+            }
+            issued = kt + 1;
+        }
+    } else if (threadIdx.x == 32) {
+        // ---------------- MMA issuer
+        constexpr uint32_t id = idesc_tf32(GBM, BN);
+        bool ok = true;
+        for (int kt = 0; kt < g.KT && ok; ++kt) {
+            const int st = kt % STAGES;
+            if (!mbar_wait(su32(&s.full[st]), (uint32_t)(kt / STAGES) & 1u)) {
+                atomicOr(g.status, kStatusTimeout);
+                s.abort = 1;
+                ok = false;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t ahi = su32(s.st[st].a_hi), alo = su32(s.st[st].a_lo);
+            const uint32_t bhi = su32(s.st[st].b_hi), blo = su32(s.st[st].b_lo);
+#pragma unroll
+            for (int k = 0; k < GBK / 8; ++k) {
+                const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
+                umma_tf32(tmem, smem_desc(ahi + off), smem_desc(bhi + off), id, (kt | k) != 0);
+                if (THREE) {
+                    umma_tf32(tmem, smem_desc(ahi + off), smem_desc(blo + off), id, 1u);
+                    umma_tf32(tmem, smem_desc(alo + off), smem_desc(bhi + off), id, 1u);
+                }
+            }
+            umma_commit(su32(&s.empty[st]));  // the stage is free once these MMAs are done
+        }
+        umma_commit(su32(&s.done));  // also after an abort: it tracks every MMA already issued
+    }
+    __syncthreads();
+
+    // ---------------- epilogue: TMEM rows -> alpha * acc + beta * C
+    bool ok = !s.abort;
+    if (ok && !mbar_wait(su32(&s.done), 0u)) {
+        if (threadIdx.x == 0) atomicOr(g.status, kStatusTimeout);
+        ok = false;
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok) {
+        const int64_t row = (int64_t)m0 + warp * 32 + lane;
+        const bool row_in = ALIGNED || row < g.M;
+        float *crow = g.C + row * g.ldc;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 8) {
+            uint32_t r[8];
+            const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c;
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                           "=r"(r[7])
+                         : "r"(taddr));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            if (!row_in) continue;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int64_t col = (int64_t)n0 + c + e;
+                if (!ALIGNED && col >= g.N) break;
+                float v = g.alpha * as_f(r[e]);
+                if (g.beta != 0.0f) v = __fmaf_rn(g.beta, crow[col], v);
+                crow[col] = v;
+            }
+        }
+    }
+    // nothing may still be landing in this CTA's shared memory or TMEM when it leaves
+    if (threadIdx.x == 0 && !ok) {
+        for (int kt = (issued > STAGES ? issued - STAGES : 0); kt < issued; ++kt)
+            mbar_wait(su32(&s.full[kt % STAGES]), (uint32_t)(kt / STAGES) & 1u);
+        mbar_wait(su32(&s.done), 0u);
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool kmajor_map(CUtensorMap *m, float *base, int64_t rows, int64_t Kp, int box_rows)
+{
+    const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)Kp * sizeof(float)};
+    const cuuint32_t box[2] = {(cuuint32_t)GBK, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return gemm_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct GemmPlan {
+    int64_t Mp, Np, Kp;
+    size_t bytes;     // workspace
+    size_t off[4];    // a_hi, a_lo, b_hi, b_lo
+};
+
+GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
+{
+    GemmPlan p;
+    p.Mp = (M + GBM - 1) / GBM * GBM;
+    p.Np = (N + TN - 1) / TN * TN;
+    p.Kp = K > 0 ? (K + GBK - 1) / GBK * GBK : GBK;  // K = 0: one zero tile, acc = 0
+    const size_t a = (size_t)(p.Mp * p.Kp) * sizeof(float), b = (size_t)(p.Np * p.Kp) * sizeof(float);
+    auto up = [](size_t x) { return (x + 1023) & ~size_t(1023); };
+    p.off[0] = 0;
+    p.off[1] = up(a);
+    p.off[2] = p.off[1] + up(a);
+    p.off[3] = p.off[2] + up(b);
+    p.bytes = p.off[3] + up(b);
+    return p;
+}
+
+template <int BN, int STAGES, bool THREE, bool ALIGNED>
+tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, int64_t tiles_m, int64_t tiles_n, cudaStream_t s)
+{
+    const void *k = (const void *)gemm_tf32_kernel<BN, STAGES, THREE, ALIGNED>;
+    const size_t smem = sizeof(GemmSmem<BN, STAGES>) + 1024;
+    static std::once_flag once[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    bool attr_ok = true;
+    std::call_once(once[dev < 0 || dev >= kMaxDevices ? 0 : dev], [&] {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+            cudaGetLastError();
+            attr_ok = false;
+        }
+    });
+    if (!attr_ok) return TM_ERR_CUDA;
+    void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
+                    const_cast<CUtensorMap *>(&maps[2]), const_cast<CUtensorMap *>(&maps[3]),
+                    const_cast<GemmArgs *>(&g)};
+    if (cudaLaunchKernel(k, dim3((unsigned)tiles_m, (unsigned)tiles_n), dim3(128), args, smem, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
+template <int BN, int STAGES>
+tm_status launch_gemm_bn(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, int64_t tmt,
+                         int64_t tn, cudaStream_t s)
+{
+    if (three)
+        return aligned ? launch_gemm<BN, STAGES, true, true>(maps, g, tmt, tn, s)
+                       : launch_gemm<BN, STAGES, true, false>(maps, g, tmt, tn, s);
+    return aligned ? launch_gemm<BN, STAGES, false, true>(maps, g, tmt, tn, s)
+                   : launch_gemm<BN, STAGES, false, false>(maps, g, tmt, tn, s);
+}
+
+bool disjoint_bytes(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x + na <= y || y + nb <= x;
+}
+
+}  // namespace
+}  // namespace libtm
+
+using namespace libtm;
+
+extern "C" size_t tm_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t TN)
+{
+    if (M <= 0 || N <= 0 || K < 0 || !(TN == 128 || TN == 256)) return 0;
+    return gemm_plan(M, N, K, TN).bytes;
+}
+
+extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                             int64_t M, int64_t N, int64_t K, float alpha, float beta, int32_t TM, int32_t TN,
+                             int32_t TK, uint32_t flags, void *workspace, size_t ws_bytes, tm_stream_t stream)
+{
+    if (M < 0 || N < 0 || K < 0) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | TM_GEMM_TF32)) return TM_ERR_INVALID_ARG;
+    if (TM != GBM || TK != GBK || !(TN == 128 || TN == 256)) return TM_ERR_UNSUPPORTED_TILE;
+    if (!valid2d(C, ldc, M, N) || !valid2d(A, lda, M, K) || !valid2d(B, ldb, K, N)) return TM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return TM_OK;
+    if (!aligned_to(C, 4) || (K > 0 && (!aligned_to(A, 4) || !aligned_to(B, 4)))) return TM_ERR_MISALIGNED;
+    if (flags & TM_ALIGNED) {
+        if (M % TM != 0 || N % TN != 0 || K % TK != 0) return TM_ERR_BROKEN_PROMISE;
+    }
+    const GemmPlan pl = gemm_plan(M, N, K, TN);
+    if (pl.Mp > INT32_MAX || pl.Np > INT32_MAX || pl.Kp > INT32_MAX || pl.Np / TN > 65535)
+        return TM_ERR_INVALID_ARG;
+    if (workspace == nullptr || ws_bytes < pl.bytes || !aligned_to(workspace, 1024)) return TM_ERR_WORKSPACE;
+    {
+        uintptr_t clo, chi;
+        span2d(C, ldc, M, N, &clo, &chi);
+        const void *cp = reinterpret_cast<const void *>(clo);
+        if (!disjoint_bytes(cp, chi - clo, workspace, pl.bytes)) return TM_ERR_INVALID_ARG;
+        if (K > 0) {
+            uintptr_t lo, hi;
+            span2d(A, lda, M, K, &lo, &hi);
+            if (!disjoint_bytes(cp, chi - clo, reinterpret_cast<const void *>(lo), hi - lo) ||
+                !disjoint_bytes(workspace, pl.bytes, reinterpret_cast<const void *>(lo), hi - lo))
+                return TM_ERR_INVALID_ARG;
+            span2d(B, ldb, K, N, &lo, &hi);
+            if (!disjoint_bytes(cp, chi - clo, reinterpret_cast<const void *>(lo), hi - lo) ||
+                !disjoint_bytes(workspace, pl.bytes, reinterpret_cast<const void *>(lo), hi - lo))
+                return TM_ERR_INVALID_ARG;
+        }
+    }
+
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    if (gemm_encode_fn() == nullptr) return TM_ERR_CUDA;
+    cudaStream_t s = as_stream(stream);
+    char *ws = static_cast<char *>(workspace);
+    float *ahi = reinterpret_cast<float *>(ws + pl.off[0]), *alo = reinterpret_cast<float *>(ws + pl.off[1]);
+    float *bhi = reinterpret_cast<float *>(ws + pl.off[2]), *blo = reinterpret_cast<float *>(ws + pl.off[3]);
+
+    // 1. split (and transpose B) into zero-padded K-major tf32 hi/lo operands
+    split_rows<<<flat_grid(pl.Mp < 8LL * dev->sms ? pl.Mp : 8LL * dev->sms), 256, 0, s>>>(A, lda, M, K, ahi, alo, pl.Mp, pl.Kp);
+    if ((st = launch_status()) != TM_OK) return st;
+    split_transpose<<<flat_grid((pl.Kp / 32) * (pl.Np / 32)), 256, 0, s>>>(B, ldb, K, N, bhi, blo, pl.Np, pl.Kp);
+    if ((st = launch_status()) != TM_OK) return st;
+
+    // 2. the tensor-core gemm over whole tiles
+    CUtensorMap maps[4];
+    if (!kmajor_map(&maps[0], ahi, pl.Mp, pl.Kp, GBM) || !kmajor_map(&maps[1], alo, pl.Mp, pl.Kp, GBM) ||
+        !kmajor_map(&maps[2], bhi, pl.Np, pl.Kp, TN) || !kmajor_map(&maps[3], blo, pl.Np, pl.Kp, TN))
+        return TM_ERR_CUDA;
+    GemmArgs g;
+    g.C = C;
+    g.ldc = ldc;
+    g.M = M;
+    g.N = N;
+    g.alpha = alpha;
+    g.beta = beta;
+    g.KT = (int)(pl.Kp / GBK);
+    g.status = dev->status;
+    const bool three = !(flags & TM_GEMM_TF32);
+    const bool aligned = (flags & TM_ALIGNED) != 0;
+    if (TN == 128) return launch_gemm_bn<128, 3>(three, aligned, maps, g, pl.Mp / GBM, pl.Np / TN, s);
+    return launch_gemm_bn<256, 2>(three, aligned, maps, g, pl.Mp / GBM, pl.Np / TN, s);
+}

@@ -20,6 +20,9 @@ Workloads (sizes from the pages; distributions and seeds fixed here):
 * ``rowmax_8192``  -- [8192, 1000], U[-30, -1), seed 4, BC = 64
   ("Slicing, bounds and masking", "Reductions over a ragged tile": negative
   scores, last column tile ragged).
+* ``gemm_4100`` / ``gemm_8192`` -- the gemm of "@aligned" on U[-1, 1)
+  operands: [4100, 1000] x [1000, 4100] (K = 1000 from "Loops over a dynamic
+  extent") and [8192, 8192] x [8192, 8192] on whole tiles.
 """
 from __future__ import annotations
 
@@ -75,7 +78,22 @@ WORKLOADS = {
                          dist=("normal",), seed=5, TM=32, TN=128),
     "channel_nchw": dict(kind="channel", M=32 * 256, N=56 * 56, C=256, layout=1,
                          dist=("normal",), seed=5, TM=32, TN=128),
+    # the gemm of "@aligned" (A [M, K] B [K, N], alpha, beta): K = 1000 as in "Slicing,
+    # bounds and masking", "Loops over a dynamic extent" (ragged against TILE_K = 32),
+    # M = N = 4100 like the ragged 2-D workload; and a square whole-tile case
+    "gemm_4100": dict(kind="gemm", M=4100, N=4100, K=1000, seeds=(7, 8, 9), alpha=1.5, beta=0.5,
+                      TM=128, TN=256, TK=32),
+    "gemm_8192": dict(kind="gemm", M=8192, N=8192, K=8192, seeds=(10, 11, 12), alpha=1.5, beta=0.5,
+                      TM=128, TN=256, TK=32),
 }
+
+
+def gemm_inputs(name: str):
+    """A [M, K], B [K, N] ~ U[-1, 1) and C [M, N] ~ U[-1, 1) of a gemm workload."""
+    w = WORKLOADS[name]
+    sa, sb, sc = w["seeds"]
+    return (uniform((w["M"], w["K"]), -1.0, 1.0, sa), uniform((w["K"], w["N"]), -1.0, 1.0, sb),
+            uniform((w["M"], w["N"]), -1.0, 1.0, sc))
 
 
 def channel_params(C: int, seed: int = 6):

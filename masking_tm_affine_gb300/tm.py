@@ -67,6 +67,9 @@ SIGNATURES = {
     "tm_rowmax_masked": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
     "tm_softmax_rowstats": (_st, [_vp, _i64, _i64, _i64, _vp, _vp, _i32, _i32, _st, _u32, _vp]),
     "tm_colsum_noalloc": (_st, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _st, _u32, _vp]),
+    "tm_gemm_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
+    "tm_gemm": (_st, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _i64, _f32, _f32, _i32, _i32, _i32, _u32,
+                      _vp, _sz, _vp]),
     "tm_check": (_st, [_vp]),
     "tm_tile_walk_probe": (_st, [_i64, _i32, _vp, _vp]),
     "tm_scale2d_unchecked": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
@@ -206,6 +209,21 @@ def tm_softmax_rowstats(S, lds: int, M: int, N: int, m, l, BR: int = 8, BC: int 
                         fill: int = TM_FILL_NEG_INF, flags: int = 0, stream=None) -> None:
     _ok(load().tm_softmax_rowstats(_ptr(S), lds, M, N, _ptr(m), _ptr(l), BR, BC, fill, flags, _stream(stream)),
         "tm_softmax_rowstats")
+
+
+TM_GEMM_TF32 = 0x100  # include/tm.h
+
+
+def tm_gemm_workspace_bytes(M: int, N: int, K: int, TN: int = 256) -> int:
+    return load().tm_gemm_workspace_bytes(M, N, K, TN)
+
+
+def tm_gemm(A, lda: int, B, ldb: int, C, ldc: int, M: int, N: int, K: int, alpha: float, beta: float,
+            workspace, ws_bytes: int, TM: int = 128, TN: int = 256, TK: int = 32, flags: int = 0,
+            stream=None) -> None:
+    """C = alpha * (A B) + beta * C on the tensor cores (3xTF32 unless TM_GEMM_TF32)."""
+    _ok(load().tm_gemm(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, M, N, K, alpha, beta, TM, TN, TK, flags,
+                       _ptr(workspace), ws_bytes, _stream(stream)), "tm_gemm")
 
 
 def tm_check(stream=None) -> None:

@@ -137,3 +137,34 @@ def test_padding_helpers_match_oracle(lib, oracle):
     assert tm.tm_row_stride(10, 6) == -1 and tm.tm_row_stride(10, 12) == -1
     assert tm.tm_padded_extent(2**63 - 1, [2]) == -1       # the next multiple of 2 overflows int64
     assert tm.tm_padded_extent(2**62, [3, 5, 7]) == -(-2**62 // 105) * 105
+
+
+def test_gemm_host_validation(lib):
+    W = 0x7F0200000000  # 1024-byte aligned fake workspace
+    ws = tm.tm_gemm_workspace_bytes(4100, 4100, 1000, 256)
+    # operands zero-padded to whole tiles: [4224, 1024] hi + lo and [4352, 1024] hi + lo
+    assert ws == 2 * 4224 * 1024 * 4 + 2 * 4352 * 1024 * 4
+    assert tm.tm_gemm_workspace_bytes(4100, 4100, 0, 256) == 2 * 4224 * 32 * 4 + 2 * 4352 * 32 * 4
+    assert tm.tm_gemm_workspace_bytes(0, 4, 4, 256) == 0 and tm.tm_gemm_workspace_bytes(4, 4, 4, 64) == 0
+
+    def g(A=P0, lda=1000, B=P1, ldb=4100, C=W + (1 << 34), ldc=4100, M=4100, N=4100, K=1000, TM=128, TN=256,
+          TK=32, flags=0, ws_ptr=W, ws_bytes=ws):
+        return st("tm_gemm", A, lda, B, ldb, C, ldc, M, N, K, 1.5, 0.5, TM, TN, TK, flags, ws_ptr, ws_bytes, None)
+
+    assert g(TM=64) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert g(TK=16) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert g(TN=512) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert g(M=-1) == tm.TM_ERR_INVALID_ARG
+    assert g(lda=999) == tm.TM_ERR_INVALID_ARG
+    assert g(flags=0x4) == tm.TM_ERR_INVALID_ARG
+    assert g(A=None) == tm.TM_ERR_INVALID_ARG
+    assert g(A=P0 + 2) == tm.TM_ERR_MISALIGNED
+    assert g(flags=tm.TM_ALIGNED) == tm.TM_ERR_BROKEN_PROMISE
+    assert g(M=4096, N=4096, K=1000, ldc=4096, flags=tm.TM_ALIGNED, ws_bytes=ws) == tm.TM_ERR_BROKEN_PROMISE
+    assert g(ws_bytes=ws - 1) == tm.TM_ERR_WORKSPACE
+    assert g(ws_ptr=W + 512) == tm.TM_ERR_WORKSPACE
+    assert g(ws_ptr=None) == tm.TM_ERR_WORKSPACE
+    assert g(C=P0 + 4096) == tm.TM_ERR_INVALID_ARG                     # C overlaps A
+    assert g(ws_ptr=P1) == tm.TM_ERR_INVALID_ARG                       # workspace overlaps B
+    assert g(N=256 * 65536, ldb=256 * 65536, ldc=256 * 65536, K=32, ws_bytes=1 << 62) == tm.TM_ERR_INVALID_ARG
+    assert g(M=0) == tm.TM_OK and g(N=0) == tm.TM_OK                   # empty: nothing launched
