@@ -672,6 +672,27 @@ def run_gemm_case(name, args, dev, stream, flush):
         if args.oracle:
             row["oracle"] = time_oracle_gemm(w, a, b, c)
         out.append(row)
+    # context: cuBLAS through torch.matmul on the same operands, fp32 and tf32
+    # math (C = alpha A B + beta C via addmm), same flush and event timing
+    for label, tf32 in (("cublas_fp32", False), ("cublas_tf32", True)):
+        prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = tf32
+        ts = []
+        for rep in range(min(args.reps, 10) + 3):
+            C.copy_(C0)
+            if not args.no_flush:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            torch.addmm(C, A, B, beta=w["beta"], alpha=w["alpha"], out=C)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        torch.backends.cuda.matmul.allow_tf32 = prev
+        t = statistics.median(ts)
+        out.append({"case": name, "kernel": label, "us": round(t * 1e6, 2),
+                    "TFLOPs": round(2.0 * M * N * K / t / 1e12, 2), "note": "library reference, context only"})
     return out
 
 

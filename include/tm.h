@@ -335,9 +335,10 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
  *   + 2^-23 * (|alpha * (A B)_ij| + |beta c_ij|) (3xTF32; tensor-core
  *   accumulation is taken as fp32 with truncation).  Integer-valued inputs
  *   whose partial sums stay below 2^24 give exact results.
- * Errors: INVALID_ARG (extents, NULL, ld, overlap, unknown flag, N beyond
- *   TN * 65535 or a padded extent beyond 2^31 - 1), UNSUPPORTED_TILE, MISALIGNED (a pointer not 4-byte
- *   aligned), BROKEN_PROMISE (host check of TM_ALIGNED), WORKSPACE, CUDA;
+ * Errors: INVALID_ARG (extents, NULL, ld, overlap, unknown flag, a padded
+ *   extent or the tile count beyond 2^31 - 1), UNSUPPORTED_TILE, MISALIGNED
+ *   (a pointer not 4-byte aligned), BROKEN_PROMISE (host check of
+ *   TM_ALIGNED), WORKSPACE, CUDA;
  *   TIMEOUT through tm_check if the tensor-core pipeline stalls (its waits
  *   are bounded; C is then left partly written).
  */

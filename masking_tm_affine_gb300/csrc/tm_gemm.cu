@@ -158,7 +158,10 @@ struct GemmArgs {
     float *C;
     int64_t ldc, M, N;
     float alpha, beta;
-    int KT;  // whole K tiles (of 32) after padding
+    int KT;       // K tiles (of 32) after padding
+    int tiles_m;  // output tiles along M; tile t is (t % tiles_m, t / tiles_m)
+    int ntiles;
+    int vec_c;    // C base 16-byte aligned and ldc % 4 == 0: 16-byte epilogue accesses
     unsigned *status;
 };
 
@@ -171,15 +174,57 @@ struct GemmSmem {
         alignas(1024) float b_lo[BN * GBK];
     };
     Stage st[STAGES];
-    alignas(8) uint64_t full[STAGES];
-    alignas(8) uint64_t empty[STAGES];
-    alignas(8) uint64_t done;
+    alignas(8) uint64_t full[STAGES];   // TMA -> MMA: the stage's operands have landed
+    alignas(8) uint64_t empty[STAGES];  // MMA -> TMA: the MMAs reading the stage are done
+    alignas(8) uint64_t acc_full[2];    // MMA -> epilogue: accumulator buffer holds a finished tile
+    alignas(8) uint64_t acc_empty[2];   // epilogue -> MMA: accumulator buffer has been read out
+    alignas(8) uint64_t done;           // every MMA issued has completed
     uint32_t tmem;
     int abort;
 };
 
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA (and TMEM owner), warps 2-5 epilogue
+
+__device__ __forceinline__ bool gemm_aborted(const int *flag) { return *(volatile const int *)flag != 0; }
+
+// The epilogue waits a whole tile's K loop for its accumulator, so its limit
+// grows with K (a stage takes a few microseconds at most; 40000 cycles are
+// allowed per stage on top of the fixed limit).  A stall inside the pipeline
+// is caught sooner by the producer's and the MMA issuer's own waits, which set
+// the abort flag that this wait also watches.
+__device__ __forceinline__ bool acc_wait(uint32_t bar, uint32_t parity, int KT, const int *abort_flag)
+{
+    if (mbar_try(bar, parity)) return true;
+    const long long limit = kGemmWait + 40000LL * KT;
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (*(volatile const int *)abort_flag != 0 || clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void gemm_fail(int *flag, unsigned *status)
+{
+    atomicOr(status, kStatusTimeout);
+    *(volatile int *)flag = 1;
+}
+
+__device__ __forceinline__ void ld_c4(const float *p, float &a, float &b, float &c, float &d)
+{
+    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "l"(p));
+}
+
+__device__ __forceinline__ void st_c4(float *p, float a, float b, float c, float d)
+{
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// One CTA per SM, persistent over the output tiles (M-fastest, the page's pm =
+// block.x order, so neighbouring CTAs share the B tile in L2).  The accumulator
+// is double-buffered in TMEM (2 x BN columns): the epilogue of one tile runs
+// while the MMAs of the next accumulate into the other buffer.
 template <int BN, int STAGES, bool THREE, bool ALIGNED>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tf32_kernel(const __grid_constant__ CUtensorMap m_ahi, const __grid_constant__ CUtensorMap m_alo,
                      const __grid_constant__ CUtensorMap m_bhi, const __grid_constant__ CUtensorMap m_blo,
                      const GemmArgs g)
@@ -188,19 +233,23 @@ __global__ void __launch_bounds__(128, 1)
     extern __shared__ __align__(1024) unsigned char raw[];
     Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * GBM, n0 = blockIdx.y * BN;  // pm = block.x, pn = block.y as on the page
     constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BN) * GBK * sizeof(float));
+    constexpr uint32_t kCols = 2 * BN;  // TMEM columns: two accumulator buffers
 
-    if (warp == 0) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s.tmem)),
-                     "r"(BN)
+                     "r"(kCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (threadIdx.x == 32) {
+    if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.full[i])));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.empty[i])));
+        }
+        for (int i = 0; i < 2; ++i) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.acc_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(su32(&s.acc_empty[i])));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.done)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -211,99 +260,156 @@ __global__ void __launch_bounds__(128, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s.tmem;
 
-    int issued = 0;  // producer: stages loaded
-    if (threadIdx.x == 0) {
-        // ---------------- producer: TMA copies of the four operand tiles
-        for (int kt = 0; kt < g.KT; ++kt) {
-            const int st = kt % STAGES;
-            if (kt >= STAGES && !mbar_wait(su32(&s.empty[st]), (uint32_t)((kt / STAGES) + 1) & 1u)) {
-                atomicOr(g.status, kStatusTimeout);
-                s.abort = 1;
-                break;
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer: the four operand tiles of every K stage
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < g.ntiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % g.tiles_m) * GBM, n0 = (tile / g.tiles_m) * BN;
+                for (int kt = 0; kt < g.KT; ++kt, ++it) {
+                    const uint32_t st = it % STAGES;
+                    if (it >= STAGES && !mbar_wait(su32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
+                        gemm_fail(&s.abort, g.status);
+                        ok = false;
+                        break;
+                    }
+                    if (gemm_aborted(&s.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = su32(&s.full[st]);
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                                 "r"(kStageBytes)
+                                 : "memory");
+                    const int kx = kt * GBK;
+                    tma_load(su32(s.st[st].a_hi), &m_ahi, kx, m0, bar);
+                    tma_load(su32(s.st[st].b_hi), &m_bhi, kx, n0, bar);
+                    if (THREE) {
+                        tma_load(su32(s.st[st].a_lo), &m_alo, kx, m0, bar);
+                        tma_load(su32(s.st[st].b_lo), &m_blo, kx, n0, bar);
+                    }
+                }
             }
-            const uint32_t bar = su32(&s.full[st]);
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kStageBytes)
-                         : "memory");
-            const int kx = kt * GBK;
-            tma_load(su32(s.st[st].a_hi), &m_ahi, kx, m0, bar);
-            tma_load(su32(s.st[st].b_hi), &m_bhi, kx, n0, bar);
-            if (THREE) {
-                tma_load(su32(s.st[st].a_lo), &m_alo, kx, m0, bar);
-                tma_load(su32(s.st[st].b_lo), &m_blo, kx, n0, bar);
+            if (!ok) {  // nothing may still be landing in shared memory when the CTA leaves
+                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                    mbar_wait(su32(&s.full[j % STAGES]), (j / STAGES) & 1u);
             }
-            issued = kt + 1;
         }
-    } else if (threadIdx.x == 32) {
-        // ---------------- MMA issuer
-        constexpr uint32_t id = idesc_tf32(GBM, BN);
-        bool ok = true;
-        for (int kt = 0; kt < g.KT && ok; ++kt) {
-            const int st = kt % STAGES;
-            if (!mbar_wait(su32(&s.full[st]), (uint32_t)(kt / STAGES) & 1u)) {
-                atomicOr(g.status, kStatusTimeout);
-                s.abort = 1;
-                ok = false;
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer: 3 (or 1) tf32 MMAs per 8-wide K step
+            constexpr uint32_t id = idesc_tf32(GBM, BN);
+            uint32_t it = 0;
+            bool ok = true;
+            int t = 0;
+            for (int tile = blockIdx.x; tile < g.ntiles && ok; tile += gridDim.x, ++t) {
+                const uint32_t ab = (uint32_t)t & 1u;
+                if (t >= 2 && !mbar_wait(su32(&s.acc_empty[ab]), ((uint32_t)(t / 2) - 1) & 1u)) {
+                    gemm_fail(&s.abort, g.status);
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t d = tmem + ab * BN;
+                for (int kt = 0; kt < g.KT; ++kt, ++it) {
+                    const uint32_t st = it % STAGES;
+                    if (!mbar_wait(su32(&s.full[st]), (it / STAGES) & 1u) || gemm_aborted(&s.abort)) {
+                        if (!gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t ahi = su32(s.st[st].a_hi), alo = su32(s.st[st].a_lo);
+                    const uint32_t bhi = su32(s.st[st].b_hi), blo = su32(s.st[st].b_lo);
+#pragma unroll
+                    for (int k = 0; k < GBK / 8; ++k) {
+                        const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
+                        umma_tf32(d, smem_desc(ahi + off), smem_desc(bhi + off), id, (kt | k) != 0);
+                        if (THREE) {
+                            umma_tf32(d, smem_desc(ahi + off), smem_desc(blo + off), id, 1u);
+                            umma_tf32(d, smem_desc(alo + off), smem_desc(bhi + off), id, 1u);
+                        }
+                    }
+                    umma_commit(su32(&s.empty[st]));  // the stage is free once these MMAs are done
+                }
+                if (ok) umma_commit(su32(&s.acc_full[ab]));
+            }
+            umma_commit(su32(&s.done));  // tracks every MMA issued, also after an abort
+            if (!mbar_wait(su32(&s.done), 0u)) gemm_fail(&s.abort, g.status);
+        }
+    } else {
+        // ---------------- epilogue: TMEM rows -> alpha * acc + beta * C
+        const int eg = warp & 3;  // TMEM lane group this warp may access
+        const bool use_c = g.beta != 0.0f;
+        int t = 0;
+        for (int tile = blockIdx.x; tile < g.ntiles; tile += gridDim.x, ++t) {
+            const uint32_t ab = (uint32_t)t & 1u;
+            const int64_t m0 = (int64_t)(tile % g.tiles_m) * GBM, n0 = (int64_t)(tile / g.tiles_m) * BN;
+            const int64_t row = m0 + eg * 32 + lane;
+            const bool row_in = ALIGNED || row < g.M;
+            float *crow = g.C + row * g.ldc + n0;
+            const int ncols = ALIGNED ? BN : (int)(g.N - n0 < BN ? g.N - n0 : BN);
+            if (use_c && row_in) {  // C arrives in L2 while this tile's MMAs run
+                for (int c = 0; c < ncols; c += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + c));
+            }
+            if (!acc_wait(su32(&s.acc_full[ab]), ((uint32_t)t / 2) & 1u, g.KT, &s.abort) || gemm_aborted(&s.abort)) {
+                if (!gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t ahi = su32(s.st[st].a_hi), alo = su32(s.st[st].a_lo);
-            const uint32_t bhi = su32(s.st[st].b_hi), blo = su32(s.st[st].b_lo);
+            const uint32_t tbase = tmem + ((uint32_t)(eg * 32) << 16) + ab * BN;
+            for (int c = 0; c < ncols; c += 32) {  // warp-uniform: the load below is .sync.aligned
+                uint32_t r[32];
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                      "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+                      "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+                      "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                    : "r"(tbase + (uint32_t)c));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (!row_in) continue;
+                float *p = crow + c;
+                if (g.vec_c && (ALIGNED || c + 32 <= ncols)) {
 #pragma unroll
-            for (int k = 0; k < GBK / 8; ++k) {
-                const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
-                umma_tf32(tmem, smem_desc(ahi + off), smem_desc(bhi + off), id, (kt | k) != 0);
-                if (THREE) {
-                    umma_tf32(tmem, smem_desc(ahi + off), smem_desc(blo + off), id, 1u);
-                    umma_tf32(tmem, smem_desc(alo + off), smem_desc(bhi + off), id, 1u);
+                    for (int q = 0; q < 8; ++q) {
+                        float v0 = g.alpha * as_f(r[4 * q]), v1 = g.alpha * as_f(r[4 * q + 1]);
+                        float v2 = g.alpha * as_f(r[4 * q + 2]), v3 = g.alpha * as_f(r[4 * q + 3]);
+                        if (use_c) {
+                            float c0, c1, c2, c3;
+                            ld_c4(p + 4 * q, c0, c1, c2, c3);
+                            v0 = __fmaf_rn(g.beta, c0, v0);
+                            v1 = __fmaf_rn(g.beta, c1, v1);
+                            v2 = __fmaf_rn(g.beta, c2, v2);
+                            v3 = __fmaf_rn(g.beta, c3, v3);
+                        }
+                        st_c4(p + 4 * q, v0, v1, v2, v3);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if (c + e < ncols) {
+                            float v = g.alpha * as_f(r[e]);
+                            if (use_c) v = __fmaf_rn(g.beta, p[e], v);
+                            p[e] = v;
+                        }
+                    }
                 }
             }
-            umma_commit(su32(&s.empty[st]));  // the stage is free once these MMAs are done
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&s.acc_empty[ab])) : "memory");
         }
-        umma_commit(su32(&s.done));  // also after an abort: it tracks every MMA already issued
     }
-    __syncthreads();
 
-    // ---------------- epilogue: TMEM rows -> alpha * acc + beta * C
-    bool ok = !s.abort;
-    if (ok && !mbar_wait(su32(&s.done), 0u)) {
-        if (threadIdx.x == 0) atomicOr(g.status, kStatusTimeout);
-        ok = false;
-    }
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (ok) {
-        const int64_t row = (int64_t)m0 + warp * 32 + lane;
-        const bool row_in = ALIGNED || row < g.M;
-        float *crow = g.C + row * g.ldc;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 8) {
-            uint32_t r[8];
-            const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c;
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                           "=r"(r[7])
-                         : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (!row_in) continue;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int64_t col = (int64_t)n0 + c + e;
-                if (!ALIGNED && col >= g.N) break;
-                float v = g.alpha * as_f(r[e]);
-                if (g.beta != 0.0f) v = __fmaf_rn(g.beta, crow[col], v);
-                crow[col] = v;
-            }
-        }
-    }
-    // nothing may still be landing in this CTA's shared memory or TMEM when it leaves
-    if (threadIdx.x == 0 && !ok) {
-        for (int kt = (issued > STAGES ? issued - STAGES : 0); kt < issued; ++kt)
-            mbar_wait(su32(&s.full[kt % STAGES]), (uint32_t)(kt / STAGES) & 1u);
-        mbar_wait(su32(&s.done), 0u);
-    }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+    }
 }
 
 // ------------------------------------------------------------------ host
@@ -358,7 +464,7 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
 }
 
 template <int BN, int STAGES, bool THREE, bool ALIGNED>
-tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, int64_t tiles_m, int64_t tiles_n, cudaStream_t s)
+tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid, cudaStream_t s)
 {
     const void *k = (const void *)gemm_tf32_kernel<BN, STAGES, THREE, ALIGNED>;
     const size_t smem = sizeof(GemmSmem<BN, STAGES>) + 1024;
@@ -376,7 +482,7 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, int64_t tiles_
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<CUtensorMap *>(&maps[3]),
                     const_cast<GemmArgs *>(&g)};
-    if (cudaLaunchKernel(k, dim3((unsigned)tiles_m, (unsigned)tiles_n), dim3(128), args, smem, s) != cudaSuccess) {
+    if (cudaLaunchKernel(k, dim3(grid), dim3(kGemmThreads), args, smem, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
@@ -384,14 +490,14 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, int64_t tiles_
 }
 
 template <int BN, int STAGES>
-tm_status launch_gemm_bn(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, int64_t tmt,
-                         int64_t tn, cudaStream_t s)
+tm_status launch_gemm_bn(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
+                         cudaStream_t s)
 {
     if (three)
-        return aligned ? launch_gemm<BN, STAGES, true, true>(maps, g, tmt, tn, s)
-                       : launch_gemm<BN, STAGES, true, false>(maps, g, tmt, tn, s);
-    return aligned ? launch_gemm<BN, STAGES, false, true>(maps, g, tmt, tn, s)
-                   : launch_gemm<BN, STAGES, false, false>(maps, g, tmt, tn, s);
+        return aligned ? launch_gemm<BN, STAGES, true, true>(maps, g, grid, s)
+                       : launch_gemm<BN, STAGES, true, false>(maps, g, grid, s);
+    return aligned ? launch_gemm<BN, STAGES, false, true>(maps, g, grid, s)
+                   : launch_gemm<BN, STAGES, false, false>(maps, g, grid, s);
 }
 
 bool disjoint_bytes(const void *a, size_t na, const void *b, size_t nb)
@@ -425,7 +531,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
         if (M % TM != 0 || N % TN != 0 || K % TK != 0) return TM_ERR_BROKEN_PROMISE;
     }
     const GemmPlan pl = gemm_plan(M, N, K, TN);
-    if (pl.Mp > INT32_MAX || pl.Np > INT32_MAX || pl.Kp > INT32_MAX || pl.Np / TN > 65535)
+    if (pl.Mp > INT32_MAX || pl.Np > INT32_MAX || pl.Kp > INT32_MAX || (pl.Mp / GBM) * (pl.Np / TN) > INT32_MAX)
         return TM_ERR_INVALID_ARG;
     if (workspace == nullptr || ws_bytes < pl.bytes || !aligned_to(workspace, 1024)) return TM_ERR_WORKSPACE;
     {
@@ -474,9 +580,13 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     g.alpha = alpha;
     g.beta = beta;
     g.KT = (int)(pl.Kp / GBK);
+    g.tiles_m = (int)(pl.Mp / GBM);
+    g.ntiles = (int)((pl.Mp / GBM) * (pl.Np / TN));
+    g.vec_c = aligned_to(C, 16) && ldc % 4 == 0;
     g.status = dev->status;
     const bool three = !(flags & TM_GEMM_TF32);
     const bool aligned = (flags & TM_ALIGNED) != 0;
-    if (TN == 128) return launch_gemm_bn<128, 3>(three, aligned, maps, g, pl.Mp / GBM, pl.Np / TN, s);
-    return launch_gemm_bn<256, 2>(three, aligned, maps, g, pl.Mp / GBM, pl.Np / TN, s);
+    const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);  // persistent: one CTA per SM
+    if (TN == 128) return launch_gemm_bn<128, 3>(three, aligned, maps, g, grid, s);
+    return launch_gemm_bn<256, 2>(three, aligned, maps, g, grid, s);
 }
