@@ -325,7 +325,9 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
  * K == 0 gives C = beta * C.
  *   A, lda   device input [M, lda]    B, ldb   device input [K, ldb]
  *   C, ldc   device in/out [M, ldc]; C must not overlap A, B or the workspace
- *   TM, TN, TK   the output tile and K tile: TM = 128, TK = 32, TN = 128 or 256
+ *   TM, TN, TK   the output tile and K tile: TM = 128, TN = 128 or 256, TK = 16
+ *            or 32 (the K width of one pipeline stage: TK 16 gives twice as
+ *            many, half-size stages in the same shared memory)
  *   flags    TM_ALIGNED (M % TM == 0, N % TN == 0, K % TK == 0: the output
  *            tiles store without masks), TM_GEMM_TF32
  *   workspace, ws_bytes   device scratch of at least

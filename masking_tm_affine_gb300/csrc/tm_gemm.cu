@@ -34,7 +34,7 @@ namespace libtm {
 namespace {
 
 constexpr int GBM = 128;  // UMMA M (one CTA)
-constexpr int GBK = 32;   // K per stage: one 128-byte swizzle row of fp32
+constexpr int GBK = 32;   // K padding granule of the split operands (a multiple of both stage widths)
 constexpr long long kGemmWait = 2000000000LL;
 
 // ------------------------------------------------------------------ split pass
@@ -116,12 +116,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 
 // Shared-memory matrix descriptor: start >> 4 in [0, 14), leading byte offset
 // >> 4 in [16, 30), stride byte offset >> 4 in [32, 46), descriptor version 1
-// at bit 46, layout 2 (128-byte swizzle) in [61, 64).  K-major with 128-byte
-// rows: consecutive 8-row groups are 1024 bytes apart.
+// at bit 46, layout in [61, 64): 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+// K-major rows of BK fp32 (BK * 4 bytes, the swizzle width): consecutive
+// 8-row groups are 8 * BK * 4 bytes apart.
+template <int BK>
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr)
 {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+    static_assert(BK == 16 || BK == 32, "stage K must fill one 64- or 128-byte swizzle row");
+    constexpr uint64_t kSbo = 8 * BK * 4, kLayout = BK == 32 ? 2 : 4;
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((kSbo >> 4) << 32) | ((uint64_t)1 << 46) |
+           (kLayout << 61);
 }
 
 // Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B tf32
@@ -165,13 +169,13 @@ struct GemmArgs {
     unsigned *status;
 };
 
-template <int BN, int STAGES>
+template <int BN, int BK, int STAGES>
 struct GemmSmem {
     struct Stage {
-        alignas(1024) float a_hi[GBM * GBK];
-        alignas(1024) float a_lo[GBM * GBK];
-        alignas(1024) float b_hi[BN * GBK];
-        alignas(1024) float b_lo[BN * GBK];
+        alignas(1024) float a_hi[GBM * BK];
+        alignas(1024) float a_lo[GBM * BK];
+        alignas(1024) float b_hi[BN * BK];
+        alignas(1024) float b_lo[BN * BK];
     };
     Stage st[STAGES];
     alignas(8) uint64_t full[STAGES];   // TMA -> MMA: the stage's operands have landed
@@ -223,17 +227,34 @@ __device__ __forceinline__ void st_c4(float *p, float a, float b, float c, float
 // block.x order, so neighbouring CTAs share the B tile in L2).  The accumulator
 // is double-buffered in TMEM (2 x BN columns): the epilogue of one tile runs
 // while the MMAs of the next accumulate into the other buffer.
-template <int BN, int STAGES, bool THREE, bool ALIGNED>
+// Output tile t -> (m0, n0): groups of kGroupM tile rows, M-fastest inside a
+// group, so the CTAs running at the same time share a compact block of A and
+// B tiles in L2 (the page's pm = block.x, pn = block.y order within a group).
+constexpr int kGroupM = 16;
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &m0, int &n0, int BN)
+{
+    const int64_t per_group = (int64_t)kGroupM * tiles_n;
+    const int group = (int)(tile / per_group);
+    const int first = group * kGroupM;
+    const int gm = tiles_m - first < kGroupM ? tiles_m - first : kGroupM;
+    const int local = (int)(tile - group * per_group);
+    m0 = (first + local % gm) * GBM;
+    n0 = (local / gm) * BN;
+}
+
+template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tf32_kernel(const __grid_constant__ CUtensorMap m_ahi, const __grid_constant__ CUtensorMap m_alo,
                      const __grid_constant__ CUtensorMap m_bhi, const __grid_constant__ CUtensorMap m_blo,
                      const GemmArgs g)
 {
-    using Smem = GemmSmem<BN, STAGES>;
+    using Smem = GemmSmem<BN, BK, STAGES>;
     extern __shared__ __align__(1024) unsigned char raw[];
     Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BN) * GBK * sizeof(float));
+    const int tiles_n = g.ntiles / g.tiles_m;
+    constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BN) * BK * sizeof(float));
     constexpr uint32_t kCols = 2 * BN;  // TMEM columns: two accumulator buffers
 
     if (warp == 1) {
@@ -266,7 +287,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < g.ntiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % g.tiles_m) * GBM, n0 = (tile / g.tiles_m) * BN;
+                int m0, n0;
+                tile_coords(tile, g.tiles_m, tiles_n, m0, n0, BN);
                 for (int kt = 0; kt < g.KT; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
                     if (it >= STAGES && !mbar_wait(su32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
@@ -282,7 +304,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                                  "r"(kStageBytes)
                                  : "memory");
-                    const int kx = kt * GBK;
+                    const int kx = kt * BK;
                     tma_load(su32(s.st[st].a_hi), &m_ahi, kx, m0, bar);
                     tma_load(su32(s.st[st].b_hi), &m_bhi, kx, n0, bar);
                     if (THREE) {
@@ -322,12 +344,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t ahi = su32(s.st[st].a_hi), alo = su32(s.st[st].a_lo);
                     const uint32_t bhi = su32(s.st[st].b_hi), blo = su32(s.st[st].b_lo);
 #pragma unroll
-                    for (int k = 0; k < GBK / 8; ++k) {
+                    for (int k = 0; k < BK / 8; ++k) {
                         const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
-                        umma_tf32(d, smem_desc(ahi + off), smem_desc(bhi + off), id, (kt | k) != 0);
+                        umma_tf32(d, smem_desc<BK>(ahi + off), smem_desc<BK>(bhi + off), id, (kt | k) != 0);
                         if (THREE) {
-                            umma_tf32(d, smem_desc(ahi + off), smem_desc(blo + off), id, 1u);
-                            umma_tf32(d, smem_desc(alo + off), smem_desc(bhi + off), id, 1u);
+                            umma_tf32(d, smem_desc<BK>(ahi + off), smem_desc<BK>(blo + off), id, 1u);
+                            umma_tf32(d, smem_desc<BK>(alo + off), smem_desc<BK>(bhi + off), id, 1u);
                         }
                     }
                     umma_commit(su32(&s.empty[st]));  // the stage is free once these MMAs are done
@@ -344,7 +366,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int t = 0;
         for (int tile = blockIdx.x; tile < g.ntiles; tile += gridDim.x, ++t) {
             const uint32_t ab = (uint32_t)t & 1u;
-            const int64_t m0 = (int64_t)(tile % g.tiles_m) * GBM, n0 = (int64_t)(tile / g.tiles_m) * BN;
+            int m0i, n0i;
+            tile_coords(tile, g.tiles_m, tiles_n, m0i, n0i, BN);
+            const int64_t m0 = m0i, n0 = n0i;
             const int64_t row = m0 + eg * 32 + lane;
             const bool row_in = ALIGNED || row < g.M;
             float *crow = g.C + row * g.ldc + n0;
@@ -430,14 +454,14 @@ PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn()
     return fn;
 }
 
-bool kmajor_map(CUtensorMap *m, float *base, int64_t rows, int64_t Kp, int box_rows)
+bool kmajor_map(CUtensorMap *m, float *base, int64_t rows, int64_t Kp, int box_rows, int BK)
 {
     const cuuint64_t dims[2] = {(cuuint64_t)Kp, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)Kp * sizeof(float)};
-    const cuuint32_t box[2] = {(cuuint32_t)GBK, (cuuint32_t)box_rows};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
     return gemm_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -463,11 +487,11 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
     return p;
 }
 
-template <int BN, int STAGES, bool THREE, bool ALIGNED>
+template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED>
 tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid, cudaStream_t s)
 {
-    const void *k = (const void *)gemm_tf32_kernel<BN, STAGES, THREE, ALIGNED>;
-    const size_t smem = sizeof(GemmSmem<BN, STAGES>) + 1024;
+    const void *k = (const void *)gemm_tf32_kernel<BN, BK, STAGES, THREE, ALIGNED>;
+    const size_t smem = sizeof(GemmSmem<BN, BK, STAGES>) + 1024;
     static std::once_flag once[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -489,15 +513,17 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
     return TM_OK;
 }
 
-template <int BN, int STAGES>
-tm_status launch_gemm_bn(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
-                         cudaStream_t s)
+// Stages fill about 192 KB of shared memory: 96 KB (TN 256, TK 32), 64 KB
+// (TN 128, TK 32), 48 KB (TN 256, TK 16) or 32 KB (TN 128, TK 16) each.
+template <int BN, int BK, int STAGES>
+tm_status launch_gemm_cfg(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
+                          cudaStream_t s)
 {
     if (three)
-        return aligned ? launch_gemm<BN, STAGES, true, true>(maps, g, grid, s)
-                       : launch_gemm<BN, STAGES, true, false>(maps, g, grid, s);
-    return aligned ? launch_gemm<BN, STAGES, false, true>(maps, g, grid, s)
-                   : launch_gemm<BN, STAGES, false, false>(maps, g, grid, s);
+        return aligned ? launch_gemm<BN, BK, STAGES, true, true>(maps, g, grid, s)
+                       : launch_gemm<BN, BK, STAGES, true, false>(maps, g, grid, s);
+    return aligned ? launch_gemm<BN, BK, STAGES, false, true>(maps, g, grid, s)
+                   : launch_gemm<BN, BK, STAGES, false, false>(maps, g, grid, s);
 }
 
 bool disjoint_bytes(const void *a, size_t na, const void *b, size_t nb)
@@ -523,7 +549,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
 {
     if (M < 0 || N < 0 || K < 0) return TM_ERR_INVALID_ARG;
     if (!flags_ok(flags, TM_ALIGNED | TM_GEMM_TF32)) return TM_ERR_INVALID_ARG;
-    if (TM != GBM || TK != GBK || !(TN == 128 || TN == 256)) return TM_ERR_UNSUPPORTED_TILE;
+    if (TM != GBM || !(TK == 16 || TK == 32) || !(TN == 128 || TN == 256)) return TM_ERR_UNSUPPORTED_TILE;
     if (!valid2d(C, ldc, M, N) || !valid2d(A, lda, M, K) || !valid2d(B, ldb, K, N)) return TM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return TM_OK;
     if (!aligned_to(C, 4) || (K > 0 && (!aligned_to(A, 4) || !aligned_to(B, 4)))) return TM_ERR_MISALIGNED;
@@ -569,8 +595,8 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
 
     // 2. the tensor-core gemm over whole tiles
     CUtensorMap maps[4];
-    if (!kmajor_map(&maps[0], ahi, pl.Mp, pl.Kp, GBM) || !kmajor_map(&maps[1], alo, pl.Mp, pl.Kp, GBM) ||
-        !kmajor_map(&maps[2], bhi, pl.Np, pl.Kp, TN) || !kmajor_map(&maps[3], blo, pl.Np, pl.Kp, TN))
+    if (!kmajor_map(&maps[0], ahi, pl.Mp, pl.Kp, GBM, TK) || !kmajor_map(&maps[1], alo, pl.Mp, pl.Kp, GBM, TK) ||
+        !kmajor_map(&maps[2], bhi, pl.Np, pl.Kp, TN, TK) || !kmajor_map(&maps[3], blo, pl.Np, pl.Kp, TN, TK))
         return TM_ERR_CUDA;
     GemmArgs g;
     g.C = C;
@@ -579,7 +605,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     g.N = N;
     g.alpha = alpha;
     g.beta = beta;
-    g.KT = (int)(pl.Kp / GBK);
+    g.KT = (int)(pl.Kp / TK);
     g.tiles_m = (int)(pl.Mp / GBM);
     g.ntiles = (int)((pl.Mp / GBM) * (pl.Np / TN));
     g.vec_c = aligned_to(C, 16) && ldc % 4 == 0;
@@ -587,6 +613,10 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     const bool three = !(flags & TM_GEMM_TF32);
     const bool aligned = (flags & TM_ALIGNED) != 0;
     const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);  // persistent: one CTA per SM
-    if (TN == 128) return launch_gemm_bn<128, 3>(three, aligned, maps, g, grid, s);
-    return launch_gemm_bn<256, 2>(three, aligned, maps, g, grid, s);
+    if (TK == 32) {
+        if (TN == 128) return launch_gemm_cfg<128, 32, 3>(three, aligned, maps, g, grid, s);
+        return launch_gemm_cfg<256, 32, 2>(three, aligned, maps, g, grid, s);
+    }
+    if (TN == 128) return launch_gemm_cfg<128, 16, 6>(three, aligned, maps, g, grid, s);
+    return launch_gemm_cfg<256, 16, 4>(three, aligned, maps, g, grid, s);
 }

@@ -34,7 +34,7 @@ def workspace(M, N, K, TN):
     return raw, (base + 1023) // 1024 * 1024, ws
 
 
-def run(a, b, c, alpha, beta, TN=256, flags=0, lda=None, ldb=None, ldc=None):
+def run(a, b, c, alpha, beta, TN=256, flags=0, lda=None, ldb=None, ldc=None, TK=32):
     """C <- alpha a b + beta c on the GPU; returns (the [M, ldc] result, the
     padded host inputs, and a guard check)."""
     M, K = a.shape
@@ -45,7 +45,7 @@ def run(a, b, c, alpha, beta, TN=256, flags=0, lda=None, ldb=None, ldc=None):
     Ch = synth.pad_rows(c, ldc) if M and N else np.zeros(max(M * ldc, 1), np.float32)
     AD, BD, CD = DevBuf(Ah), DevBuf(Bh), DevBuf(Ch)
     raw, ws, wsb = workspace(max(M, 1), max(N, 1), K, TN)
-    tm.tm_gemm(AD.ptr, lda, BD.ptr, ldb, CD.ptr, ldc, M, N, K, alpha, beta, ws, wsb, 128, TN, 32, flags)
+    tm.tm_gemm(AD.ptr, lda, BD.ptr, ldb, CD.ptr, ldc, M, N, K, alpha, beta, ws, wsb, 128, TN, TK, flags)
     tm.tm_check()
     assert AD.guards_intact() and BD.guards_intact() and CD.guards_intact()
     out = CD.payload_f32()
@@ -71,22 +71,24 @@ SHAPES = [(1, 1, 1), (1, 5, 3), (7, 9, 13), (128, 256, 32), (128, 128, 64), (130
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("TN", [128, 256])
+@pytest.mark.parametrize("TK", [16, 32])
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
-def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, flags):
+def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags):
     a, b, c = ints((M, K), 11 + M), ints((K, N), 12 + N), ints((M, N), 13 + K)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, lda=K + 3, ldb=N + 1, ldc=N + 2)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, lda=K + 3, ldb=N + 1, ldc=N + 2, TK=TK)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, 0.5)
     got = out.reshape(M, ldc)[:, :N]
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 32), (256, 512, 1024), (384, 128, 96)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 32), (256, 512, 1024), (384, 128, 96), (2048, 1024, 48)])
 @pytest.mark.parametrize("TN", [128, 256])
-def test_gemm_aligned_promise_exact(cuda, oracle, M, N, K, TN):
-    if N % TN:
-        pytest.skip("N not a multiple of TN")
+@pytest.mark.parametrize("TK", [16, 32])
+def test_gemm_aligned_promise_exact(cuda, oracle, M, N, K, TN, TK):
+    if N % TN or K % TK:
+        pytest.skip("N not a multiple of TN or K not a multiple of TK")
     a, b, c = ints((M, K), 21), ints((K, N), 22), ints((M, N), 23)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, -1.0, 2.0, TN, tm.TM_ALIGNED)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, -1.0, 2.0, TN, tm.TM_ALIGNED, TK=TK)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, -1.0, 2.0)
     assert np.array_equal(out.reshape(M, N).view(np.uint32), want.view(np.uint32))
 
@@ -115,13 +117,15 @@ def test_gemm_single_product_split_accuracy(cuda, oracle, flags):
         assert rel.max() > 2.0 ** -16, "tf32-only result unexpectedly accurate"
 
 
-@pytest.mark.parametrize("M,N,K", [(130, 200, 1000), (257, 300, 33), (1, 1000, 4099), (500, 37, 1)])
+@pytest.mark.parametrize("M,N,K", [(130, 200, 1000), (257, 300, 33), (1, 1000, 4099), (500, 37, 1),
+                                   (2100, 700, 260)])
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
-def test_gemm_real_within_bound(cuda, oracle, M, N, K, flags):
+@pytest.mark.parametrize("TN,TK", [(256, 32), (128, 16)])
+def test_gemm_real_within_bound(cuda, oracle, M, N, K, flags, TN, TK):
     a = synth.uniform((M, K), -1.0, 1.0, 41)
     b = synth.normal((K, N), 42)
     c = synth.uniform((M, N), -4.0, 4.0, 43)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, -0.5, 256, flags)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, -0.5, TN, flags, TK=TK)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, -0.5)
     got = out.reshape(M, N)
     err = np.abs(got.astype(np.float64) - want)
@@ -160,7 +164,7 @@ def test_gemm_errors(cuda):
     base = (AD.ptr, 16, BD.ptr, 16, CD.ptr, 16, 16, 16, 16, 1.0, 0.0)
     assert status(*base, ws, wsb, TM=64) == tm.TM_ERR_UNSUPPORTED_TILE
     assert status(*base, ws, wsb, TN=64) == tm.TM_ERR_UNSUPPORTED_TILE
-    assert status(*base, ws, wsb, TK=16) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert status(*base, ws, wsb, TK=8) == tm.TM_ERR_UNSUPPORTED_TILE
     assert status(*base, ws, wsb, flags=tm.TM_ALIGNED) == tm.TM_ERR_BROKEN_PROMISE
     assert status(*base, ws, wsb, flags=0x2) == tm.TM_ERR_INVALID_ARG
     assert status(*base, ws, wsb - 4) == tm.TM_ERR_WORKSPACE
