@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kNaiveRows) colsum_naive(const float *__restri
                                                            int64_t N, float *__restrict__ part, int64_t npad,
                                                            int64_t programs)
 {
+    pdl_trigger();  // the finish may launch once every block has started
     __shared__ float warp_sums[kNaiveRows / 32];
     for (int64_t pid = blockIdx.x; pid < programs; pid += gridDim.x) {
         const int64_t col = pid % N;  // neighbouring programs read neighbouring columns
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(256) colsum_finish(const float *__restrict__ p
                                                      int64_t N, float *__restrict__ c)
 {
     __shared__ float grp[kFinishPG][33];
+    pdl_wait();  // launched as a dependent of the partial-sum pass: its writes first
     const int cx = threadIdx.x & 31, py = threadIdx.x >> 5;
     const int64_t per = (P + kFinishPG - 1) / kFinishPG;
     const int64_t p_lo = py * per;
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
     constexpr int UNR = 8;                // rows in flight per thread
     static_assert(CL * RL == kThreads, "strip does not fit the block");
     __shared__ float red[RL][TN];
+    pdl_trigger();  // the finish may launch once every block has started
 
     if constexpr (ALIGNED) {
         const bool whole = (a.M % a.TM == 0) && (a.N % TN == 0);
@@ -257,6 +260,7 @@ template <int TM, int TN, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
                                                           int stages)
 {
+    pdl_trigger();  // the finish may launch once every block has started
     constexpr int CL = TN / 4;            // column lanes, 4 columns each
     constexpr int RL = kThreads / CL;     // row lanes
     constexpr int TILE = TM * TN;         // floats per stage
@@ -470,10 +474,13 @@ tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, cudaStrea
     return TM_OK;
 }
 
+// The finish runs as a programmatic dependent of the partial-sum pass, which
+// releases it as soon as its last block has started: the finish's blocks are
+// resident and waiting (pdl_wait) when the partial sums land.
 tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, float *c, cudaStream_t s)
 {
-    colsum_finish<<<flat_grid((N + 31) / 32), 256, 0, s>>>(part, npad, P, N, c);
-    return launch_status();
+    void *args[] = {const_cast<float **>(&part), &npad, &P, &N, &c};
+    return launch_dependent((const void *)colsum_finish, dim3(flat_grid((N + 31) / 32)), dim3(256), args, 0, s);
 }
 
 enum class Variant { Naive, RegDirect, Staged };

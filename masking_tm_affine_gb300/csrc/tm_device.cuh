@@ -95,6 +95,16 @@ __device__ __forceinline__ void st_v8(void *p, const u32x8 &x)
 }
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
+
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start (and run its prologue) while the
+// kernel before it in the stream finishes; pdl_wait() then blocks the calling
+// thread until that kernel has completed and its writes are visible.  In a
+// normally launched kernel both are no-ops.  pdl_trigger() lets the dependent
+// launch begin once every block of this grid has issued it or exited.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ uint32_t as_u(float f) { return __float_as_uint(f); }
 
 // ---------------------------------------------------------------- tile walk

@@ -45,46 +45,48 @@ __device__ __forceinline__ uint32_t to_tf32(float x)
     return r;
 }
 
-// A: hi/lo [Mp, Kp] row-major (K-major operand), zero outside [M, K].  Blocks
-// over rows, threads over k: both sides coalesced.
-__global__ void __launch_bounds__(256) split_rows(const float *__restrict__ A, int64_t lda, int64_t M, int64_t K,
-                                                  float *__restrict__ hi, float *__restrict__ lo, int64_t Mp,
-                                                  int64_t Kp)
+// One launch splits both operands.  Blocks [0, blocks_a) walk A's rows
+// (threads over k, both sides coalesced) into hi/lo [Mp, Kp]; the rest walk
+// 32 x 32 tiles of B through shared memory into the transposed hi/lo
+// [Np, Kp].  Everything outside [M, K] (resp. [K, N]) is written as zero.
+struct SplitArgs {
+    const float *A, *B;
+    int64_t lda, ldb, M, N, K, Mp, Np, Kp;
+    float *ahi, *alo, *bhi, *blo;
+    unsigned blocks_a, blocks_b;
+};
+
+__device__ __forceinline__ void split_store(float *hi, float *lo, int64_t at, float x)
 {
-    for (int64_t i = blockIdx.x; i < Mp; i += gridDim.x) {
-        for (int64_t k = threadIdx.x; k < Kp; k += blockDim.x) {
-            const float x = (i < M && k < K) ? as_f(ld_nc_b32(A + i * lda + k)) : 0.0f;
-            const uint32_t h = to_tf32(x);
-            hi[i * Kp + k] = as_f(h);
-            lo[i * Kp + k] = as_f(to_tf32(x - as_f(h)));
-        }
-    }
+    const uint32_t h = to_tf32(x);
+    hi[at] = as_f(h);
+    lo[at] = as_f(to_tf32(x - as_f(h)));
 }
 
-// B [K, N] -> hi/lo [Np, Kp] (transposed, K-major), zero outside; 32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) split_transpose(const float *__restrict__ B, int64_t ldb, int64_t K,
-                                                       int64_t N, float *__restrict__ hi, float *__restrict__ lo,
-                                                       int64_t Np, int64_t Kp)
+__global__ void __launch_bounds__(256) split_operands(const SplitArgs a)
 {
     __shared__ float t[32][33];
-    const int64_t tiles_k = Kp / 32, tiles_n = Np / 32;
-    for (int64_t tile = blockIdx.x; tile < tiles_k * tiles_n; tile += gridDim.x) {
+    pdl_trigger();  // the gemm's prologue may start once every block has started
+    if (blockIdx.x < a.blocks_a) {
+        for (int64_t i = blockIdx.x; i < a.Mp; i += a.blocks_a)
+            for (int64_t k = threadIdx.x; k < a.Kp; k += blockDim.x) {
+                const float x = (i < a.M && k < a.K) ? as_f(ld_nc_b32(a.A + i * a.lda + k)) : 0.0f;
+                split_store(a.ahi, a.alo, i * a.Kp + k, x);
+            }
+        return;
+    }
+    const int64_t tiles_k = a.Kp / 32, tiles_n = a.Np / 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    for (int64_t tile = blockIdx.x - a.blocks_a; tile < tiles_k * tiles_n; tile += a.blocks_b) {
         const int64_t k0 = (tile / tiles_n) * 32, n0 = (tile % tiles_n) * 32;
-        const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
 #pragma unroll
         for (int r = ty; r < 32; r += 8) {
             const int64_t k = k0 + r, n = n0 + tx;
-            t[r][tx] = (k < K && n < N) ? as_f(ld_nc_b32(B + k * ldb + n)) : 0.0f;
+            t[r][tx] = (k < a.K && n < a.N) ? as_f(ld_nc_b32(a.B + k * a.ldb + n)) : 0.0f;
         }
         __syncthreads();
 #pragma unroll
-        for (int r = ty; r < 32; r += 8) {
-            const int64_t n = n0 + r, k = k0 + tx;
-            const float x = t[tx][r];
-            const uint32_t h = to_tf32(x);
-            hi[n * Kp + k] = as_f(h);
-            lo[n * Kp + k] = as_f(to_tf32(x - as_f(h)));
-        }
+        for (int r = ty; r < 32; r += 8) split_store(a.bhi, a.blo, (n0 + r) * a.Kp + k0 + tx, t[tx][r]);
         __syncthreads();
     }
 }
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s.tmem;
+    pdl_wait();  // launched as a dependent of the split pass: its operands first
 
     if (warp == 0) {
         if (lane == 0) {
@@ -506,11 +509,7 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<CUtensorMap *>(&maps[3]),
                     const_cast<GemmArgs *>(&g)};
-    if (cudaLaunchKernel(k, dim3(grid), dim3(kGemmThreads), args, smem, s) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_dependent(k, dim3(grid), dim3(kGemmThreads), args, smem, s);
 }
 
 // Stages fill about 192 KB of shared memory: 96 KB (TN 256, TK 32), 64 KB
@@ -588,9 +587,32 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     float *bhi = reinterpret_cast<float *>(ws + pl.off[2]), *blo = reinterpret_cast<float *>(ws + pl.off[3]);
 
     // 1. split (and transpose B) into zero-padded K-major tf32 hi/lo operands
-    split_rows<<<flat_grid(pl.Mp < 8LL * dev->sms ? pl.Mp : 8LL * dev->sms), 256, 0, s>>>(A, lda, M, K, ahi, alo, pl.Mp, pl.Kp);
-    if ((st = launch_status()) != TM_OK) return st;
-    split_transpose<<<flat_grid((pl.Kp / 32) * (pl.Np / 32)), 256, 0, s>>>(B, ldb, K, N, bhi, blo, pl.Np, pl.Kp);
+    SplitArgs sa;
+    sa.A = A;
+    sa.B = B;
+    sa.lda = lda;
+    sa.ldb = ldb;
+    sa.M = M;
+    sa.N = N;
+    sa.K = K;
+    sa.Mp = pl.Mp;
+    sa.Np = pl.Np;
+    sa.Kp = pl.Kp;
+    sa.ahi = ahi;
+    sa.alo = alo;
+    sa.bhi = bhi;
+    sa.blo = blo;
+    {
+        // A: up to 8 blocks per SM over rows (each streams whole padded rows);
+        // B: up to 32 per SM over 32 x 32 tiles (each tile is a short
+        // load-transpose-store round trip, so more blocks keep more in flight)
+        const int64_t tiles_b = (pl.Kp / 32) * (pl.Np / 32);
+        const int64_t na = pl.Mp < 8LL * dev->sms ? pl.Mp : 8LL * dev->sms;
+        const int64_t nb = tiles_b < 32LL * dev->sms ? tiles_b : 32LL * dev->sms;
+        sa.blocks_a = (unsigned)na;
+        sa.blocks_b = (unsigned)nb;
+    }
+    split_operands<<<sa.blocks_a + sa.blocks_b, 256, 0, s>>>(sa);
     if ((st = launch_status()) != TM_OK) return st;
 
     // 2. the tensor-core gemm over whole tiles

@@ -43,6 +43,29 @@ inline tm_status launch_status()
 
 inline cudaStream_t as_stream(tm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Launch `kernel` as a programmatic dependent of the previous kernel in the
+// stream (see pdl_wait in tm_device.cuh): its blocks may start while that
+// kernel drains; the kernel must pdl_wait() before reading what it produced.
+inline tm_status launch_dependent(const void *kernel, dim3 grid, dim3 block, void **args, size_t smem,
+                                  cudaStream_t s)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
 inline bool aligned_to(const void *p, uintptr_t bytes)
 {
     return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
