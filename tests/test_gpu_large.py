@@ -88,3 +88,42 @@ def test_reductions_past_2_31_elements(cuda, oracle):
     got = c.cpu().numpy()[cols].astype(np.float64)
     assert np.all(np.abs(got - exact) <= 1e-5 * (np.abs(h - 1019).sum(axis=0) / 64.0))
     del X, W
+
+
+def small_pattern(rows, cols, seed, row0=0):
+    """fp32 values k/64 with |k| <= 16 from the same kind of seeded hash: with
+    K <= 1040 every product and partial sum of two of them is exact in fp32."""
+    i = torch.arange(row0, row0 + rows, device="cuda", dtype=torch.int64)[:, None]
+    j = torch.arange(cols, device="cuda", dtype=torch.int64)[None, :]
+    h = (i * 1000003 + j * 7919 + seed * 104729) % 33
+    return ((h - 16).to(torch.float32) / 64.0)
+
+
+def small_pattern_host(rows_idx, cols, seed):
+    i = np.asarray(rows_idx, dtype=np.int64)[:, None]
+    j = np.arange(cols, dtype=np.int64)[None, :]
+    h = (i * 1000003 + j * 7919 + seed * 104729) % 33
+    return ((h - 16).astype(np.float32) / np.float32(64.0))
+
+
+def test_gemm_past_2_31_elements(cuda, oracle):
+    # A [2^21 + 5, 1040]: 2.18e9 elements (8.7 GB), its split operands 17.7 GB;
+    # ragged in M (5 rows past a 128-row tile), N (72 of a 128-wide tile) and K
+    M, N, K = (1 << 21) + 5, 72, 1040
+    A = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    step = 1 << 18
+    for r0 in range(0, M, step):  # built in slices to bound the index temporaries
+        A[r0:r0 + step] = small_pattern(min(step, M - r0), K, 5, r0)
+    B = small_pattern(K, N, 6)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    wsb = tm.tm_gemm_workspace_bytes(M, N, K, 128)
+    raw = torch.empty(wsb + 1024, dtype=torch.uint8, device="cuda")
+    ws = (raw.data_ptr() + 1023) // 1024 * 1024
+    tm.tm_gemm(A, K, B, N, C, N, M, N, K, 1.0, 0.0, ws, wsb, 128, 128, 16)
+    tm.tm_check()
+    rows = [0, 1, 127, 128, M // 2, M - 6, M - 5, M - 1]
+    a = small_pattern_host(rows, K, 5)
+    b = small_pattern_host(np.arange(K), N, 6)
+    want = oracle.gemm_rows(a, K, b, N, None, 0, np.arange(len(rows)), N, K, 1.0, 0.0)
+    assert np.array_equal(C[rows].cpu().numpy(), want)
+    del A, B, C, raw
