@@ -12,17 +12,22 @@
 // hi + lo with hi = x rounded to tf32 and lo = (x - hi) rounded to tf32, and
 // the product is hi*hi + hi*lo + lo*hi (the lo*lo term is below fp32
 // resolution); TM_GEMM_TF32 keeps the single hi*hi pass instead.
-//   1. split pass (memory-bound): A [M, K] and B [K, N] become K-major hi/lo
-//      operands zero-padded to whole tiles -- the zero padding is exactly the
-//      masked remainder tile's fill -- with B transposed on the way.
-//   2. gemm: one 128 x BN output tile per CTA, flat grid.  One thread issues
-//      TMA copies (128-byte swizzle, K-major) into a ring of STAGES shared-
-//      memory stages; one thread issues the MMAs (K = 8 per instruction, four
-//      per 32-wide K tile, three passes each) and commits each stage back to
-//      the producer through an mbarrier; the four warps then read the
-//      accumulator rows out of TMEM (32x32b loads) and write
-//      alpha * acc + beta * C, masking the M and N edges unless the promise
-//      holds.  Every wait is bounded; a stalled pipeline sets the status word.
+//   1. split pass (one launch, memory-bound): A [M, K] and B [K, N] become
+//      K-major hi/lo operands zero-padded to whole tiles -- the zero padding
+//      is exactly the masked remainder tile's fill -- with B transposed on
+//      the way.
+//   2. gemm (a programmatic dependent of the split): persistent, one
+//      192-thread CTA per SM walking 128 x BN output tiles.  Warp 0 issues
+//      TMA copies (K-major, 64- or 128-byte swizzle) into a ring of STAGES
+//      shared-memory stages; warp 1 owns the TMEM accumulators (two buffers
+//      of BN columns) and one of its threads issues the MMAs (K = 8 each,
+//      three per K step for 3xTF32), committing each stage back to the
+//      producer and each finished tile to the epilogue through mbarriers;
+//      warps 2-5 read the other accumulator buffer out of TMEM (32x32b loads)
+//      and write alpha * acc + beta * C, masking the M and N edges unless the
+//      promise holds, while the next tile accumulates.  Every wait is
+//      bounded; a stalled pipeline sets the status word and the CTA drains
+//      and frees its TMEM before it exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,7 +40,7 @@ namespace {
 
 constexpr int GBM = 128;  // UMMA M (one CTA)
 constexpr int GBK = 32;   // K padding granule of the split operands (a multiple of both stage widths)
-constexpr long long kGemmWait = 2000000000LL;
+constexpr long long kGemmWait = 2000000000LL;  // clock64 cycles (~1 s) a pipeline wait may take
 
 // ------------------------------------------------------------------ split pass
 __device__ __forceinline__ uint32_t to_tf32(float x)
@@ -49,6 +54,7 @@ __device__ __forceinline__ uint32_t to_tf32(float x)
 // (threads over k, both sides coalesced) into hi/lo [Mp, Kp]; the rest walk
 // 32 x 32 tiles of B through shared memory into the transposed hi/lo
 // [Np, Kp].  Everything outside [M, K] (resp. [K, N]) is written as zero.
+// With alo == blo == nullptr (the single-pass mode) only hi is written.
 struct SplitArgs {
     const float *A, *B;
     int64_t lda, ldb, M, N, K, Mp, Np, Kp;
@@ -60,7 +66,7 @@ __device__ __forceinline__ void split_store(float *hi, float *lo, int64_t at, fl
 {
     const uint32_t h = to_tf32(x);
     hi[at] = as_f(h);
-    lo[at] = as_f(to_tf32(x - as_f(h)));
+    if (lo != nullptr) lo[at] = as_f(to_tf32(x - as_f(h)));
 }
 
 __global__ void __launch_bounds__(256) split_operands(const SplitArgs a)
@@ -164,21 +170,32 @@ struct GemmArgs {
     float *C;
     int64_t ldc, M, N;
     float alpha, beta;
-    int KT;       // K tiles (of 32) after padding
-    int tiles_m;  // output tiles along M; tile t is (t % tiles_m, t / tiles_m)
-    int ntiles;
+    int KT;       // pipeline stages per output tile: Kp / BK
+    int tiles_m;  // output tiles along M (tile order: tile_coords)
+    int ntiles;   // tiles_m * tiles along N
     int vec_c;    // C base 16-byte aligned and ldc % 4 == 0: 16-byte epilogue accesses
     unsigned *status;
 };
 
-template <int BN, int BK, int STAGES>
+template <int BN, int BK, bool THREE>
+struct GemmStage {
+    static constexpr int kLo = THREE ? 1 : 0;  // the single-pass mode keeps no lo operands
+    alignas(1024) float a_hi[GBM * BK];
+    alignas(1024) float b_hi[BN * BK];
+    alignas(1024) float a_lo[kLo * GBM * BK + (1 - kLo)];
+    alignas(1024) float b_lo[kLo * BN * BK + (1 - kLo)];
+};
+
+// Stages that fit the ~192 KB of shared memory given to the ring.
+template <int BN, int BK, bool THREE>
+constexpr int gemm_stages()
+{
+    return (int)((192u * 1024u) / sizeof(GemmStage<BN, BK, THREE>));
+}
+
+template <int BN, int BK, int STAGES, bool THREE>
 struct GemmSmem {
-    struct Stage {
-        alignas(1024) float a_hi[GBM * BK];
-        alignas(1024) float a_lo[GBM * BK];
-        alignas(1024) float b_hi[BN * BK];
-        alignas(1024) float b_lo[BN * BK];
-    };
+    using Stage = GemmStage<BN, BK, THREE>;
     Stage st[STAGES];
     alignas(8) uint64_t full[STAGES];   // TMA -> MMA: the stage's operands have landed
     alignas(8) uint64_t empty[STAGES];  // MMA -> TMA: the MMAs reading the stage are done
@@ -225,16 +242,12 @@ __device__ __forceinline__ void st_c4(float *p, float a, float b, float c, float
     asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-// One CTA per SM, persistent over the output tiles (M-fastest, the page's pm =
-// block.x order, so neighbouring CTAs share the B tile in L2).  The accumulator
-// is double-buffered in TMEM (2 x BN columns): the epilogue of one tile runs
-// while the MMAs of the next accumulate into the other buffer.
 // Output tile t -> (m0, n0): groups of kGroupM tile rows, M-fastest inside a
 // group, so the CTAs running at the same time share a compact block of A and
 // B tiles in L2 (the page's pm = block.x, pn = block.y order within a group).
 constexpr int kGroupM = 16;
 
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int &m0, int &n0, int BN)
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int BN, int &m0, int &n0)
 {
     const int64_t per_group = (int64_t)kGroupM * tiles_n;
     const int group = (int)(tile / per_group);
@@ -245,13 +258,16 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     n0 = (local / gm) * BN;
 }
 
+// One CTA per SM, persistent over the output tiles in tile_coords order.  The
+// accumulator is double-buffered in TMEM (2 x BN columns): the epilogue of one
+// tile runs while the MMAs of the next accumulate into the other buffer.
 template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tf32_kernel(const __grid_constant__ CUtensorMap m_ahi, const __grid_constant__ CUtensorMap m_alo,
                      const __grid_constant__ CUtensorMap m_bhi, const __grid_constant__ CUtensorMap m_blo,
                      const GemmArgs g)
 {
-    using Smem = GemmSmem<BN, BK, STAGES>;
+    using Smem = GemmSmem<BN, BK, STAGES, THREE>;
     extern __shared__ __align__(1024) unsigned char raw[];
     Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < g.ntiles && ok; tile += gridDim.x) {
                 int m0, n0;
-                tile_coords(tile, g.tiles_m, tiles_n, m0, n0, BN);
+                tile_coords(tile, g.tiles_m, tiles_n, BN, m0, n0);
                 for (int kt = 0; kt < g.KT; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
                     if (it >= STAGES && !mbar_wait(su32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int tile = blockIdx.x; tile < g.ntiles; tile += gridDim.x, ++t) {
             const uint32_t ab = (uint32_t)t & 1u;
             int m0i, n0i;
-            tile_coords(tile, g.tiles_m, tiles_n, m0i, n0i, BN);
+            tile_coords(tile, g.tiles_m, tiles_n, BN, m0i, n0i);
             const int64_t m0 = m0i, n0 = n0i;
             const int64_t row = m0 + eg * 32 + lane;
             const bool row_in = ALIGNED || row < g.M;
@@ -490,11 +506,13 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
     return p;
 }
 
-template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED>
+template <int BN, int BK, bool THREE, bool ALIGNED>
 tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid, cudaStream_t s)
 {
+    constexpr int STAGES = gemm_stages<BN, BK, THREE>();
+    static_assert(STAGES >= 2, "shared-memory ring needs two stages");
     const void *k = (const void *)gemm_tf32_kernel<BN, BK, STAGES, THREE, ALIGNED>;
-    const size_t smem = sizeof(GemmSmem<BN, BK, STAGES>) + 1024;
+    const size_t smem = sizeof(GemmSmem<BN, BK, STAGES, THREE>) + 1024;
     static std::once_flag once[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -512,17 +530,18 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
     return launch_dependent(k, dim3(grid), dim3(kGemmThreads), args, smem, s);
 }
 
-// Stages fill about 192 KB of shared memory: 96 KB (TN 256, TK 32), 64 KB
-// (TN 128, TK 32), 48 KB (TN 256, TK 16) or 32 KB (TN 128, TK 16) each.
-template <int BN, int BK, int STAGES>
+// Stages fill about 192 KB of shared memory: 3xTF32 stages hold hi and lo of
+// both operands (96 KB at TN 256 and TK 32, 48 KB at TK 16, ...), single-pass
+// stages only hi, so that mode runs twice as many.
+template <int BN, int BK>
 tm_status launch_gemm_cfg(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
                           cudaStream_t s)
 {
     if (three)
-        return aligned ? launch_gemm<BN, BK, STAGES, true, true>(maps, g, grid, s)
-                       : launch_gemm<BN, BK, STAGES, true, false>(maps, g, grid, s);
-    return aligned ? launch_gemm<BN, BK, STAGES, false, true>(maps, g, grid, s)
-                   : launch_gemm<BN, BK, STAGES, false, false>(maps, g, grid, s);
+        return aligned ? launch_gemm<BN, BK, true, true>(maps, g, grid, s)
+                       : launch_gemm<BN, BK, true, false>(maps, g, grid, s);
+    return aligned ? launch_gemm<BN, BK, false, true>(maps, g, grid, s)
+                   : launch_gemm<BN, BK, false, false>(maps, g, grid, s);
 }
 
 bool disjoint_bytes(const void *a, size_t na, const void *b, size_t nb)
@@ -598,10 +617,11 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     sa.Mp = pl.Mp;
     sa.Np = pl.Np;
     sa.Kp = pl.Kp;
+    const bool three = !(flags & TM_GEMM_TF32);
     sa.ahi = ahi;
-    sa.alo = alo;
+    sa.alo = three ? alo : nullptr;
     sa.bhi = bhi;
-    sa.blo = blo;
+    sa.blo = three ? blo : nullptr;
     {
         // A: up to 8 blocks per SM over rows (each streams whole padded rows);
         // B: up to 32 per SM over 32 x 32 tiles (each tile is a short
@@ -632,13 +652,12 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     g.ntiles = (int)((pl.Mp / GBM) * (pl.Np / TN));
     g.vec_c = aligned_to(C, 16) && ldc % 4 == 0;
     g.status = dev->status;
-    const bool three = !(flags & TM_GEMM_TF32);
     const bool aligned = (flags & TM_ALIGNED) != 0;
     const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);  // persistent: one CTA per SM
     if (TK == 32) {
-        if (TN == 128) return launch_gemm_cfg<128, 32, 3>(three, aligned, maps, g, grid, s);
-        return launch_gemm_cfg<256, 32, 2>(three, aligned, maps, g, grid, s);
+        if (TN == 128) return launch_gemm_cfg<128, 32>(three, aligned, maps, g, grid, s);
+        return launch_gemm_cfg<256, 32>(three, aligned, maps, g, grid, s);
     }
-    if (TN == 128) return launch_gemm_cfg<128, 16, 6>(three, aligned, maps, g, grid, s);
-    return launch_gemm_cfg<256, 16, 4>(three, aligned, maps, g, grid, s);
+    if (TN == 128) return launch_gemm_cfg<128, 16>(three, aligned, maps, g, grid, s);
+    return launch_gemm_cfg<256, 16>(three, aligned, maps, g, grid, s);
 }
