@@ -173,7 +173,7 @@ struct GemmArgs {
     int KT;       // pipeline stages per output tile: Kp / BK
     int tiles_m;  // output tiles along M (tile order: tile_coords)
     int ntiles;   // tiles_m * tiles along N
-    int vec_c;    // C base 16-byte aligned and ldc % 4 == 0: 16-byte epilogue accesses
+    int vec_c;    // C base 16-byte aligned, ldc % 4 == 0 and N % 4 == 0: the epilogue moves C by TMA
     unsigned *status;
 };
 
@@ -186,7 +186,8 @@ struct GemmStage {
     alignas(1024) float b_lo[kLo * BN * BK + (1 - kLo)];
 };
 
-// Stages that fit the ~192 KB of shared memory given to the ring.
+// Stages that fit the 192 KB of shared memory given to the ring (the C
+// staging buffers take 32 KB more, inside the 227 KB a CTA may have).
 template <int BN, int BK, bool THREE>
 constexpr int gemm_stages()
 {
@@ -197,6 +198,10 @@ template <int BN, int BK, int STAGES, bool THREE>
 struct GemmSmem {
     using Stage = GemmStage<BN, BK, THREE>;
     Stage st[STAGES];
+    // epilogue staging: per epilogue warp two 32 x 32 fp32 chunks of C in the
+    // TMA 128-byte-swizzled layout (row r's 16-byte piece j at j ^ (r % 8))
+    alignas(1024) float cbuf[4][2][32 * 32];
+    alignas(8) uint64_t cbar[4][2];     // TMA -> epilogue warp: the chunk of C has landed
     alignas(8) uint64_t full[STAGES];   // TMA -> MMA: the stage's operands have landed
     alignas(8) uint64_t empty[STAGES];  // MMA -> TMA: the MMAs reading the stage are done
     alignas(8) uint64_t acc_full[2];    // MMA -> epilogue: accumulator buffer holds a finished tile
@@ -232,15 +237,32 @@ __device__ __forceinline__ void gemm_fail(int *flag, unsigned *status)
     *(volatile int *)flag = 1;
 }
 
-__device__ __forceinline__ void ld_c4(const float *p, float &a, float &b, float &c, float &d)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
 {
-    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "l"(p));
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_c4(float *p, float a, float b, float c, float d)
+__device__ __forceinline__ void tma_store(const CUtensorMap *map, int x, int y, uint32_t src)
 {
-    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+
+// The calling thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The calling thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Output tile t -> (m0, n0): groups of kGroupM tile rows, M-fastest inside a
 // group, so the CTAs running at the same time share a compact block of A and
@@ -265,7 +287,7 @@ template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tf32_kernel(const __grid_constant__ CUtensorMap m_ahi, const __grid_constant__ CUtensorMap m_alo,
                      const __grid_constant__ CUtensorMap m_bhi, const __grid_constant__ CUtensorMap m_blo,
-                     const GemmArgs g)
+                     const __grid_constant__ CUtensorMap m_c, const GemmArgs g)
 {
     using Smem = GemmSmem<BN, BK, STAGES, THREE>;
     extern __shared__ __align__(1024) unsigned char raw[];
@@ -291,6 +313,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(su32(&s.acc_empty[i])));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.done)));
+        for (int i = 0; i < 4; ++i)
+            for (int j = 0; j < 2; ++j) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.cbar[i][j])));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.abort = 0;
     }
@@ -380,20 +404,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else {
         // ---------------- epilogue: TMEM rows -> alpha * acc + beta * C
-        const int eg = warp & 3;  // TMEM lane group this warp may access
+        const int eg = warp & 3;  // TMEM lane group this warp may access (rows 32 eg .. 32 eg + 31)
         const bool use_c = g.beta != 0.0f;
+        uint32_t cpar = 0;        // bit j: parity of the next completion of cbar[eg][j]
+        uint32_t loads_out = 0;   // bit j: a load into cbuf[eg][j] is in flight
         int t = 0;
         for (int tile = blockIdx.x; tile < g.ntiles; tile += gridDim.x, ++t) {
             const uint32_t ab = (uint32_t)t & 1u;
             int m0i, n0i;
             tile_coords(tile, g.tiles_m, tiles_n, BN, m0i, n0i);
             const int64_t m0 = m0i, n0 = n0i;
-            const int64_t row = m0 + eg * 32 + lane;
+            const int64_t row0 = m0 + eg * 32, row = row0 + lane;
+            const bool rows_in = ALIGNED || row0 < g.M;  // warp-uniform: any row of this warp inside C
             const bool row_in = ALIGNED || row < g.M;
             float *crow = g.C + row * g.ldc + n0;
             const int ncols = ALIGNED ? BN : (int)(g.N - n0 < BN ? g.N - n0 : BN);
-            if (use_c && row_in) {  // C arrives in L2 while this tile's MMAs run
-                for (int c = 0; c < ncols; c += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + c));
+            const bool tma_path = g.vec_c && rows_in;
+            const int nchunks = (ncols + 31) / 32;
+            // C of chunks 0 and 1 heads for this warp's staging buffers (both
+            // free: the last tile ended with its stores' reads complete), the
+            // rest into L2, while this tile's MMAs run
+            if (use_c && tma_path && lane == 0) {
+                for (int ci = 0; ci < 2 && ci < nchunks; ++ci) {
+                    const uint32_t bar = su32(&s.cbar[eg][ci]);
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 4096;" ::"r"(bar) : "memory");
+                    tma_load(su32(s.cbuf[eg][ci]), &m_c, (int)n0 + 32 * ci, (int)row0, bar);
+                    loads_out |= 1u << ci;
+                }
+            }
+            if (use_c && row_in) {
+                for (int c = tma_path ? 64 : 0; c < ncols; c += 32)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + c));
             }
             if (!acc_wait(su32(&s.acc_full[ab]), ((uint32_t)t / 2) & 1u, g.KT, &s.abort) || gemm_aborted(&s.abort)) {
                 if (!gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
@@ -401,36 +442,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t tbase = tmem + ((uint32_t)(eg * 32) << 16) + ab * BN;
-            for (int c = 0; c < ncols; c += 32) {  // warp-uniform: the load below is .sync.aligned
-                uint32_t r[32];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                    "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                    : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                      "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                      "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-                      "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-                      "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                    : "r"(tbase + (uint32_t)c));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (!row_in) continue;
-                float *p = crow + c;
-                if (g.vec_c && (ALIGNED || c + 32 <= ncols)) {
+            bool ok = true;
+            if (tma_path) {
+                // TMA path: C moves in 32 x 32 chunks through this warp's two
+                // staging buffers; TMA clips rows >= M and columns >= N on the
+                // store and reads them as 0 on the load.
+                for (int ci = 0; ci < nchunks; ++ci) {
+                    const int bsel = ci & 1;
+                    if (ci >= 1 && lane == 0) {
+                        bulk_wait_read();  // chunk ci-1's store has read its buffer (and ci-2's, this one)
+                        if (use_c && ci + 1 < nchunks) {
+                            const uint32_t bar = su32(&s.cbar[eg][bsel ^ 1]);
+                            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 4096;" ::"r"(bar)
+                                         : "memory");
+                            tma_load(su32(s.cbuf[eg][bsel ^ 1]), &m_c, (int)n0 + 32 * (ci + 1), (int)row0, bar);
+                            loads_out |= 1u << (bsel ^ 1);
+                        }
+                    }
+                    uint32_t r[32];
+                    tmem_ld32(tbase + (uint32_t)(32 * ci), r);
+                    if (use_c) {
+                        if (!mbar_wait(su32(&s.cbar[eg][bsel]), (cpar >> bsel) & 1u)) {
+                            gemm_fail(&s.abort, g.status);
+                            ok = false;
+                            break;
+                        }
+                        cpar ^= 1u << bsel;
+                        loads_out &= ~(1u << bsel);
+                    }
+                    __syncwarp();
+                    float *rowp = s.cbuf[eg][bsel] + lane * 32;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        float v0 = g.alpha * as_f(r[4 * q]), v1 = g.alpha * as_f(r[4 * q + 1]);
-                        float v2 = g.alpha * as_f(r[4 * q + 2]), v3 = g.alpha * as_f(r[4 * q + 3]);
+                        float4 *slot = reinterpret_cast<float4 *>(rowp + 4 * (q ^ (lane & 7)));
+                        float4 v;
+                        v.x = g.alpha * as_f(r[4 * q]);
+                        v.y = g.alpha * as_f(r[4 * q + 1]);
+                        v.z = g.alpha * as_f(r[4 * q + 2]);
+                        v.w = g.alpha * as_f(r[4 * q + 3]);
                         if (use_c) {
-                            float c0, c1, c2, c3;
-                            ld_c4(p + 4 * q, c0, c1, c2, c3);
-                            v0 = __fmaf_rn(g.beta, c0, v0);
-                            v1 = __fmaf_rn(g.beta, c1, v1);
-                            v2 = __fmaf_rn(g.beta, c2, v2);
-                            v3 = __fmaf_rn(g.beta, c3, v3);
+                            const float4 cv = *slot;
+                            v.x = __fmaf_rn(g.beta, cv.x, v.x);
+                            v.y = __fmaf_rn(g.beta, cv.y, v.y);
+                            v.z = __fmaf_rn(g.beta, cv.z, v.z);
+                            v.w = __fmaf_rn(g.beta, cv.w, v.w);
                         }
-                        st_c4(p + 4 * q, v0, v1, v2, v3);
+                        *slot = v;
                     }
-                } else {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA store
+                    __syncwarp();
+                    if (lane == 0) tma_store(&m_c, (int)n0 + 32 * ci, (int)row0, su32(s.cbuf[eg][bsel]));
+                }
+                if (lane == 0) bulk_wait_read();  // both buffers free for the next tile
+                __syncwarp();
+            } else if (rows_in) {
+                // direct path (C not 16-byte aligned or ldc % 4 != 0): one row per lane
+                for (int c = 0; c < ncols; c += 32) {  // warp-uniform: the TMEM load is .sync.aligned
+                    uint32_t r[32];
+                    tmem_ld32(tbase + (uint32_t)c, r);
+                    if (!row_in) continue;
+                    float *p = crow + c;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         if (c + e < ncols) {
@@ -443,7 +514,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&s.acc_empty[ab])) : "memory");
+            if (!ok) break;
         }
+        if (lane == 0) {
+            bulk_wait_all();  // stores complete before the CTA (and its shared memory) goes away
+            for (int j = 0; j < 2; ++j)  // a load still in flight after an abort lands first
+                if (loads_out & (1u << j)) mbar_wait(su32(&s.cbar[eg][j]), (cpar >> j) & 1u);
+        }
+        __syncwarp();
     }
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -526,7 +604,7 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
     if (!attr_ok) return TM_ERR_CUDA;
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<CUtensorMap *>(&maps[3]),
-                    const_cast<GemmArgs *>(&g)};
+                    const_cast<CUtensorMap *>(&maps[4]), const_cast<GemmArgs *>(&g)};
     return launch_dependent(k, dim3(grid), dim3(kGemmThreads), args, smem, s);
 }
 
@@ -636,10 +714,26 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     if ((st = launch_status()) != TM_OK) return st;
 
     // 2. the tensor-core gemm over whole tiles
-    CUtensorMap maps[4];
+    CUtensorMap maps[5] = {};
     if (!kmajor_map(&maps[0], ahi, pl.Mp, pl.Kp, GBM, TK) || !kmajor_map(&maps[1], alo, pl.Mp, pl.Kp, GBM, TK) ||
         !kmajor_map(&maps[2], bhi, pl.Np, pl.Kp, TN, TK) || !kmajor_map(&maps[3], blo, pl.Np, pl.Kp, TN, TK))
         return TM_ERR_CUDA;
+    // C as 32 x 32 TMA chunks (the epilogue's staging unit), when its rows
+    // start on 16-byte boundaries and N % 4 == 0: a TMA store clips the inner
+    // dimension only at 16-byte granularity (measured: with N = 1 it wrote
+    // columns 1-3 of the row's padding), so a row end inside a 16-byte piece
+    // would be overrun.  Otherwise the epilogue writes C directly.
+    const bool vec_c = aligned_to(C, 16) && ldc % 4 == 0 && N % 4 == 0;
+    if (vec_c) {
+        const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)ldc * sizeof(float)};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t es[2] = {1, 1};
+        if (gemm_encode_fn()(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, es,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TM_ERR_CUDA;
+    }
     GemmArgs g;
     g.C = C;
     g.ldc = ldc;
@@ -650,7 +744,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     g.KT = (int)(pl.Kp / TK);
     g.tiles_m = (int)(pl.Mp / GBM);
     g.ntiles = (int)((pl.Mp / GBM) * (pl.Np / TN));
-    g.vec_c = aligned_to(C, 16) && ldc % 4 == 0;
+    g.vec_c = vec_c;
     g.status = dev->status;
     const bool aligned = (flags & TM_ALIGNED) != 0;
     const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);  // persistent: one CTA per SM

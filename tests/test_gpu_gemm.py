@@ -66,16 +66,24 @@ def bound(a, b, c, alpha, beta, want, three=True):
 
 
 SHAPES = [(1, 1, 1), (1, 5, 3), (7, 9, 13), (128, 256, 32), (128, 128, 64), (130, 200, 1000), (257, 300, 33),
-          (300, 513, 95), (64, 1000, 1000), (1000, 36, 8)]
+          (300, 513, 95), (64, 1000, 1000), (1000, 36, 8), (4, 4, 4), (129, 132, 40)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("TN", [128, 256])
 @pytest.mark.parametrize("TK", [16, 32])
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
-def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags):
+@pytest.mark.parametrize("c_rows", ["tma", "direct"])
+def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags, c_rows):
+    # c_rows: ldc a multiple of 4 (C moves through TMA chunks when N % 4 == 0,
+    # the edges clipped by the copy engine; direct stores otherwise, with the
+    # ld gap right after a row end that is not 16-byte aligned) or ldc not a
+    # multiple of 4 (direct stores)
+    ldc = (N + 3) // 4 * 4 + 4 if c_rows == "tma" else N + 2
+    if c_rows == "direct" and ldc % 4 == 0:
+        ldc += 1
     a, b, c = ints((M, K), 11 + M), ints((K, N), 12 + N), ints((M, N), 13 + K)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, lda=K + 3, ldb=N + 1, ldc=N + 2, TK=TK)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, lda=K + 3, ldb=N + 1, ldc=ldc, TK=TK)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, 0.5)
     got = out.reshape(M, ldc)[:, :N]
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
@@ -137,12 +145,13 @@ def test_gemm_degenerate(cuda, oracle):
     c = ints((70, 90), 51)
     out, *_ = run(np.zeros((70, 0), np.float32), np.zeros((0, 90), np.float32), c, 1.5, 0.5, lda=1, ldb=90)
     assert np.array_equal(out.reshape(70, 90), 0.5 * c)
-    # beta == 0 never reads C: NaN in C does not reach the result
+    # beta == 0 never reads C: NaN in C does not reach the result (direct and TMA epilogues)
     a, b = ints((40, 20), 52), ints((20, 30), 53)
     cn = np.full((40, 30), np.nan, np.float32)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, cn, 1.0, 0.0)
-    want = oracle.gemm_rows(Ah, lda, Bh, ldb, None, 0, np.arange(40), 30, 20, 1.0, 0.0)
-    assert np.array_equal(out.reshape(40, 30), want)
+    for ldc in (30, 36):
+        out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, cn, 1.0, 0.0, ldc=ldc)
+        want = oracle.gemm_rows(Ah, lda, Bh, ldb, None, 0, np.arange(40), 30, 20, 1.0, 0.0)
+        assert np.array_equal(out.reshape(40, ldc)[:, :30], want)
     # empty M or N: nothing launched, nothing written
     CD = DevBuf.empty(16)
     raw, ws, wsb = workspace(1, 1, 4, 256)
