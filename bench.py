@@ -638,12 +638,13 @@ def run_gemm_case(name, args, dev, stream, flush):
     C0 = torch.from_numpy(c).to(dev)
     C = C0.clone()
     parts = [int(t) for t in args.tile.split("x")] if args.tile else []
+    TM_ = parts[0] if parts else w["TM"]
     TN_ = parts[1] if len(parts) > 1 else w["TN"]
     TK_ = parts[2] if len(parts) > 2 else w["TK"]
     wsb = tm.tm_gemm_workspace_bytes(M, N, K, TN_)
     raw = torch.empty(wsb + 1024, dtype=torch.uint8, device=dev)
     ws = (raw.data_ptr() + 1023) // 1024 * 1024
-    aligned = M % 128 == 0 and N % TN_ == 0 and K % TK_ == 0
+    aligned = M % TM_ == 0 and N % TN_ == 0 and K % TK_ == 0
     peak, peak_src = tf32_peak()
     s = stream.cuda_stream
     out = []
@@ -657,7 +658,7 @@ def run_gemm_case(name, args, dev, stream, flush):
                 flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            tm.tm_gemm(A, K, B, N, C, N, M, N, K, w["alpha"], w["beta"], ws, wsb, 128, TN_, TK_, fl, s)
+            tm.tm_gemm(A, K, B, N, C, N, M, N, K, w["alpha"], w["beta"], ws, wsb, TM_, TN_, TK_, fl, s)
             e1.record(stream)
             torch.cuda.synchronize(dev)
             if rep >= 3:
@@ -665,7 +666,7 @@ def run_gemm_case(name, args, dev, stream, flush):
         t = statistics.median(ts)
         flops = 2.0 * M * N * K
         passes = 3 if v == "3xtf32" else 1
-        row = {"case": name, "kernel": "gemm", "variant": v, "tile": "128x%dx%d" % (TN_, TK_), "M": M, "N": N, "K": K,
+        row = {"case": name, "kernel": "gemm", "variant": v, "tile": "%dx%dx%d" % (TM_, TN_, TK_), "M": M, "N": N, "K": K,
                "us": round(t * 1e6, 2), "TFLOPs": round(flops / t / 1e12, 2),
                "tensor_TFLOPs": round(passes * flops / t / 1e12, 2),
                "frac_of_tf32_peak": round(passes * flops / t / 1e12 / peak, 4), "tf32_peak": round(peak, 1),

@@ -325,11 +325,17 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
  * K == 0 gives C = beta * C.
  *   A, lda   device input [M, lda]    B, ldb   device input [K, ldb]
  *   C, ldc   device in/out [M, ldc]; C must not overlap A, B or the workspace
- *   TM, TN, TK   the output tile and K tile: TM = 128, TN = 128 or 256, TK = 16
- *            or 32 (the K width of one pipeline stage: TK 16 gives twice as
- *            many, half-size stages in the same shared memory)
+ *   TM, TN, TK   the output tile and K tile: TM = 128 (one CTA per tile) or
+ *            256 (a pair of CTAs on neighbouring SMs shares each tile: each
+ *            stages 128 rows of A and half of the B tile, cutting operand
+ *            traffic per flop by a third), TN = 128 or 256, TK = 16 or 32 (the
+ *            K width of one pipeline stage: TK 16 gives twice as many,
+ *            half-size stages in the same shared memory)
  *   flags    TM_ALIGNED (M % TM == 0, N % TN == 0, K % TK == 0: the output
  *            tiles store without masks), TM_GEMM_TF32
+ *   The output moves through TMA copies when C is 16-byte aligned and
+ *   ldc % 4 == 0 and N % 4 == 0, else by direct stores; either way nothing
+ *   outside [M, N] (the ld gap included) is written.
  *   workspace, ws_bytes   device scratch of at least
  *            tm_gemm_workspace_bytes(M, N, K, TN) bytes, 1024-byte aligned,
  *            overlapping no operand; contents on entry do not matter.

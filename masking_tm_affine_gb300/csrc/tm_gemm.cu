@@ -143,18 +143,96 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N)
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// tcgen05 operations of one CTA (PAIR = false) or of a CTA pair (PAIR = true:
+// cta_group::2, issued by the even CTA of a 2-CTA cluster; A is split by rows
+// between the two CTAs' shared memory, B by its N rows, and each CTA's TMEM
+// holds its 128 rows of the 256-row accumulator).  A kernel uses one group
+// throughout.
+template <bool PAIR>
 __device__ __forceinline__ void umma_tf32(uint32_t tmem, uint64_t da, uint64_t db, uint32_t id, uint32_t acc)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-        "l"(da), "l"(db), "r"(id), "r"(acc)
-        : "memory");
+    if constexpr (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+            "l"(da), "l"(db), "r"(id), "r"(acc)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+            "l"(da), "l"(db), "r"(id), "r"(acc)
+            : "memory");
 }
 
+// Arrive on `bar` (same offset in both CTAs of a pair) once every MMA issued
+// so far by this thread has completed.
+template <bool PAIR>
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+    if constexpr (PAIR)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                bar),
+            "h"((uint16_t)3)
+            : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t cols)
+{
+    if constexpr (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols)
+{
+    if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on the
+// even CTA's barrier `bar` (a cluster address): a pair's operand copies.
+__device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
@@ -269,40 +347,43 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // B tiles in L2 (the page's pm = block.x, pn = block.y order within a group).
 constexpr int kGroupM = 16;
 
-__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int BN, int &m0, int &n0)
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int BM, int BN, int &m0, int &n0)
 {
     const int64_t per_group = (int64_t)kGroupM * tiles_n;
     const int group = (int)(tile / per_group);
     const int first = group * kGroupM;
     const int gm = tiles_m - first < kGroupM ? tiles_m - first : kGroupM;
     const int local = (int)(tile - group * per_group);
-    m0 = (first + local % gm) * GBM;
+    m0 = (first + local % gm) * BM;
     n0 = (local / gm) * BN;
 }
 
-// One CTA per SM, persistent over the output tiles in tile_coords order.  The
-// accumulator is double-buffered in TMEM (2 x BN columns): the epilogue of one
-// tile runs while the MMAs of the next accumulate into the other buffer.
-template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED>
+// Persistent over the output tiles in tile_coords order: one CTA per SM
+// (PAIR = false, 128-row tiles) or one 2-CTA cluster per SM pair (PAIR = true,
+// 256-row tiles: each CTA stages its 128 rows of A and half of B's BN rows, so
+// a pair moves a third fewer operand bytes per flop than two single CTAs).
+// The accumulator is double-buffered in TMEM (2 x BN columns): the epilogue of
+// one tile runs while the MMAs of the next accumulate into the other buffer.
+template <int BN, int BK, int STAGES, bool THREE, bool ALIGNED, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tf32_kernel(const __grid_constant__ CUtensorMap m_ahi, const __grid_constant__ CUtensorMap m_alo,
                      const __grid_constant__ CUtensorMap m_bhi, const __grid_constant__ CUtensorMap m_blo,
                      const __grid_constant__ CUtensorMap m_c, const GemmArgs g)
 {
-    using Smem = GemmSmem<BN, BK, STAGES, THREE>;
+    constexpr int BH = PAIR ? BN / 2 : BN;   // B rows staged per CTA
+    constexpr int TMR = PAIR ? 2 * GBM : GBM;  // output tile rows
+    using Smem = GemmSmem<BH, BK, STAGES, THREE>;
     extern __shared__ __align__(1024) unsigned char raw[];
     Smem &s = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_n = g.ntiles / g.tiles_m;
-    constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BN) * BK * sizeof(float));
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;  // 0: this CTA issues the MMAs
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BH) * BK * sizeof(float));  // per CTA
     constexpr uint32_t kCols = 2 * BN;  // TMEM columns: two accumulator buffers
 
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s.tmem)),
-                     "r"(kCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc<PAIR>(su32(&s.tmem), kCols);
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.full[i])));
@@ -310,7 +391,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.acc_full[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(su32(&s.acc_empty[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&s.acc_empty[i])),
+                         "r"(PAIR ? 256 : 128));
         }
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.done)));
         for (int i = 0; i < 4; ++i)
@@ -320,18 +402,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote signal
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s.tmem;
     pdl_wait();  // launched as a dependent of the split pass: its operands first
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer: the four operand tiles of every K stage
+            // ---------------- TMA producer: this CTA's operand tiles of every K stage
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < g.ntiles && ok; tile += gridDim.x) {
+            for (int tile = unit; tile < g.ntiles && ok; tile += units) {
                 int m0, n0;
-                tile_coords(tile, g.tiles_m, tiles_n, BN, m0, n0);
+                tile_coords(tile, g.tiles_m, tiles_n, TMR, BN, m0, n0);
+                const int am = m0 + (int)rank * GBM, bn = n0 + (int)rank * BH;
                 for (int kt = 0; kt < g.KT; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
                     if (it >= STAGES && !mbar_wait(su32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
@@ -343,32 +427,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = su32(&s.full[st]);
-                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                                 "r"(kStageBytes)
-                                 : "memory");
                     const int kx = kt * BK;
-                    tma_load(su32(s.st[st].a_hi), &m_ahi, kx, m0, bar);
-                    tma_load(su32(s.st[st].b_hi), &m_bhi, kx, n0, bar);
-                    if (THREE) {
-                        tma_load(su32(s.st[st].a_lo), &m_alo, kx, m0, bar);
-                        tma_load(su32(s.st[st].b_lo), &m_blo, kx, n0, bar);
+                    if constexpr (PAIR) {
+                        // the even CTA's barrier counts both CTAs' bytes
+                        if (rank == 0)
+                            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                                             su32(&s.full[st])),
+                                         "r"(2 * kStageBytes)
+                                         : "memory");
+                        const uint32_t bar = cluster_addr(su32(&s.full[st]), 0);
+                        tma_load_pair(su32(s.st[st].a_hi), &m_ahi, kx, am, bar);
+                        tma_load_pair(su32(s.st[st].b_hi), &m_bhi, kx, bn, bar);
+                        if (THREE) {
+                            tma_load_pair(su32(s.st[st].a_lo), &m_alo, kx, am, bar);
+                            tma_load_pair(su32(s.st[st].b_lo), &m_blo, kx, bn, bar);
+                        }
+                    } else {
+                        const uint32_t bar = su32(&s.full[st]);
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                                     "r"(kStageBytes)
+                                     : "memory");
+                        tma_load(su32(s.st[st].a_hi), &m_ahi, kx, am, bar);
+                        tma_load(su32(s.st[st].b_hi), &m_bhi, kx, bn, bar);
+                        if (THREE) {
+                            tma_load(su32(s.st[st].a_lo), &m_alo, kx, am, bar);
+                            tma_load(su32(s.st[st].b_lo), &m_blo, kx, bn, bar);
+                        }
                     }
                 }
             }
-            if (!ok) {  // nothing may still be landing in shared memory when the CTA leaves
-                for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                    mbar_wait(su32(&s.full[j % STAGES]), (j / STAGES) & 1u);
+            // Nothing may still be landing in shared memory when the CTA (or
+            // its pair) leaves: the barriers this CTA armed see every byte.
+            // After a normal run they have all completed already.
+            if (!ok || PAIR) {
+                if (rank == 0)
+                    for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                        mbar_wait(su32(&s.full[j % STAGES]), (j / STAGES) & 1u);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer: 3 (or 1) tf32 MMAs per 8-wide K step
-            constexpr uint32_t id = idesc_tf32(GBM, BN);
+            constexpr uint32_t id = idesc_tf32(TMR, BN);
             uint32_t it = 0;
             bool ok = true;
             int t = 0;
-            for (int tile = blockIdx.x; tile < g.ntiles && ok; tile += gridDim.x, ++t) {
+            for (int tile = unit; tile < g.ntiles && ok; tile += units, ++t) {
                 const uint32_t ab = (uint32_t)t & 1u;
                 if (t >= 2 && !mbar_wait(su32(&s.acc_empty[ab]), ((uint32_t)(t / 2) - 1) & 1u)) {
                     gemm_fail(&s.abort, g.status);
@@ -389,31 +493,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 8; ++k) {
                         const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
-                        umma_tf32(d, smem_desc<BK>(ahi + off), smem_desc<BK>(bhi + off), id, (kt | k) != 0);
+                        umma_tf32<PAIR>(d, smem_desc<BK>(ahi + off), smem_desc<BK>(bhi + off), id, (kt | k) != 0);
                         if (THREE) {
-                            umma_tf32(d, smem_desc<BK>(ahi + off), smem_desc<BK>(blo + off), id, 1u);
-                            umma_tf32(d, smem_desc<BK>(alo + off), smem_desc<BK>(bhi + off), id, 1u);
+                            umma_tf32<PAIR>(d, smem_desc<BK>(ahi + off), smem_desc<BK>(blo + off), id, 1u);
+                            umma_tf32<PAIR>(d, smem_desc<BK>(alo + off), smem_desc<BK>(bhi + off), id, 1u);
                         }
                     }
-                    umma_commit(su32(&s.empty[st]));  // the stage is free once these MMAs are done
+                    umma_commit<PAIR>(su32(&s.empty[st]));  // the stage (in both CTAs) is free once these are done
                 }
-                if (ok) umma_commit(su32(&s.acc_full[ab]));
+                if (ok) umma_commit<PAIR>(su32(&s.acc_full[ab]));
             }
-            umma_commit(su32(&s.done));  // tracks every MMA issued, also after an abort
+            umma_commit<PAIR>(su32(&s.done));  // tracks every MMA issued, also after an abort
             if (!mbar_wait(su32(&s.done), 0u)) gemm_fail(&s.abort, g.status);
         }
     } else {
         // ---------------- epilogue: TMEM rows -> alpha * acc + beta * C
         const int eg = warp & 3;  // TMEM lane group this warp may access (rows 32 eg .. 32 eg + 31)
         const bool use_c = g.beta != 0.0f;
+        // the MMA issuer's "accumulator free" barrier (in the even CTA of a pair)
+        const uint32_t acc_empty0 = PAIR ? cluster_addr(su32(&s.acc_empty[0]), 0) : su32(&s.acc_empty[0]);
+        const uint32_t acc_empty1 = PAIR ? cluster_addr(su32(&s.acc_empty[1]), 0) : su32(&s.acc_empty[1]);
         uint32_t cpar = 0;        // bit j: parity of the next completion of cbar[eg][j]
         uint32_t loads_out = 0;   // bit j: a load into cbuf[eg][j] is in flight
         int t = 0;
-        for (int tile = blockIdx.x; tile < g.ntiles; tile += gridDim.x, ++t) {
+        for (int tile = unit; tile < g.ntiles; tile += units, ++t) {
             const uint32_t ab = (uint32_t)t & 1u;
             int m0i, n0i;
-            tile_coords(tile, g.tiles_m, tiles_n, BN, m0i, n0i);
-            const int64_t m0 = m0i, n0 = n0i;
+            tile_coords(tile, g.tiles_m, tiles_n, TMR, BN, m0i, n0i);
+            const int64_t m0 = m0i + (int64_t)rank * GBM, n0 = n0i;  // this CTA's 128 rows
             const int64_t row0 = m0 + eg * 32, row = row0 + lane;
             const bool rows_in = ALIGNED || row0 < g.M;  // warp-uniform: any row of this warp inside C
             const bool row_in = ALIGNED || row < g.M;
@@ -513,7 +620,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&s.acc_empty[ab])) : "memory");
+            const uint32_t freed = ab ? acc_empty1 : acc_empty0;
+            if constexpr (PAIR)
+                asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(freed) : "memory");
+            else
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(freed) : "memory");
             if (!ok) break;
         }
         if (lane == 0) {
@@ -526,10 +637,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the pair's MMAs, copies and remote arrivals are over
     if (warp == 1) {
         __syncwarp();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+        tmem_dealloc<PAIR>(tmem, kCols);
     }
 }
 
@@ -571,7 +683,7 @@ struct GemmPlan {
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
 {
     GemmPlan p;
-    p.Mp = (M + GBM - 1) / GBM * GBM;
+    p.Mp = (M + 2 * GBM - 1) / (2 * GBM) * (2 * GBM);  // whole 256-row tiles: either TM fits
     p.Np = (N + TN - 1) / TN * TN;
     p.Kp = K > 0 ? (K + GBK - 1) / GBK * GBK : GBK;  // K = 0: one zero tile, acc = 0
     const size_t a = (size_t)(p.Mp * p.Kp) * sizeof(float), b = (size_t)(p.Np * p.Kp) * sizeof(float);
@@ -584,13 +696,14 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
     return p;
 }
 
-template <int BN, int BK, bool THREE, bool ALIGNED>
+template <int BN, int BK, bool THREE, bool ALIGNED, bool PAIR>
 tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid, cudaStream_t s)
 {
-    constexpr int STAGES = gemm_stages<BN, BK, THREE>();
+    constexpr int BH = PAIR ? BN / 2 : BN;
+    constexpr int STAGES = gemm_stages<BH, BK, THREE>();
     static_assert(STAGES >= 2, "shared-memory ring needs two stages");
-    const void *k = (const void *)gemm_tf32_kernel<BN, BK, STAGES, THREE, ALIGNED>;
-    const size_t smem = sizeof(GemmSmem<BN, BK, STAGES, THREE>) + 1024;
+    const void *k = (const void *)gemm_tf32_kernel<BN, BK, STAGES, THREE, ALIGNED, PAIR>;
+    const size_t smem = sizeof(GemmSmem<BH, BK, STAGES, THREE>) + 1024;
     static std::once_flag once[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -605,21 +718,52 @@ tm_status launch_gemm(const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
     void *args[] = {const_cast<CUtensorMap *>(&maps[0]), const_cast<CUtensorMap *>(&maps[1]),
                     const_cast<CUtensorMap *>(&maps[2]), const_cast<CUtensorMap *>(&maps[3]),
                     const_cast<CUtensorMap *>(&maps[4]), const_cast<GemmArgs *>(&g)};
-    return launch_dependent(k, dim3(grid), dim3(kGemmThreads), args, smem, s);
+    // a programmatic dependent of the split pass; CTA pairs as 2-CTA clusters
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 2 : 1;
+    if (cudaLaunchKernelExC(&cfg, k, args) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
 }
 
 // Stages fill about 192 KB of shared memory: 3xTF32 stages hold hi and lo of
-// both operands (96 KB at TN 256 and TK 32, 48 KB at TK 16, ...), single-pass
-// stages only hi, so that mode runs twice as many.
-template <int BN, int BK>
+// both operands (96 KB at TN 256 and TK 32, 48 KB at TK 16, ...; a pair's CTA
+// holds half of B), single-pass stages only hi, so that mode runs twice as many.
+template <int BN, int BK, bool PAIR>
 tm_status launch_gemm_cfg(bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g, unsigned grid,
                           cudaStream_t s)
 {
     if (three)
-        return aligned ? launch_gemm<BN, BK, true, true>(maps, g, grid, s)
-                       : launch_gemm<BN, BK, true, false>(maps, g, grid, s);
-    return aligned ? launch_gemm<BN, BK, false, true>(maps, g, grid, s)
-                   : launch_gemm<BN, BK, false, false>(maps, g, grid, s);
+        return aligned ? launch_gemm<BN, BK, true, true, PAIR>(maps, g, grid, s)
+                       : launch_gemm<BN, BK, true, false, PAIR>(maps, g, grid, s);
+    return aligned ? launch_gemm<BN, BK, false, true, PAIR>(maps, g, grid, s)
+                   : launch_gemm<BN, BK, false, false, PAIR>(maps, g, grid, s);
+}
+
+template <bool PAIR>
+tm_status launch_gemm_tiles(int TN, int TK, bool three, bool aligned, const CUtensorMap *maps, const GemmArgs &g,
+                            unsigned grid, cudaStream_t s)
+{
+    if (TK == 32) {
+        if (TN == 128) return launch_gemm_cfg<128, 32, PAIR>(three, aligned, maps, g, grid, s);
+        return launch_gemm_cfg<256, 32, PAIR>(three, aligned, maps, g, grid, s);
+    }
+    if (TN == 128) return launch_gemm_cfg<128, 16, PAIR>(three, aligned, maps, g, grid, s);
+    return launch_gemm_cfg<256, 16, PAIR>(three, aligned, maps, g, grid, s);
 }
 
 bool disjoint_bytes(const void *a, size_t na, const void *b, size_t nb)
@@ -645,7 +789,8 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
 {
     if (M < 0 || N < 0 || K < 0) return TM_ERR_INVALID_ARG;
     if (!flags_ok(flags, TM_ALIGNED | TM_GEMM_TF32)) return TM_ERR_INVALID_ARG;
-    if (TM != GBM || !(TK == 16 || TK == 32) || !(TN == 128 || TN == 256)) return TM_ERR_UNSUPPORTED_TILE;
+    if (!(TM == GBM || TM == 2 * GBM) || !(TK == 16 || TK == 32) || !(TN == 128 || TN == 256))
+        return TM_ERR_UNSUPPORTED_TILE;
     if (!valid2d(C, ldc, M, N) || !valid2d(A, lda, M, K) || !valid2d(B, ldb, K, N)) return TM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return TM_OK;
     if (!aligned_to(C, 4) || (K > 0 && (!aligned_to(A, 4) || !aligned_to(B, 4)))) return TM_ERR_MISALIGNED;
@@ -653,7 +798,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
         if (M % TM != 0 || N % TN != 0 || K % TK != 0) return TM_ERR_BROKEN_PROMISE;
     }
     const GemmPlan pl = gemm_plan(M, N, K, TN);
-    if (pl.Mp > INT32_MAX || pl.Np > INT32_MAX || pl.Kp > INT32_MAX || (pl.Mp / GBM) * (pl.Np / TN) > INT32_MAX)
+    if (pl.Mp > INT32_MAX || pl.Np > INT32_MAX || pl.Kp > INT32_MAX || (pl.Mp / TM) * (pl.Np / TN) > INT32_MAX)
         return TM_ERR_INVALID_ARG;
     if (workspace == nullptr || ws_bytes < pl.bytes || !aligned_to(workspace, 1024)) return TM_ERR_WORKSPACE;
     {
@@ -715,8 +860,10 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
 
     // 2. the tensor-core gemm over whole tiles
     CUtensorMap maps[5] = {};
+    // each CTA copies 128 rows of A and its TN (one CTA) or TN / 2 (a pair) rows of B per stage
+    const int b_rows = TM == 2 * GBM ? TN / 2 : TN;
     if (!kmajor_map(&maps[0], ahi, pl.Mp, pl.Kp, GBM, TK) || !kmajor_map(&maps[1], alo, pl.Mp, pl.Kp, GBM, TK) ||
-        !kmajor_map(&maps[2], bhi, pl.Np, pl.Kp, TN, TK) || !kmajor_map(&maps[3], blo, pl.Np, pl.Kp, TN, TK))
+        !kmajor_map(&maps[2], bhi, pl.Np, pl.Kp, b_rows, TK) || !kmajor_map(&maps[3], blo, pl.Np, pl.Kp, b_rows, TK))
         return TM_ERR_CUDA;
     // C as 32 x 32 TMA chunks (the epilogue's staging unit), when its rows
     // start on 16-byte boundaries and N % 4 == 0: a TMA store clips the inner
@@ -742,16 +889,17 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     g.alpha = alpha;
     g.beta = beta;
     g.KT = (int)(pl.Kp / TK);
-    g.tiles_m = (int)(pl.Mp / GBM);
-    g.ntiles = (int)((pl.Mp / GBM) * (pl.Np / TN));
+    g.tiles_m = (int)(pl.Mp / TM);
+    g.ntiles = (int)((pl.Mp / TM) * (pl.Np / TN));
     g.vec_c = vec_c;
     g.status = dev->status;
     const bool aligned = (flags & TM_ALIGNED) != 0;
-    const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);  // persistent: one CTA per SM
-    if (TK == 32) {
-        if (TN == 128) return launch_gemm_cfg<128, 32>(three, aligned, maps, g, grid, s);
-        return launch_gemm_cfg<256, 32>(three, aligned, maps, g, grid, s);
+    // persistent: one CTA per SM, or one 2-CTA cluster per SM pair
+    if (TM == 2 * GBM) {
+        const int pairs = dev->sms / 2;
+        const unsigned grid = 2u * (unsigned)(g.ntiles < pairs ? g.ntiles : pairs);
+        return launch_gemm_tiles<true>(TN, TK, three, aligned, maps, g, grid, s);
     }
-    if (TN == 128) return launch_gemm_cfg<128, 16>(three, aligned, maps, g, grid, s);
-    return launch_gemm_cfg<256, 16>(three, aligned, maps, g, grid, s);
+    const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);
+    return launch_gemm_tiles<false>(TN, TK, three, aligned, maps, g, grid, s);
 }

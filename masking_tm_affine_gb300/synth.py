@@ -82,9 +82,9 @@ WORKLOADS = {
     # bounds and masking", "Loops over a dynamic extent" (ragged against TILE_K = 32),
     # M = N = 4100 like the ragged 2-D workload; and a square whole-tile case
     "gemm_4100": dict(kind="gemm", M=4100, N=4100, K=1000, seeds=(7, 8, 9), alpha=1.5, beta=0.5,
-                      TM=128, TN=256, TK=16),
+                      TM=256, TN=256, TK=32),
     "gemm_8192": dict(kind="gemm", M=8192, N=8192, K=8192, seeds=(10, 11, 12), alpha=1.5, beta=0.5,
-                      TM=128, TN=256, TK=16),
+                      TM=256, TN=256, TK=32),
 }
 
 

@@ -219,9 +219,10 @@ def tm_gemm_workspace_bytes(M: int, N: int, K: int, TN: int = 256) -> int:
 
 
 def tm_gemm(A, lda: int, B, ldb: int, C, ldc: int, M: int, N: int, K: int, alpha: float, beta: float,
-            workspace, ws_bytes: int, TM: int = 128, TN: int = 256, TK: int = 16, flags: int = 0,
+            workspace, ws_bytes: int, TM: int = 256, TN: int = 256, TK: int = 32, flags: int = 0,
             stream=None) -> None:
-    """C = alpha * (A B) + beta * C on the tensor cores (3xTF32 unless TM_GEMM_TF32)."""
+    """C = alpha * (A B) + beta * C on the tensor cores (3xTF32 unless TM_GEMM_TF32).
+    TM = 256 runs CTA pairs (the default, fastest); TM = 128 single CTAs."""
     _ok(load().tm_gemm(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, M, N, K, alpha, beta, TM, TN, TK, flags,
                        _ptr(workspace), ws_bytes, _stream(stream)), "tm_gemm")
 

@@ -147,9 +147,9 @@ def test_padding_helpers_match_oracle(lib, oracle):
 def test_gemm_host_validation(lib):
     W = 0x7F0200000000  # 1024-byte aligned fake workspace
     ws = tm.tm_gemm_workspace_bytes(4100, 4100, 1000, 256)
-    # operands zero-padded to whole tiles: [4224, 1024] hi + lo and [4352, 1024] hi + lo
-    assert ws == 2 * 4224 * 1024 * 4 + 2 * 4352 * 1024 * 4
-    assert tm.tm_gemm_workspace_bytes(4100, 4100, 0, 256) == 2 * 4224 * 32 * 4 + 2 * 4352 * 32 * 4
+    # operands zero-padded to whole tiles (rows of A to 256, either TM): [4352, 1024] hi + lo twice
+    assert ws == 2 * 4352 * 1024 * 4 + 2 * 4352 * 1024 * 4
+    assert tm.tm_gemm_workspace_bytes(4100, 4100, 0, 256) == 4 * 4352 * 32 * 4
     assert tm.tm_gemm_workspace_bytes(0, 4, 4, 256) == 0 and tm.tm_gemm_workspace_bytes(4, 4, 4, 64) == 0
 
     def g(A=P0, lda=1000, B=P1, ldb=4100, C=W + (1 << 34), ldc=4100, M=4100, N=4100, K=1000, TM=128, TN=256,
@@ -157,6 +157,9 @@ def test_gemm_host_validation(lib):
         return st("tm_gemm", A, lda, B, ldb, C, ldc, M, N, K, 1.5, 0.5, TM, TN, TK, flags, ws_ptr, ws_bytes, None)
 
     assert g(TM=64) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert g(TM=512) == tm.TM_ERR_UNSUPPORTED_TILE
+    assert g(M=4224, N=4096, K=1024, lda=1024, ldb=4096, ldc=4096, TM=256,
+             flags=tm.TM_ALIGNED) == tm.TM_ERR_BROKEN_PROMISE       # 4224 % 256 != 0
     assert g(TK=8) == tm.TM_ERR_UNSUPPORTED_TILE
     assert g(TK=64) == tm.TM_ERR_UNSUPPORTED_TILE
     assert g(TN=512) == tm.TM_ERR_UNSUPPORTED_TILE

@@ -34,7 +34,7 @@ def workspace(M, N, K, TN):
     return raw, (base + 1023) // 1024 * 1024, ws
 
 
-def run(a, b, c, alpha, beta, TN=256, flags=0, lda=None, ldb=None, ldc=None, TK=32):
+def run(a, b, c, alpha, beta, TN=256, flags=0, lda=None, ldb=None, ldc=None, TK=32, TM=128):
     """C <- alpha a b + beta c on the GPU; returns (the [M, ldc] result, the
     padded host inputs, and a guard check)."""
     M, K = a.shape
@@ -45,7 +45,7 @@ def run(a, b, c, alpha, beta, TN=256, flags=0, lda=None, ldb=None, ldc=None, TK=
     Ch = synth.pad_rows(c, ldc) if M and N else np.zeros(max(M * ldc, 1), np.float32)
     AD, BD, CD = DevBuf(Ah), DevBuf(Bh), DevBuf(Ch)
     raw, ws, wsb = workspace(max(M, 1), max(N, 1), K, TN)
-    tm.tm_gemm(AD.ptr, lda, BD.ptr, ldb, CD.ptr, ldc, M, N, K, alpha, beta, ws, wsb, 128, TN, TK, flags)
+    tm.tm_gemm(AD.ptr, lda, BD.ptr, ldb, CD.ptr, ldc, M, N, K, alpha, beta, ws, wsb, TM, TN, TK, flags)
     tm.tm_check()
     assert AD.guards_intact() and BD.guards_intact() and CD.guards_intact()
     out = CD.payload_f32()
@@ -74,7 +74,9 @@ SHAPES = [(1, 1, 1), (1, 5, 3), (7, 9, 13), (128, 256, 32), (128, 128, 64), (130
 @pytest.mark.parametrize("TK", [16, 32])
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
 @pytest.mark.parametrize("c_rows", ["tma", "direct"])
-def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags, c_rows):
+@pytest.mark.parametrize("TM", [128, 256])
+def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags, c_rows, TM):
+    # TM 256: CTA pairs (cta_group::2), each CTA holding half of every B tile
     # c_rows: ldc a multiple of 4 (C moves through TMA chunks when N % 4 == 0,
     # the edges clipped by the copy engine; direct stores otherwise, with the
     # ld gap right after a row end that is not 16-byte aligned) or ldc not a
@@ -83,7 +85,7 @@ def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags, c_rows):
     if c_rows == "direct" and ldc % 4 == 0:
         ldc += 1
     a, b, c = ints((M, K), 11 + M), ints((K, N), 12 + N), ints((M, N), 13 + K)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, lda=K + 3, ldb=N + 1, ldc=ldc, TK=TK)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, lda=K + 3, ldb=N + 1, ldc=ldc, TK=TK, TM=TM)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, 0.5)
     got = out.reshape(M, ldc)[:, :N]
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
@@ -92,17 +94,19 @@ def test_gemm_integers_exact(cuda, oracle, M, N, K, TN, TK, flags, c_rows):
 @pytest.mark.parametrize("M,N,K", [(128, 256, 32), (256, 512, 1024), (384, 128, 96), (2048, 1024, 48)])
 @pytest.mark.parametrize("TN", [128, 256])
 @pytest.mark.parametrize("TK", [16, 32])
-def test_gemm_aligned_promise_exact(cuda, oracle, M, N, K, TN, TK):
-    if N % TN or K % TK:
-        pytest.skip("N not a multiple of TN or K not a multiple of TK")
+@pytest.mark.parametrize("TM", [128, 256])
+def test_gemm_aligned_promise_exact(cuda, oracle, M, N, K, TN, TK, TM):
+    if N % TN or K % TK or M % TM:
+        pytest.skip("extents not whole tiles")
     a, b, c = ints((M, K), 21), ints((K, N), 22), ints((M, N), 23)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, -1.0, 2.0, TN, tm.TM_ALIGNED, TK=TK)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, -1.0, 2.0, TN, tm.TM_ALIGNED, TK=TK, TM=TM)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, -1.0, 2.0)
     assert np.array_equal(out.reshape(M, N).view(np.uint32), want.view(np.uint32))
 
 
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
-def test_gemm_single_product_split_accuracy(cuda, oracle, flags):
+@pytest.mark.parametrize("TM", [128, 256])
+def test_gemm_single_product_split_accuracy(cuda, oracle, flags, TM):
     # B holds one nonzero per column: C[i, j] = alpha * A[i, k_j] * B[k_j, j]
     M, N, K = 200, 300, 77
     a = synth.uniform((M, K), -1.0, 1.0, 31)
@@ -111,7 +115,7 @@ def test_gemm_single_product_split_accuracy(cuda, oracle, flags):
     b = np.zeros((K, N), np.float32)
     b[kj, np.arange(N)] = vals
     c = np.zeros((M, N), np.float32)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.0, 0.0, 256, flags)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.0, 0.0, 256, flags, TM=TM)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.0, 0.0)
     got = out.reshape(M, N).astype(np.float64)
     rel = np.abs(got - want) / np.maximum(np.abs(want.astype(np.float64)), 1e-30)
@@ -128,12 +132,12 @@ def test_gemm_single_product_split_accuracy(cuda, oracle, flags):
 @pytest.mark.parametrize("M,N,K", [(130, 200, 1000), (257, 300, 33), (1, 1000, 4099), (500, 37, 1),
                                    (2100, 700, 260)])
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
-@pytest.mark.parametrize("TN,TK", [(256, 32), (128, 16)])
-def test_gemm_real_within_bound(cuda, oracle, M, N, K, flags, TN, TK):
+@pytest.mark.parametrize("TM,TN,TK", [(128, 256, 32), (128, 128, 16), (256, 256, 16), (256, 128, 32)])
+def test_gemm_real_within_bound(cuda, oracle, M, N, K, flags, TM, TN, TK):
     a = synth.uniform((M, K), -1.0, 1.0, 41)
     b = synth.normal((K, N), 42)
     c = synth.uniform((M, N), -4.0, 4.0, 43)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, -0.5, TN, flags, TK=TK)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, -0.5, TN, flags, TK=TK, TM=TM)
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, -0.5)
     got = out.reshape(M, N)
     err = np.abs(got.astype(np.float64) - want)
@@ -186,7 +190,8 @@ def test_gemm_errors(cuda):
 
 
 @pytest.mark.parametrize("name", ["gemm_4100", "gemm_8192"])
-def test_gemm_full_size_sampled_rows(cuda, oracle, name):
+@pytest.mark.parametrize("TM", [128, 256])
+def test_gemm_full_size_sampled_rows(cuda, oracle, name, TM):
     # the bench workloads, in the launch configuration the bench times; rows at
     # tile edges and a seeded sample, each checked element by element
     w = synth.WORKLOADS[name]
@@ -194,8 +199,8 @@ def test_gemm_full_size_sampled_rows(cuda, oracle, name):
     a, b, c = synth.gemm_inputs(name)
     A, B, C = (torch.from_numpy(t).cuda() for t in (a, b, c))
     raw, ws, wsb = workspace(M, N, K, w["TN"])
-    aligned = M % w["TM"] == 0 and N % w["TN"] == 0 and K % w["TK"] == 0
-    tm.tm_gemm(A, K, B, N, C, N, M, N, K, w["alpha"], w["beta"], ws, wsb, w["TM"], w["TN"], w["TK"],
+    aligned = M % TM == 0 and N % w["TN"] == 0 and K % w["TK"] == 0
+    tm.tm_gemm(A, K, B, N, C, N, M, N, K, w["alpha"], w["beta"], ws, wsb, TM, w["TN"], w["TK"],
                tm.TM_ALIGNED if aligned else 0)
     tm.tm_check()
     rng = np.random.Generator(np.random.PCG64(M + K))
