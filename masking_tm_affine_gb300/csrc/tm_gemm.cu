@@ -16,18 +16,20 @@
 //      K-major hi/lo operands zero-padded to whole tiles -- the zero padding
 //      is exactly the masked remainder tile's fill -- with B transposed on
 //      the way.
-//   2. gemm (a programmatic dependent of the split): persistent, one
-//      192-thread CTA per SM walking 128 x BN output tiles.  Warp 0 issues
-//      TMA copies (K-major, 64- or 128-byte swizzle) into a ring of STAGES
-//      shared-memory stages; warp 1 owns the TMEM accumulators (two buffers
-//      of BN columns) and one of its threads issues the MMAs (K = 8 each,
-//      three per K step for 3xTF32), committing each stage back to the
-//      producer and each finished tile to the epilogue through mbarriers;
-//      warps 2-5 read the other accumulator buffer out of TMEM (32x32b loads)
-//      and write alpha * acc + beta * C, masking the M and N edges unless the
-//      promise holds, while the next tile accumulates.  Every wait is
-//      bounded; a stalled pipeline sets the status word and the CTA drains
-//      and frees its TMEM before it exits.
+//   2. gemm (a programmatic dependent of the split): persistent 192-thread
+//      CTAs walking the output tiles -- by default CTA pairs (2-CTA clusters,
+//      256-row tiles, tcgen05 cta_group::2: each CTA stages 128 rows of A and
+//      half of the B tile, and the even CTA issues the MMAs for both), else
+//      one CTA per 128-row tile.  Warp 0 issues TMA copies (K-major, 64- or
+//      128-byte swizzle) into a ring of STAGES shared-memory stages; warp 1
+//      owns the TMEM accumulators (two buffers of BN columns) and one of its
+//      threads issues the MMAs (K = 8 each, three per K step for 3xTF32),
+//      committing each stage back to the producers and each finished tile to
+//      the epilogues through mbarriers; warps 2-5 read the other accumulator
+//      buffer out of TMEM (32x32b loads) and write alpha * acc + beta * C
+//      (through TMA when C's layout allows), while the next tile accumulates.
+//      Every wait is bounded; a stalled pipeline sets the status word and the
+//      CTA drains and frees its TMEM before it exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
