@@ -594,3 +594,47 @@ def test_gemm_rows_row_subset_and_lds(oracle):
     Af = A.reshape(M, lda)[:, :K].astype(np.float64)
     Bf = B.reshape(K, ldb)[:, :N].astype(np.float64)
     assert np.allclose(got, (Af @ Bf)[rows].astype(np.float32), rtol=1e-6, atol=1e-6)
+
+
+def test_gemm_rows_exact_rationals_brute_force(oracle):
+    # small dyadic entries: every fp64 product and partial sum is exact, so the
+    # oracle must equal the exact rational result rounded once to fp32
+    from fractions import Fraction
+    rng = np.random.Generator(np.random.PCG64(77))
+    for M, N, K in [(1, 1, 1), (2, 3, 4), (3, 5, 7), (4, 2, 9)]:
+        A = (rng.integers(-64, 65, (M, K)) / 16.0).astype(np.float32)
+        B = (rng.integers(-64, 65, (K, N)) / 8.0).astype(np.float32)
+        C = (rng.integers(-64, 65, (M, N)) / 4.0).astype(np.float32)
+        alpha, beta = -0.75, 1.5
+        got = oracle.gemm_rows(A, K, B, N, C, N, np.arange(M), N, K, alpha, beta)
+        for i in range(M):
+            for j in range(N):
+                exact = Fraction(alpha) * sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(K)) \
+                    + Fraction(beta) * Fraction(float(C[i, j]))
+                assert got[i, j] == np.float32(float(exact)), (M, N, K, i, j)
+
+
+def test_gemm_rows_rounds_once(oracle):
+    # 1 + 2^-24 + 2^-24: an fp32 running sum rounds each step back to 1 (ties to
+    # even); the definition's exact sum 1 + 2^-23 is an fp32 number
+    A = np.array([[1.0, 2.0 ** -24, 2.0 ** -24]], np.float32)
+    B = np.ones((3, 1), np.float32)
+    got = oracle.gemm_rows(A, 3, B, 1, None, 0, np.arange(1), 1, 3)
+    assert got[0, 0] == np.float32(1.0 + 2.0 ** -23)
+    f32 = np.float32(0.0)
+    for x in A[0]:
+        f32 = np.float32(f32 + x)
+    assert f32 == np.float32(1.0)       # the mistake this pin catches
+
+
+def test_gemm_rows_beta_zero_ignores_c(oracle):
+    # beta == 0 takes no term from C (BLAS convention): NaN in C stays out
+    A = synth.uniform((3, 4), -1.0, 1.0, 78)
+    B = synth.uniform((4, 2), -1.0, 1.0, 79)
+    C = np.full((3, 2), np.nan, np.float32)
+    got = oracle.gemm_rows(A, 4, B, 2, C, 2, np.arange(3), 2, 4, 2.0, 0.0)
+    want = oracle.gemm_rows(A, 4, B, 2, None, 0, np.arange(3), 2, 4, 2.0, 0.0)
+    assert np.all(np.isfinite(got)) and np.array_equal(got, want)
+    # alpha == 0, beta == 1: C passes through unchanged
+    C2 = synth.normal((3, 2), 80)
+    assert np.array_equal(oracle.gemm_rows(A, 4, B, 2, C2, 2, np.arange(3), 2, 4, 0.0, 1.0), C2)
