@@ -804,7 +804,9 @@ def run_cases(args):
                 O = torch.empty(Mw, dtype=torch.float32, device=dev)
                 nbytes = 4 * Mw * Nw + 4 * Mw
                 fl = {"vec": 0, "scalar": tm.TM_PATH_SCALAR}
-                RT_, RN_ = tile or ROWSUM_TILE
+                # [4096, 4096]: 2 rows x 512 columns per block fills one wave (ncu sweep:
+                # 12.6 us vs 13.4 us at 1 x 1024); the step's [8192, 8192] keeps ROWSUM_TILE
+                RT_, RN_ = tile or ((2, 512) if Mw * Nw <= (1 << 24) else ROWSUM_TILE)
                 mk = lambda v: (lambda: tm.tm_rowsum(X, Nw, Mw, Nw, O, RT_, RN_, fl[v], s))
             elif kern == "colsum":
                 O = torch.empty(Nw, dtype=torch.float32, device=dev)
@@ -845,7 +847,7 @@ def run_cases(args):
                 nbytes = 4 * Mw * Nw + 4 * Mw
                 fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
                       "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
-                BR_, BC_ = tile or (16 if Nw < 4096 else ROWMAX_BR, w.get("BC", 64))
+                BR_, BC_ = tile or (8 if Nw < 4096 else ROWMAX_BR, w.get("BC", 64))  # short rows: 8 per block
                 mk = lambda v: (lambda: tm.tm_rowmax_masked(X, Nw, Mw, Nw, O, BR_, BC_, fm[v][0], fm[v][1], s))
         chosen = variants if args.variant == "all" else [args.variant or variants[0]]
         for v in chosen:
