@@ -64,7 +64,7 @@ typedef enum tm_status {
     TM_ERR_MISALIGNED = 3,       /* a vector path or TM_ALIGNED with a pointer or ld that breaks 16-byte alignment */
     TM_ERR_BROKEN_PROMISE = 4,   /* TM_ALIGNED while M % TM != 0 or N % TN != 0 */
     TM_ERR_CUDA = 5,             /* a CUDA runtime call or kernel launch failed */
-    TM_ERR_WORKSPACE = 6,        /* colsum workspace NULL, too small or not 16-byte aligned */
+    TM_ERR_WORKSPACE = 6,        /* workspace NULL, too small or misaligned (colsum: 16 bytes, gemm: 1024) */
     TM_ERR_TIMEOUT = 7           /* a bounded device-side wait gave up (reported by tm_check) */
 } tm_status;
 
@@ -338,7 +338,9 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
  *   outside [M, N] (the ld gap included) is written.
  *   workspace, ws_bytes   device scratch of at least
  *            tm_gemm_workspace_bytes(M, N, K, TN) bytes, 1024-byte aligned,
- *            overlapping no operand; contents on entry do not matter.
+ *            overlapping no operand; contents on entry do not matter.  It is in
+ *            use until the call's kernels finish on `stream`: calls that may
+ *            run at the same time need separate workspaces.
  * Accuracy: |C - exact| <= (3*2^-22 + 3*K*2^-23) * |alpha| * sum_k |a_ik||b_kj|
  *   + 2^-23 * (|alpha * (A B)_ij| + |beta c_ij|) (3xTF32; tensor-core
  *   accumulation is taken as fp32 with truncation).  Integer-valued inputs
@@ -376,6 +378,18 @@ tm_status tm_check(tm_stream_t stream);
  * Errors: INVALID_ARG (K < 0, T <= 0, out4 NULL), CUDA.
  */
 tm_status tm_tile_walk_probe(int64_t K, int32_t T, int64_t *out4, tm_stream_t stream);
+
+/*
+ * tm_wait_timeout_probe -- exercises the failure path of the pipelined kernels
+ * (the gemm and the staged column sum), which has no counterpart in the
+ * pages: one thread waits, with the same bounded mbarrier wait those kernels
+ * use, on a barrier that nothing arrives at.  After the limit (about 2e9 SM
+ * cycles, ~1 s) the wait gives up, the kernel records the timeout in the
+ * device's status word and ends normally; the next tm_check returns
+ * TM_ERR_TIMEOUT and the context stays usable.
+ * Errors: CUDA.
+ */
+tm_status tm_wait_timeout_probe(tm_stream_t stream);
 
 /*
  * tm_scale2d_unchecked -- tm_scale2d on its TM_ALIGNED path without the host

@@ -647,6 +647,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
+// One thread waits, with the pipeline's own bounded wait, on an mbarrier that
+// nothing arrives at; when the limit runs out it records the timeout exactly
+// as a stalled gemm role does, and the kernel ends normally.
+__global__ void __launch_bounds__(32) wait_timeout_probe(unsigned *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_flag = 0;
+        if (!mbar_wait(su32(&bar), 0u)) gemm_fail(&abort_flag, status);
+    }
+}
+
 // ------------------------------------------------------------------ host
 PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn()
 {
@@ -904,4 +919,13 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     }
     const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);
     return launch_gemm_tiles<false>(TN, TK, three, aligned, maps, g, grid, s);
+}
+
+extern "C" tm_status tm_wait_timeout_probe(tm_stream_t stream)
+{
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    wait_timeout_probe<<<1, 32, 0, as_stream(stream)>>>(dev->status);
+    return launch_status();
 }

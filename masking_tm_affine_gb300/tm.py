@@ -73,6 +73,7 @@ SIGNATURES = {
     "tm_check": (_st, [_vp]),
     "tm_tile_walk_probe": (_st, [_i64, _i32, _vp, _vp]),
     "tm_scale2d_unchecked": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
+    "tm_wait_timeout_probe": (_st, [_vp]),
 }
 
 _lib = None
@@ -233,6 +234,11 @@ def tm_check(stream=None) -> None:
 
 def tm_tile_walk_probe(K: int, T: int, out4, stream=None) -> None:
     _ok(load().tm_tile_walk_probe(K, T, _ptr(out4), _stream(stream)), "tm_tile_walk_probe")
+
+
+def tm_wait_timeout_probe(stream=None) -> None:
+    """A bounded wait that runs out (~1 s): the next tm_check raises TM_ERR_TIMEOUT."""
+    _ok(load().tm_wait_timeout_probe(_stream(stream)), "tm_wait_timeout_probe")
 
 
 def tm_scale2d_unchecked(X, ldx: int, Y, ldy: int, M: int, N: int, alpha: float, TM: int, TN: int,

@@ -34,3 +34,19 @@ def test_probe_closed_form_sweep(cuda):
 def test_check_clean(cuda):
     tm.tm_check()
     assert np.isfinite(1.0)
+
+
+def test_bounded_wait_times_out_and_context_survives(cuda):
+    # a wait on a barrier nothing arrives at gives up after ~1 s and reports
+    # TM_ERR_TIMEOUT through tm_check; the context keeps working afterwards
+    tm.tm_check()
+    tm.tm_wait_timeout_probe()
+    with pytest.raises(tm.TmError) as e:
+        tm.tm_check()
+    assert e.value.status == tm.TM_ERR_TIMEOUT
+    tm.tm_check()                                   # the status word was cleared
+    a = torch.arange(1000, dtype=torch.float32, device="cuda")
+    out = torch.empty_like(a)
+    tm.tm_affine(a, out, 1000)
+    tm.tm_check()
+    assert torch.equal(out, a * 2 + 1)
