@@ -84,7 +84,9 @@ def build(force: bool = False) -> str:
     if force or _stale(LIB, objs):
         tmp = LIB + ".tmp%d" % os.getpid()
         libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
-        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath," + libdir, "-o", tmp, *objs]
+        # --no-undefined: a symbol some unit uses but none defines fails the build, not the first load
+        cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath," + libdir, "-Xlinker", "--no-undefined",
+               "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link of libtm.so failed:\n%s" % r.stderr[-6000:])

@@ -38,7 +38,6 @@ constexpr int kNaiveRows = 256;        // the page's program length
 constexpr int64_t kTargetUnits = 8192; // (strip, chunk) work units aimed for: one block each
 constexpr int64_t kMinChunkRows = 64;  // rows per chunk at least: 8 row lanes x 8 loads in flight
 constexpr int kFinishPG = 8;           // chunk groups per column in the finish pass
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 
 struct ColPlan {
     int64_t S;      // column strips: ceil(N / TN)
@@ -227,35 +226,6 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
 }
 
 // ------------------------------------------------------------------ STAGED (TMA)
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for phase `parity` of the mbarrier, giving up after ~1 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) return false;
-    }
-    return true;
-}
-
 template <int TM, int TN, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
                                                           int stages)
@@ -376,22 +346,6 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
 
 bool staged_tile(int TM, int TN)
 {
@@ -563,7 +517,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     if (variant == TM_VAR_NAIVE) v = Variant::Naive;
     else if (variant == TM_VAR_REGDIRECT) v = Variant::RegDirect;
     else if (variant == TM_VAR_STAGED) {
-        if (encode_fn() == nullptr) return TM_ERR_CUDA;
+        if (tensor_map_encoder() == nullptr) return TM_ERR_CUDA;
         v = Variant::Staged;
     } else v = Variant::RegDirect;  // measured faster than STAGED at every tile on GB300 (e.g. 51.9 vs 66.2 us
                                     // at 8192 x 8192, 32 x 128): lanes over columns already coalesce
@@ -593,7 +547,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
                 const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
                 const cuuint32_t box[2] = {(cuuint32_t)TN, (cuuint32_t)TM};
                 const cuuint32_t estr[2] = {1, 1};
-                if (encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(X), dims, strides,
+                if (tensor_map_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(X), dims, strides,
                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                     return TM_ERR_CUDA;

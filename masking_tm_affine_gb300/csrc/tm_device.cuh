@@ -96,6 +96,39 @@ __device__ __forceinline__ void st_v8(void *p, const u32x8 &x)
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
+// ---------------------------------------------------------------- mbarriers
+// Bounded waits on shared-memory mbarriers (the TMA pipelines of the staged
+// column sum and the gemm).  A wait gives up after kWaitCycles SM clock cycles
+// (~1 s at full clock): the caller then records kStatusTimeout, drains what it
+// started and exits, so a stalled pipeline never hangs the GPU.
+constexpr long long kWaitCycles = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the completion of phase `parity` of the mbarrier at shared address
+// `bar`; false if it has not completed within `limit` cycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit = kWaitCycles)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) return false;
+    return true;
+}
+
 // ---------------------------------------------------------------- dependent launch
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start (and run its prologue) while the

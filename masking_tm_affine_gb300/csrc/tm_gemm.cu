@@ -42,7 +42,6 @@ namespace {
 
 constexpr int GBM = 128;  // UMMA M (one CTA)
 constexpr int GBK = 32;   // K padding granule of the split operands (a multiple of both stage widths)
-constexpr long long kGemmWait = 2000000000LL;  // clock64 cycles (~1 s) a pipeline wait may take
 
 // ------------------------------------------------------------------ split pass
 __device__ __forceinline__ uint32_t to_tf32(float x)
@@ -100,30 +99,6 @@ __global__ void __launch_bounds__(256) split_operands(const SplitArgs a)
 }
 
 // ------------------------------------------------------------------ gemm
-__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try(bar, parity))
-        if (clock64() - t0 > kGemmWait) return false;
-    return true;
-}
-
 // Shared-memory matrix descriptor: start >> 4 in [0, 14), leading byte offset
 // >> 4 in [16, 30), stride byte offset >> 4 in [32, 46), descriptor version 1
 // at bit 46, layout in [61, 64): 2 = 128-byte swizzle, 4 = 64-byte swizzle.
@@ -302,10 +277,10 @@ __device__ __forceinline__ bool gemm_aborted(const int *flag) { return *(volatil
 // the abort flag that this wait also watches.
 __device__ __forceinline__ bool acc_wait(uint32_t bar, uint32_t parity, int KT, const int *abort_flag)
 {
-    if (mbar_try(bar, parity)) return true;
-    const long long limit = kGemmWait + 40000LL * KT;
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long limit = kWaitCycles + 40000LL * KT;
     const long long t0 = clock64();
-    while (!mbar_try(bar, parity)) {
+    while (!mbar_try_wait(bar, parity)) {
         if (*(volatile const int *)abort_flag != 0 || clock64() - t0 > limit) return false;
     }
     return true;
@@ -385,20 +360,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     constexpr uint32_t kStageBytes = (uint32_t)((THREE ? 2 : 1) * (GBM + BH) * BK * sizeof(float));  // per CTA
     constexpr uint32_t kCols = 2 * BN;  // TMEM columns: two accumulator buffers
 
-    if (warp == 1) tmem_alloc<PAIR>(su32(&s.tmem), kCols);
+    if (warp == 1) tmem_alloc<PAIR>(smem_u32(&s.tmem), kCols);
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.full[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.empty[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s.full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s.empty[i])));
         }
         for (int i = 0; i < 2; ++i) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.acc_full[i])));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&s.acc_empty[i])),
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s.acc_full[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&s.acc_empty[i])),
                          "r"(PAIR ? 256 : 128));
         }
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.done)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s.done)));
         for (int i = 0; i < 4; ++i)
-            for (int j = 0; j < 2; ++j) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&s.cbar[i][j])));
+            for (int j = 0; j < 2; ++j) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s.cbar[i][j])));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s.abort = 0;
     }
@@ -420,7 +395,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int am = m0 + (int)rank * GBM, bn = n0 + (int)rank * BH;
                 for (int kt = 0; kt < g.KT; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
-                    if (it >= STAGES && !mbar_wait(su32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
+                    if (it >= STAGES && !mbar_wait_bounded(smem_u32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
                         gemm_fail(&s.abort, g.status);
                         ok = false;
                         break;
@@ -434,26 +409,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         // the even CTA's barrier counts both CTAs' bytes
                         if (rank == 0)
                             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
-                                             su32(&s.full[st])),
+                                             smem_u32(&s.full[st])),
                                          "r"(2 * kStageBytes)
                                          : "memory");
-                        const uint32_t bar = cluster_addr(su32(&s.full[st]), 0);
-                        tma_load_pair(su32(s.st[st].a_hi), &m_ahi, kx, am, bar);
-                        tma_load_pair(su32(s.st[st].b_hi), &m_bhi, kx, bn, bar);
+                        const uint32_t bar = cluster_addr(smem_u32(&s.full[st]), 0);
+                        tma_load_pair(smem_u32(s.st[st].a_hi), &m_ahi, kx, am, bar);
+                        tma_load_pair(smem_u32(s.st[st].b_hi), &m_bhi, kx, bn, bar);
                         if (THREE) {
-                            tma_load_pair(su32(s.st[st].a_lo), &m_alo, kx, am, bar);
-                            tma_load_pair(su32(s.st[st].b_lo), &m_blo, kx, bn, bar);
+                            tma_load_pair(smem_u32(s.st[st].a_lo), &m_alo, kx, am, bar);
+                            tma_load_pair(smem_u32(s.st[st].b_lo), &m_blo, kx, bn, bar);
                         }
                     } else {
-                        const uint32_t bar = su32(&s.full[st]);
+                        const uint32_t bar = smem_u32(&s.full[st]);
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                                      "r"(kStageBytes)
                                      : "memory");
-                        tma_load(su32(s.st[st].a_hi), &m_ahi, kx, am, bar);
-                        tma_load(su32(s.st[st].b_hi), &m_bhi, kx, bn, bar);
+                        tma_load(smem_u32(s.st[st].a_hi), &m_ahi, kx, am, bar);
+                        tma_load(smem_u32(s.st[st].b_hi), &m_bhi, kx, bn, bar);
                         if (THREE) {
-                            tma_load(su32(s.st[st].a_lo), &m_alo, kx, am, bar);
-                            tma_load(su32(s.st[st].b_lo), &m_blo, kx, bn, bar);
+                            tma_load(smem_u32(s.st[st].a_lo), &m_alo, kx, am, bar);
+                            tma_load(smem_u32(s.st[st].b_lo), &m_blo, kx, bn, bar);
                         }
                     }
                 }
@@ -464,7 +439,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!ok || PAIR) {
                 if (rank == 0)
                     for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                        mbar_wait(su32(&s.full[j % STAGES]), (j / STAGES) & 1u);
+                        mbar_wait_bounded(smem_u32(&s.full[j % STAGES]), (j / STAGES) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -476,7 +451,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int t = 0;
             for (int tile = unit; tile < g.ntiles && ok; tile += units, ++t) {
                 const uint32_t ab = (uint32_t)t & 1u;
-                if (t >= 2 && !mbar_wait(su32(&s.acc_empty[ab]), ((uint32_t)(t / 2) - 1) & 1u)) {
+                if (t >= 2 && !mbar_wait_bounded(smem_u32(&s.acc_empty[ab]), ((uint32_t)(t / 2) - 1) & 1u)) {
                     gemm_fail(&s.abort, g.status);
                     break;
                 }
@@ -484,14 +459,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t d = tmem + ab * BN;
                 for (int kt = 0; kt < g.KT; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
-                    if (!mbar_wait(su32(&s.full[st]), (it / STAGES) & 1u) || gemm_aborted(&s.abort)) {
+                    if (!mbar_wait_bounded(smem_u32(&s.full[st]), (it / STAGES) & 1u) || gemm_aborted(&s.abort)) {
                         if (!gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
                         ok = false;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t ahi = su32(s.st[st].a_hi), alo = su32(s.st[st].a_lo);
-                    const uint32_t bhi = su32(s.st[st].b_hi), blo = su32(s.st[st].b_lo);
+                    const uint32_t ahi = smem_u32(s.st[st].a_hi), alo = smem_u32(s.st[st].a_lo);
+                    const uint32_t bhi = smem_u32(s.st[st].b_hi), blo = smem_u32(s.st[st].b_lo);
 #pragma unroll
                     for (int k = 0; k < BK / 8; ++k) {
                         const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
@@ -501,20 +476,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             umma_tf32<PAIR>(d, smem_desc<BK>(alo + off), smem_desc<BK>(bhi + off), id, 1u);
                         }
                     }
-                    umma_commit<PAIR>(su32(&s.empty[st]));  // the stage (in both CTAs) is free once these are done
+                    umma_commit<PAIR>(smem_u32(&s.empty[st]));  // the stage (in both CTAs) is free once these are done
                 }
-                if (ok) umma_commit<PAIR>(su32(&s.acc_full[ab]));
+                if (ok) umma_commit<PAIR>(smem_u32(&s.acc_full[ab]));
             }
-            umma_commit<PAIR>(su32(&s.done));  // tracks every MMA issued, also after an abort
-            if (!mbar_wait(su32(&s.done), 0u)) gemm_fail(&s.abort, g.status);
+            umma_commit<PAIR>(smem_u32(&s.done));  // tracks every MMA issued, also after an abort
+            if (!mbar_wait_bounded(smem_u32(&s.done), 0u)) gemm_fail(&s.abort, g.status);
         }
     } else {
         // ---------------- epilogue: TMEM rows -> alpha * acc + beta * C
         const int eg = warp & 3;  // TMEM lane group this warp may access (rows 32 eg .. 32 eg + 31)
         const bool use_c = g.beta != 0.0f;
         // the MMA issuer's "accumulator free" barrier (in the even CTA of a pair)
-        const uint32_t acc_empty0 = PAIR ? cluster_addr(su32(&s.acc_empty[0]), 0) : su32(&s.acc_empty[0]);
-        const uint32_t acc_empty1 = PAIR ? cluster_addr(su32(&s.acc_empty[1]), 0) : su32(&s.acc_empty[1]);
+        const uint32_t acc_empty0 = PAIR ? cluster_addr(smem_u32(&s.acc_empty[0]), 0) : smem_u32(&s.acc_empty[0]);
+        const uint32_t acc_empty1 = PAIR ? cluster_addr(smem_u32(&s.acc_empty[1]), 0) : smem_u32(&s.acc_empty[1]);
         uint32_t cpar = 0;        // bit j: parity of the next completion of cbar[eg][j]
         uint32_t loads_out = 0;   // bit j: a load into cbuf[eg][j] is in flight
         int t = 0;
@@ -535,9 +510,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // rest into L2, while this tile's MMAs run
             if (use_c && tma_path && lane == 0) {
                 for (int ci = 0; ci < 2 && ci < nchunks; ++ci) {
-                    const uint32_t bar = su32(&s.cbar[eg][ci]);
+                    const uint32_t bar = smem_u32(&s.cbar[eg][ci]);
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 4096;" ::"r"(bar) : "memory");
-                    tma_load(su32(s.cbuf[eg][ci]), &m_c, (int)n0 + 32 * ci, (int)row0, bar);
+                    tma_load(smem_u32(s.cbuf[eg][ci]), &m_c, (int)n0 + 32 * ci, (int)row0, bar);
                     loads_out |= 1u << ci;
                 }
             }
@@ -545,7 +520,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int c = tma_path ? 64 : 0; c < ncols; c += 32)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + c));
             }
-            if (!acc_wait(su32(&s.acc_full[ab]), ((uint32_t)t / 2) & 1u, g.KT, &s.abort) || gemm_aborted(&s.abort)) {
+            if (!acc_wait(smem_u32(&s.acc_full[ab]), ((uint32_t)t / 2) & 1u, g.KT, &s.abort) || gemm_aborted(&s.abort)) {
                 if (!gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
                 break;
             }
@@ -561,17 +536,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (ci >= 1 && lane == 0) {
                         bulk_wait_read();  // chunk ci-1's store has read its buffer (and ci-2's, this one)
                         if (use_c && ci + 1 < nchunks) {
-                            const uint32_t bar = su32(&s.cbar[eg][bsel ^ 1]);
+                            const uint32_t bar = smem_u32(&s.cbar[eg][bsel ^ 1]);
                             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 4096;" ::"r"(bar)
                                          : "memory");
-                            tma_load(su32(s.cbuf[eg][bsel ^ 1]), &m_c, (int)n0 + 32 * (ci + 1), (int)row0, bar);
+                            tma_load(smem_u32(s.cbuf[eg][bsel ^ 1]), &m_c, (int)n0 + 32 * (ci + 1), (int)row0, bar);
                             loads_out |= 1u << (bsel ^ 1);
                         }
                     }
                     uint32_t r[32];
                     tmem_ld32(tbase + (uint32_t)(32 * ci), r);
                     if (use_c) {
-                        if (!mbar_wait(su32(&s.cbar[eg][bsel]), (cpar >> bsel) & 1u)) {
+                        if (!mbar_wait_bounded(smem_u32(&s.cbar[eg][bsel]), (cpar >> bsel) & 1u)) {
                             gemm_fail(&s.abort, g.status);
                             ok = false;
                             break;
@@ -600,7 +575,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA store
                     __syncwarp();
-                    if (lane == 0) tma_store(&m_c, (int)n0 + 32 * ci, (int)row0, su32(s.cbuf[eg][bsel]));
+                    if (lane == 0) tma_store(&m_c, (int)n0 + 32 * ci, (int)row0, smem_u32(s.cbuf[eg][bsel]));
                 }
                 if (lane == 0) bulk_wait_read();  // both buffers free for the next tile
                 __syncwarp();
@@ -632,7 +607,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             bulk_wait_all();  // stores complete before the CTA (and its shared memory) goes away
             for (int j = 0; j < 2; ++j)  // a load still in flight after an abort lands first
-                if (loads_out & (1u << j)) mbar_wait(su32(&s.cbar[eg][j]), (cpar >> j) & 1u);
+                if (loads_out & (1u << j)) mbar_wait_bounded(smem_u32(&s.cbar[eg][j]), (cpar >> j) & 1u);
         }
         __syncwarp();
     }
@@ -655,30 +630,14 @@ __global__ void __launch_bounds__(32) wait_timeout_probe(unsigned *status)
     __shared__ __align__(8) uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bar)));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar)));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         abort_flag = 0;
-        if (!mbar_wait(su32(&bar), 0u)) gemm_fail(&abort_flag, status);
+        if (!mbar_wait_bounded(smem_u32(&bar), 0u)) gemm_fail(&abort_flag, status);
     }
 }
 
 // ------------------------------------------------------------------ host
-PFN_cuTensorMapEncodeTiled_v12000 gemm_encode_fn()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    });
-    return fn;
-}
 
 bool kmajor_map(CUtensorMap *m, float *base, int64_t rows, int64_t Kp, int box_rows, int BK)
 {
@@ -686,7 +645,7 @@ bool kmajor_map(CUtensorMap *m, float *base, int64_t rows, int64_t Kp, int box_r
     const cuuint64_t strides[1] = {(cuuint64_t)Kp * sizeof(float)};
     const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     const cuuint32_t es[2] = {1, 1};
-    return gemm_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+    return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -839,7 +798,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     const DevInfo *dev;
     tm_status st = device_info(&dev);
     if (st != TM_OK) return st;
-    if (gemm_encode_fn() == nullptr) return TM_ERR_CUDA;
+    if (tensor_map_encoder() == nullptr) return TM_ERR_CUDA;
     cudaStream_t s = as_stream(stream);
     char *ws = static_cast<char *>(workspace);
     float *ahi = reinterpret_cast<float *>(ws + pl.off[0]), *alo = reinterpret_cast<float *>(ws + pl.off[1]);
@@ -893,7 +852,7 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
         const cuuint64_t strides[1] = {(cuuint64_t)ldc * sizeof(float)};
         const cuuint32_t box[2] = {32, 32};
         const cuuint32_t es[2] = {1, 1};
-        if (gemm_encode_fn()(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, es,
+        if (tensor_map_encoder()(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, es,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return TM_ERR_CUDA;

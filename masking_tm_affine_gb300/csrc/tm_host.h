@@ -1,6 +1,8 @@
 // tm_host.h -- host-side internals shared by the libtm translation units.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -22,6 +24,10 @@ struct DevInfo {
 
 // Current device's info; TM_ERR_CUDA if the runtime cannot answer.
 tm_status device_info(const DevInfo **out);
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime
+// (no link against libcuda); nullptr if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Flat grid: one block per work unit, capped at the 2^31-1 grid limit (the
 // kernels keep a grid-stride loop for anything beyond it).  On GB300 the block
