@@ -368,12 +368,22 @@ bool pow2_in(int v, int lo, int hi)
     return v >= lo && v <= hi && (v & (v - 1)) == 0;
 }
 
+// Persistent: as many blocks as fit on the SMs at once, each streaming its
+// units' tiles through one ring (a block's stream runs on across unit
+// boundaries).  One block per unit, as for the register-direct pass, left
+// each block two tiles at 8192 x 8192 (32 x 128) and a TMA round trip per
+// 32 KB: 52.0 us kernel time (ncu) against 46.9 us persistent.
 template <int TM, int TN>
-tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, cudaStream_t s)
+tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, int sms, cudaStream_t s)
 {
     const void *k = aligned ? (const void *)colsum_staged<TM, TN, true> : (const void *)colsum_staged<TM, TN, false>;
     const int max_stages = staged_stages(TM, TN);
-    int stages = a.CT < max_stages ? (int)a.CT : max_stages;  // a unit holds CT tiles: no deeper ring needed
+    const int64_t block_smem = (int64_t)max_stages * TM * TN * sizeof(float) + 8 * 1024;  // ring + static arrays
+    int64_t per_sm = (int64_t)(227 * 1024) / block_smem;
+    per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
+    const int64_t grid = a.units < per_sm * sms ? a.units : per_sm * sms;
+    // a block that holds one unit needs no deeper ring than the unit's CT tiles
+    int stages = (a.units <= grid && a.CT < max_stages) ? (int)a.CT : max_stages;
     const size_t max_smem = (size_t)max_stages * TM * TN * sizeof(float) + (size_t)max_stages * sizeof(uint64_t);
     const size_t smem = (size_t)stages * TM * TN * sizeof(float) + (size_t)stages * sizeof(uint64_t);
     static std::once_flag attr_once[kMaxDevices][2];
@@ -388,17 +398,18 @@ tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a
     });
     if (!attr_ok) return TM_ERR_CUDA;
     void *args[] = {const_cast<CUtensorMap *>(&map), const_cast<ColArgs *>(&a), &stages};
-    if (cudaLaunchKernel(k, dim3(flat_grid(a.units)), dim3(kThreads), args, smem, s) != cudaSuccess) {
+    if (cudaLaunchKernel(k, dim3(flat_grid(grid)), dim3(kThreads), args, smem, s) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
     return TM_OK;
 }
 
-tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a, cudaStream_t s)
+tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a, int sms,
+                        cudaStream_t s)
 {
 #define TM_STAGED(tm_, tn_) \
-    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, s);
+    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, sms, s);
     TM_STAGED(16, 64)
     TM_STAGED(32, 64)
     TM_STAGED(64, 64)
@@ -551,7 +562,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                     return TM_ERR_CUDA;
-                st = launch_staged(TM, TN, aligned, map, a, s);
+                st = launch_staged(TM, TN, aligned, map, a, dev->sms, s);
             } else {
                 switch (TN) {
                 case 64: st = launch_regdirect_t<64>(vec, aligned, a, s); break;
