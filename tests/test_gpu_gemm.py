@@ -209,3 +209,25 @@ def test_gemm_full_size_sampled_rows(cuda, oracle, name, TM):
     want = oracle.gemm_rows(a, K, b, N, c, N, rows, N, K, w["alpha"], w["beta"])
     err = np.abs(got.astype(np.float64) - want)
     assert np.all(err <= bound(a[rows], b, c[rows], w["alpha"], w["beta"], want))
+
+
+@pytest.mark.parametrize("TM", [128, 256])
+@pytest.mark.parametrize("lead", [1, 2, 3])
+def test_gemm_unaligned_bases(cuda, oracle, TM, lead):
+    # A, B and C start `lead` words past a 16-byte boundary: the split reads
+    # with 4-byte loads and C takes the direct epilogue (no TMA on C); the ld
+    # gaps hold poison that must never be read, the lead words and canaries
+    # must come back untouched
+    M, N, K = 150, 132, 70
+    a, b, c = ints((M, K), 61), ints((K, N), 62), ints((M, N), 63)
+    lda, ldb, ldc = K + 2, N + 4, N + 4
+    Ah, Bh, Ch = synth.pad_rows(a, lda), synth.pad_rows(b, ldb), synth.pad_rows(c, ldc)
+    AD, BD, CD = DevBuf(Ah, lead), DevBuf(Bh, lead), DevBuf(Ch, lead)
+    raw, ws, wsb = workspace(M, N, K, 256)
+    tm.tm_gemm(AD.ptr, lda, BD.ptr, ldb, CD.ptr, ldc, M, N, K, 1.5, 0.5, ws, wsb, TM, 256, 32)
+    tm.tm_check()
+    assert AD.guards_intact() and BD.guards_intact() and CD.guards_intact()
+    got = CD.payload_u32().reshape(M, ldc)
+    want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, 0.5)
+    assert np.array_equal(got[:, :N], want.view(np.uint32))
+    assert np.array_equal(got[:, N:], Ch.view(np.uint32).reshape(M, ldc)[:, N:])
