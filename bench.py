@@ -545,7 +545,7 @@ def run_sweep(args):
             shape, flags = (E // n, n), tm.TM_ALIGNED
         else:
             shape, flags = (1, E), 0
-        X = torch.randn(E, device=dev)
+        X = torch.randn(E, device=dev, generator=torch.Generator(device=dev).manual_seed(lg))  # values are immaterial
         Y = torch.empty_like(X)
         A1 = torch.empty_like(X)
         res = {}
