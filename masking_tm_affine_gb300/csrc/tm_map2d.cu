@@ -119,7 +119,12 @@ __device__ __forceinline__ void store_vec(float *p, const Vec<EW> &x)
     }
 }
 
-template <int TM, int TN, Op OP, Path P, int EW>
+// IT: the index type of element offsets -- uint32_t when every offset the
+// walk dereferences is below 2^31 (host-checked), int64_t otherwise.  The
+// narrower arithmetic frees registers: the ragged 64 x 64 map drops from 38
+// to fit 8 blocks per SM, so a ragged tensor of a few tens of MB runs in one
+// wave instead of 1.14.
+template <int TM, int TN, Op OP, Path P, int EW, typename IT = int64_t>
 __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
 {
     constexpr int VPR = TN / EW;                       // accesses per tile row
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
 #pragma unroll(U / UB <= 4 ? U / UB : 1)
         for (int b = 0; b < U; b += UB) {
             Vec<EW> val[UB];
-            int64_t yoff[UB];
+            IT yoff[UB];
             uint32_t chan[UB];  // Op::Channel: the first element's channel (C < 2^31)
             bool live[UB];
 #pragma unroll
@@ -162,19 +167,19 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
                 const uint32_t c = (v % VPR) * EW;
                 const uint32_t pm = fdiv(tile, p.div_tiles_n);
                 const uint32_t pn = tile - pm * p.tiles_n;
-                const int64_t i = (int64_t)pm * TM + r;
-                const int64_t j = (int64_t)pn * TN + c;
+                const IT i = (IT)pm * TM + r;
+                const IT j = (IT)pn * TN + c;
                 bool in = (G == 1) || (tile < p.ntiles);
-                if constexpr (P != Path::Aligned) in = in && (i < p.M) && (j < p.N);
+                if constexpr (P != Path::Aligned) in = in && ((int64_t)i < p.M) && ((int64_t)j < p.N);
                 live[u] = in;
-                yoff[u] = i * p.ldy + j;
+                yoff[u] = i * (IT)p.ldy + j;  // (wraps harmlessly for masked elements when IT is 32-bit)
                 if constexpr (OP == Op::Channel)
                     chan[u] = p.layout == 0 ? (uint32_t)j : (uint32_t)i - fdiv((uint32_t)i, p.div_C) * p.C;
                 // Op::Pad: the walk covers the padded extents; the source is read
                 // only inside [Msrc, Nsrc] (vectors there are whole: Nsrc % EW == 0)
-                const bool src = OP != Op::Pad || (i < p.Msrc && j < p.Nsrc);
+                const bool src = OP != Op::Pad || ((int64_t)i < p.Msrc && (int64_t)j < p.Nsrc);
                 if (in && src) {
-                    val[u] = load_vec<EW>(p.X + i * p.ldx + j);
+                    val[u] = load_vec<EW>(p.X + (i * (IT)p.ldx + j));
                 } else {
 #pragma unroll
                     for (int e = 0; e < EW; ++e) val[u].v[e] = 0u;  // a masked load reads 0
@@ -213,13 +218,27 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
     }
 }
 
+// Every element offset the ragged walk dereferences fits 31 bits: the last
+// element of X (of the source region for Op::Pad) and of Y.
+template <Op OP>
+bool offsets_fit_i32(const Map2dArgs &a)
+{
+    const int64_t xm = OP == Op::Pad ? a.Msrc : a.M, xn = OP == Op::Pad ? a.Nsrc : a.N;
+    const auto last = [](int64_t rows, int64_t ld, int64_t cols) { return rows > 0 ? (rows - 1) * ld + cols : 0; };
+    return last(xm, a.ldx, xn) <= INT32_MAX && last(a.M, a.ldy, a.N) <= INT32_MAX;
+}
+
 template <int TM, int TN, Op OP>
 tm_status launch_tile(Path path, int ew, const Map2dArgs &a, cudaStream_t s)
 {
     const void *k = nullptr;
     if (path == Path::Aligned && ew == 8) k = (const void *)map2d_kernel<TM, TN, OP, Path::Aligned, 8>;
     else if (path == Path::Aligned) k = (const void *)map2d_kernel<TM, TN, OP, Path::Aligned, 4>;
-    else if (path == Path::RaggedVec) k = (const void *)map2d_kernel<TM, TN, OP, Path::RaggedVec, 4>;
+    else if (path == Path::RaggedVec)
+        // 32 x 32 tiles already fit 32 registers with 64-bit offsets (and need more with 32-bit ones)
+        k = (!(TM == 32 && TN == 32) && offsets_fit_i32<OP>(a))
+                ? (const void *)map2d_kernel<TM, TN, OP, Path::RaggedVec, 4, uint32_t>
+                : (const void *)map2d_kernel<TM, TN, OP, Path::RaggedVec, 4>;
     else k = (const void *)map2d_kernel<TM, TN, OP, Path::Scalar, 1>;
     const int EW = path == Path::Scalar ? 1 : ew;
     const int64_t V = (int64_t)TM * TN / EW;
