@@ -578,7 +578,7 @@ CASES = {
     "ragged_copy": ("ragged_4100", "copy2d", ["auto", "scalar"]),
     "ragged_scale": ("ragged_4100", "scale2d", ["auto", "scalar"]),
     "rowsum_4096": ("coalesce_4096", "rowsum", ["vec", "scalar"]),
-    "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive"]),
+    "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive", "cluster"]),
     "rowmax_8192": ("rowmax_8192", "rowmax_masked", ["neg_inf", "zero", "scalar"]),
     "softmax_8192": ("rowmax_8192", "softmax_rowstats", ["neg_inf", "zero", "scalar"]),
     "pad_ragged": ("ragged_4100", "pad2d", ["auto"]),
@@ -587,7 +587,7 @@ CASES = {
     # the reductions on the [8192, 8192] batch of the step, for tile tuning
     "softmax_8192sq": ("scale_8192", "softmax_rowstats", ["neg_inf"]),
     "rowsum_8192sq": ("scale_8192", "rowsum", ["vec"]),
-    "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect"]),
+    "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect", "cluster"]),
     "rowmax_8192sq": ("scale_8192", "rowmax_masked", ["neg_inf"]),
     # the tensor-core gemm (3xTF32 by default; tf32 = one pass)
     "gemm_4100": ("gemm_4100", "gemm", ["3xtf32", "tf32"]),
@@ -812,6 +812,7 @@ def run_cases(args):
                 O = torch.empty(Nw, dtype=torch.float32, device=dev)
                 nbytes = 4 * Mw * Nw + 4 * Nw
                 vm = {"auto": tm.TM_VAR_AUTO, "staged": tm.TM_VAR_STAGED, "regdirect": tm.TM_VAR_REGDIRECT,
+                      "cluster": tm.TM_VAR_CLUSTER,
                       "naive": tm.TM_VAR_NAIVE}
                 CT_, CN_ = tile or COLSUM_TILE
                 ws = max(tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_NAIVE),

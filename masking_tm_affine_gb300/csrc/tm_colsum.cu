@@ -225,6 +225,99 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
     }
 }
 
+// ------------------------------------------------------------------ CLUSTER (one pass)
+// The register-direct layout, with the partial sums reduced on chip: the CS
+// CTAs of a cluster split the rows of one TN-column strip, each adds its rows
+// into a TN-wide partial in its shared memory, and after one cluster barrier
+// rank 0 adds the CS partials over distributed shared memory, in rank order,
+// and writes c.  No workspace and no second pass.
+template <int TN, int CS, bool VEC, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, float *__restrict__ c, int64_t rows_per_cta)
+{
+    constexpr int EW = VEC ? 4 : 1;
+    constexpr int CL = TN / EW;           // column lanes
+    constexpr int RL = kThreads / CL;     // row lanes
+    constexpr int UNR = 8;                // rows in flight per thread
+    static_assert(CL * RL == kThreads && TN <= kThreads, "strip does not fit the block");
+    __shared__ float red[RL][TN];
+    __shared__ float part[TN];
+
+    if constexpr (ALIGNED) {
+        // a pure function of the arguments: every CTA of every cluster returns
+        // together, so no CTA is left waiting at a cluster barrier
+        const bool whole = (a.M % a.TM == 0) && (a.N % TN == 0);
+        const bool grid_ok = !VEC || ((a.ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(a.X) & 15) == 0);
+        if (!whole || !grid_ok) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            return;
+        }
+    }
+    const uint32_t rank = cluster_rank();
+    const int64_t s = blockIdx.x / CS;
+    const int cl = threadIdx.x % CL, rl = threadIdx.x / CL;
+    const int64_t j = s * TN + (int64_t)cl * EW;
+    const bool col_in = ALIGNED || j < a.N;
+    const int64_t r0 = (int64_t)rank * rows_per_cta;
+    const int64_t r1 = r0 + rows_per_cta < a.M ? r0 + rows_per_cta : a.M;
+    float acc[EW];
+#pragma unroll
+    for (int e = 0; e < EW; ++e) acc[e] = 0.0f;
+    if (col_in) {
+        const float *xp = a.X + j;
+        int64_t row = r0 + rl;
+        for (; row + (UNR - 1) * RL < r1; row += UNR * RL) {
+            uint32_t v[UNR][EW];
+#pragma unroll
+            for (int q = 0; q < UNR; ++q) {
+                const float *ptr = xp + (row + (int64_t)q * RL) * a.ldx;
+                if constexpr (VEC) {
+                    u32x4 w = ld_nc_v4(ptr);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[q][e] = w.v[e];
+                } else {
+                    v[q][0] = ld_nc_b32(ptr);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < UNR; ++q)
+#pragma unroll
+                for (int e = 0; e < EW; ++e) acc[e] += as_f(v[q][e]);
+        }
+        for (; row < r1; row += RL) {
+            const float *ptr = xp + row * a.ldx;
+            if constexpr (VEC) {
+                u32x4 w = ld_nc_v4(ptr);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
+            } else {
+                acc[0] += as_f(ld_nc_b32(ptr));
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EW; ++e) red[rl][cl * EW + e] = acc[e];
+    __syncthreads();
+    if (rl == 0) {
+#pragma unroll
+        for (int e = 0; e < EW; ++e) {
+            float t = red[0][cl * EW + e];
+#pragma unroll
+            for (int q = 1; q < RL; ++q) t += red[q][cl * EW + e];
+            part[cl * EW + e] = t;
+        }
+    }
+    cluster_sync();  // every CTA's partial of this strip is in its shared memory
+    if (rank == 0 && threadIdx.x < TN) {
+        const uint32_t mine = smem_u32(&part[threadIdx.x]);
+        float t = 0.0f;
+#pragma unroll 4
+        for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
+        const int64_t col = s * TN + threadIdx.x;
+        if (col < a.N) c[col] = t;
+    }
+    cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
+}
+
 // ------------------------------------------------------------------ STAGED (TMA)
 template <int TM, int TN, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
@@ -448,7 +541,52 @@ tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, f
     return launch_dependent((const void *)colsum_finish, dim3(flat_grid((N + 31) / 32)), dim3(256), args, 0, s);
 }
 
-enum class Variant { Naive, RegDirect, Staged };
+// The cluster variant: CS CTAs per TN-column strip (2-CTA .. 16-CTA clusters
+// are launched with the cluster-dimension attribute; 16 needs the
+// non-portable cluster size).
+template <int TN, int CS>
+tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, cudaStream_t s)
+{
+    const void *k;
+    if (vec) k = aligned ? (const void *)colsum_cluster<TN, CS, true, true> : (const void *)colsum_cluster<TN, CS, true, false>;
+    else k = aligned ? (const void *)colsum_cluster<TN, CS, false, true> : (const void *)colsum_cluster<TN, CS, false, false>;
+    if (CS > 8) {
+        static std::once_flag once[kMaxDevices][4];
+        int devno = 0;
+        cudaGetDevice(&devno);
+        bool ok = true;
+        std::call_once(once[devno][(vec ? 2 : 0) + (aligned ? 1 : 0)], [&] {
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+                cudaGetLastError();
+                ok = false;
+            }
+        });
+        if (!ok) return TM_ERR_CUDA;
+    }
+    int64_t rows_per_cta = (a.M + CS - 1) / CS;
+    const int64_t strips = (a.N + TN - 1) / TN;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(strips * CS));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<ColArgs *>(&a), &c, &rows_per_cta};
+    if (cudaLaunchKernelExC(&cfg, k, args) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    return TM_OK;
+}
+
+constexpr int kClusterCTAs = 8;  // CTAs per strip in the cluster variant
+
+enum class Variant { Naive, RegDirect, Staged, Cluster };
 
 }  // namespace
 }  // namespace libtm
@@ -458,6 +596,7 @@ using namespace libtm;
 extern "C" size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, tm_variant variant)
 {
     if (M <= 0 || N <= 0) return 0;
+    if (variant == TM_VAR_CLUSTER) return 0;  // partials stay on chip
     if (variant == TM_VAR_NAIVE) {
         const int64_t rb = (M + kNaiveRows - 1) / kNaiveRows;
         return (size_t)(rb * ((N + 3) & ~int64_t(3)) * (int64_t)sizeof(float));
@@ -476,7 +615,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     if (N > 0 && c == nullptr) return TM_ERR_INVALID_ARG;
     if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
     if (variant != TM_VAR_AUTO && variant != TM_VAR_NAIVE && variant != TM_VAR_STAGED &&
-        variant != TM_VAR_REGDIRECT)
+        variant != TM_VAR_REGDIRECT && variant != TM_VAR_CLUSTER)
         return TM_ERR_INVALID_ARG;
     if (variant != TM_VAR_NAIVE && (!pow2_in(TM, 8, 256) || !(TN == 64 || TN == 128 || TN == 256)))
         return TM_ERR_UNSUPPORTED_TILE;
@@ -498,7 +637,15 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     int64_t P = 0;
     const int64_t npad = (N + 3) & ~int64_t(3);
     ColPlan pl{};
-    if (M > 0 && N > 0) {
+    if (M > 0 && N > 0 && variant == TM_VAR_CLUSTER) {
+        // no workspace: only X and c must not overlap
+        uintptr_t xlo, xhi;
+        span2d(X, ldx, M, N, &xlo, &xhi);
+        const uintptr_t clo = reinterpret_cast<uintptr_t>(c), chi = clo + (uintptr_t)N * 4;
+        if (!(xhi <= clo || chi <= xlo)) return TM_ERR_INVALID_ARG;
+        pl = plan_chunks(M, N, TM, TN);
+        if ((N + TN - 1) / TN * kClusterCTAs > INT32_MAX) return TM_ERR_INVALID_ARG;
+    } else if (M > 0 && N > 0) {
         const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant == TM_VAR_NAIVE ? TM_VAR_NAIVE : TM_VAR_AUTO);
         if (workspace == nullptr || ws_bytes < need || !aligned_to(workspace, 16)) return TM_ERR_WORKSPACE;
         uintptr_t xlo, xhi, wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
@@ -527,11 +674,13 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     Variant v;
     if (variant == TM_VAR_NAIVE) v = Variant::Naive;
     else if (variant == TM_VAR_REGDIRECT) v = Variant::RegDirect;
+    else if (variant == TM_VAR_CLUSTER) v = Variant::Cluster;
     else if (variant == TM_VAR_STAGED) {
         if (tensor_map_encoder() == nullptr) return TM_ERR_CUDA;
         v = Variant::Staged;
     } else v = Variant::RegDirect;  // measured faster than STAGED at every tile on GB300 (e.g. 51.9 vs 66.2 us
-                                    // at 8192 x 8192, 32 x 128): lanes over columns already coalesce
+                                    // at 8192 x 8192, 32 x 128), and level with CLUSTER inside the bench step
+                                    // (46.3 vs 46.4 us) while CLUSTER needs enough strips to fill the GPU
 
     if (M > 0) {
         if (v == Variant::Naive) {
@@ -552,7 +701,14 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
             a.units = pl.units;
             a.TM = TM;
             a.status = dev->status;
-            if (v == Variant::Staged) {
+            if (v == Variant::Cluster) {
+                switch (TN) {
+                case 64: st = launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, c, s); break;
+                case 128: st = launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, c, s); break;
+                default: st = launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, c, s); break;
+                }
+                return st;  // c is written by the cluster pass itself
+            } else if (v == Variant::Staged) {
                 CUtensorMap map;
                 const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
                 const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};

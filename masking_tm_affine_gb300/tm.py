@@ -42,6 +42,7 @@ TM_VAR_VEC8 = 4
 TM_VAR_NAIVE = 5
 TM_VAR_STAGED = 6
 TM_VAR_REGDIRECT = 7
+TM_VAR_CLUSTER = 8
 
 # tm_fill
 TM_FILL_NEG_INF = 0

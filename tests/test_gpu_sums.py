@@ -15,7 +15,7 @@ from masking_tm_affine_gb300 import synth, tm
 pytestmark = pytest.mark.gpu
 
 REL = 1e-5
-COL_VARIANTS = [tm.TM_VAR_AUTO, tm.TM_VAR_NAIVE, tm.TM_VAR_STAGED, tm.TM_VAR_REGDIRECT]
+COL_VARIANTS = [tm.TM_VAR_AUTO, tm.TM_VAR_NAIVE, tm.TM_VAR_STAGED, tm.TM_VAR_REGDIRECT, tm.TM_VAR_CLUSTER]
 
 
 def within(got, want, absref):
@@ -155,3 +155,20 @@ def test_colsum_workspace_errors(cuda):
         tm.tm_colsum(XD.ptr, 128, 64, 128, C.ptr, W.ptr, ws, 32, 128)
     assert e.value.status == tm.TM_ERR_WORKSPACE
     assert np.all(C.words() == 0xDEADBEEF)
+
+
+def test_colsum_cluster_needs_no_workspace(cuda, oracle):
+    # the one-pass variant keeps its partials on chip: NULL workspace, 0 bytes
+    M, N = 777, 1000
+    x = synth.uniform((M, N), 0.0, 1.0, 13)
+    assert tm.tm_colsum_workspace_bytes(M, N, 32, 128, tm.TM_VAR_CLUSTER) == 0
+    XD, C = DevBuf(x), DevBuf.empty(N)
+    tm.tm_colsum(XD.ptr, N, M, N, C.ptr, None, 0, 32, 128, tm.TM_VAR_CLUSTER)
+    tm.tm_check()
+    assert C.guards_intact()
+    cw = oracle.colsum(x, N, M, N)
+    assert within(C.payload_f32(), cw, cw)
+    # M == 0: zeros, still without a workspace
+    tm.tm_colsum(XD.ptr, N, 0, N, C.ptr, None, 0, 32, 128, tm.TM_VAR_CLUSTER)
+    tm.tm_check()
+    assert np.all(C.payload_f32() == 0)
