@@ -97,7 +97,7 @@ typedef enum tm_variant {
     TM_VAR_NAIVE = 5,     /* the column walk: 256-lane programs over rows, stride ld between lanes */
     TM_VAR_STAGED = 6,    /* TMA tiles staged in shared memory, columns reduced from there */
     TM_VAR_REGDIRECT = 7, /* lanes over columns: coalesced row segments straight into registers */
-    TM_VAR_CLUSTER = 8    /* REGDIRECT's layout in one pass: 16-CTA clusters split a strip's rows and add
+    TM_VAR_CLUSTER = 8    /* REGDIRECT's layout in one pass: 8-CTA clusters split a strip's rows and add
                              their partials over distributed shared memory (no workspace) */
 } tm_variant;
 
