@@ -84,6 +84,15 @@ typedef void *tm_stream_t;
 #define TM_PATH_SCALAR 0x10u /* per-element accesses with per-element masks */
 #define TM_PATH_VEC 0x20u    /* 16-byte register accesses (needs the vector alignment) */
 #define TM_PATH_TMA 0x40u    /* TMA tile copies through shared memory (needs 16-byte rows) */
+/* Overlapped launch (programmatic dependent launch): the call's kernel may
+ * start while the previous kernel in the stream is still draining.  Its loads
+ * of the inputs may then run ahead of that kernel; every store, and the
+ * kernel's completion, still wait for it, so writes stay in stream order and a
+ * chain of such calls completes in order.  Use it only when no kernel still
+ * pending on the stream writes this call's inputs (for example independent
+ * maps of one resident tensor, back to back).  Accepted by every entry point
+ * that takes flags except tm_gemm, and by tm_affine OR-ed into its variant. */
+#define TM_PDL 0x200u
 
 typedef enum tm_variant {
     TM_VAR_AUTO = 0,

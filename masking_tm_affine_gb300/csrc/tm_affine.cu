@@ -27,6 +27,8 @@ __device__ __forceinline__ uint32_t affine1(uint32_t a)
 // SCALAR: one element per thread.
 __global__ void __launch_bounds__(kThreads) affine_scalar(const float *a, float *out, int64_t n)
 {
+    pdl_trigger();
+    pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride)
         st_b32(out + i, affine1(ld_nc_b32(a + i)));
@@ -36,6 +38,8 @@ __global__ void __launch_bounds__(kThreads) affine_scalar(const float *a, float 
 // each way (the under-stated alignment of the puzzle), then the scalar tail.
 __global__ void __launch_bounds__(kThreads) affine_vec_unaligned(const float *a, float *out, int64_t n)
 {
+    pdl_trigger();
+    pdl_wait();
     const int64_t chunks = n / 4;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < chunks; c += stride) {
@@ -61,11 +65,13 @@ __global__ void __launch_bounds__(kThreads) affine_vec_unaligned(const float *a,
 template <int VW, int U>
 __global__ void __launch_bounds__(kThreads) affine_vec(const float *a, float *out, int64_t n, int64_t head)
 {
+    pdl_trigger();
     const float *va = a + head;
     float *vo = out + head;
     const int64_t nvec = (n - head) / VW;
     constexpr int64_t kPerIter = (int64_t)kThreads * U;
     const int64_t iters = nvec / kPerIter;
+    bool waited = false;
     for (int64_t it = blockIdx.x; it < iters; it += gridDim.x) {
         const int64_t v0 = it * kPerIter + threadIdx.x;
         uint32_t r[U][VW];
@@ -81,6 +87,10 @@ __global__ void __launch_bounds__(kThreads) affine_vec(const float *a, float *ou
 #pragma unroll
                 for (int e = 0; e < 8; ++e) r[u][e] = t.v[e];
             }
+        }
+        if (!waited) {  // the loads above may run ahead of the previous kernel, the stores may not
+            pdl_wait();
+            waited = true;
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -98,6 +108,7 @@ __global__ void __launch_bounds__(kThreads) affine_vec(const float *a, float *ou
             }
         }
     }
+    if (!waited) pdl_wait();
     // vectors left over after the whole iterations: one per thread
     const int64_t stride = (int64_t)gridDim.x * kThreads;
     for (int64_t v = iters * kPerIter + (int64_t)blockIdx.x * kThreads + threadIdx.x; v < nvec; v += stride) {
@@ -131,8 +142,10 @@ constexpr int kUnroll8 = 2;
 
 using namespace libtm;
 
-extern "C" tm_status tm_affine(const float *a, float *out, int64_t n, tm_variant variant, tm_stream_t stream)
+extern "C" tm_status tm_affine(const float *a, float *out, int64_t n, tm_variant variant_pdl, tm_stream_t stream)
 {
+    const bool pdl = ((uint32_t)variant_pdl & TM_PDL) != 0;
+    const tm_variant variant = (tm_variant)((uint32_t)variant_pdl & ~TM_PDL);
     if (n < 0) return TM_ERR_INVALID_ARG;
     if (n > 0 && (a == nullptr || out == nullptr)) return TM_ERR_INVALID_ARG;
     if (variant != TM_VAR_AUTO && variant != TM_VAR_SCALAR && variant != TM_VAR_VEC_UNALIGNED &&
@@ -178,22 +191,21 @@ extern "C" tm_status tm_affine(const float *a, float *out, int64_t n, tm_variant
     if (variant == TM_VAR_SCALAR || (variant == TM_VAR_AUTO && vw == 0)) {
         int64_t grid = (n + kThreads - 1) / kThreads;
         if (grid > INT32_MAX) grid = INT32_MAX;
-        affine_scalar<<<(unsigned)grid, kThreads, 0, s>>>(a, out, n);
-        return launch_status();
+        void *args[] = {(void *)&a, (void *)&out, (void *)&n};
+        return launch_kernel((const void *)affine_scalar, dim3((unsigned)grid), dim3(kThreads), args, 0, s, pdl);
     }
     if (variant == TM_VAR_VEC_UNALIGNED) {
         int64_t grid = (n / 4 + kThreads - 1) / kThreads;
         if (grid < 1) grid = 1;
         if (grid > INT32_MAX) grid = INT32_MAX;
-        affine_vec_unaligned<<<(unsigned)grid, kThreads, 0, s>>>(a, out, n);
-        return launch_status();
+        void *args[] = {(void *)&a, (void *)&out, (void *)&n};
+        return launch_kernel((const void *)affine_vec_unaligned, dim3((unsigned)grid), dim3(kThreads), args, 0, s,
+                             pdl);
     }
     const int64_t nvec = (n - head) / vw;
     const int64_t chunks = nvec / (kThreads * (vw == 4 ? kUnroll4 : kUnroll8));
     const unsigned grid = flat_grid(chunks > 0 ? chunks : (nvec + kThreads - 1) / kThreads);
-    if (vw == 4)
-        affine_vec<4, kUnroll4><<<grid, kThreads, 0, s>>>(a, out, n, head);
-    else
-        affine_vec<8, kUnroll8><<<grid, kThreads, 0, s>>>(a, out, n, head);
-    return launch_status();
+    const void *k = vw == 4 ? (const void *)affine_vec<4, kUnroll4> : (const void *)affine_vec<8, kUnroll8>;
+    void *args[] = {(void *)&a, (void *)&out, (void *)&n, (void *)&head};
+    return launch_kernel(k, dim3(grid), dim3(kThreads), args, 0, s, pdl);
 }

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kNaiveRows) colsum_naive(const float *__restri
             float t = warp_sums[0];
 #pragma unroll
             for (int w = 1; w < kNaiveRows / 32; ++w) t += warp_sums[w];
+            pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
             part[rb * npad + col] = t;
         }
         __syncthreads();
@@ -114,7 +115,8 @@ __global__ void __launch_bounds__(256) colsum_finish(const float *__restrict__ p
                                                      int64_t N, float *__restrict__ c)
 {
     __shared__ float grp[kFinishPG][33];
-    pdl_wait();  // launched as a dependent of the partial-sum pass: its writes first
+    pdl_trigger();  // a dependent next call may launch once every block has started
+    pdl_wait();     // launched as a dependent of the partial-sum pass: its writes first
     const int cx = threadIdx.x & 31, py = threadIdx.x >> 5;
     const int64_t per = (P + kFinishPG - 1) / kFinishPG;
     const int64_t p_lo = py * per;
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
         const bool grid_ok = !VEC || ((a.ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(a.X) & 15) == 0);
         if (!whole || !grid_ok) {
             if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            pdl_wait();
             return;
         }
     }
@@ -213,6 +216,7 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
         for (int e = 0; e < EW; ++e) red[rl][cl * EW + e] = acc[e];
         __syncthreads();
         if (rl == 0 && col_in) {
+            pdl_wait();  // the loads above may run ahead of the previous kernel, the stores may not
 #pragma unroll
             for (int e = 0; e < EW; ++e) {
                 float t = red[0][cl * EW + e];
@@ -242,6 +246,7 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, floa
     __shared__ float red[RL][TN];
     __shared__ float part[TN];
 
+    pdl_trigger();
     if constexpr (ALIGNED) {
         // a pure function of the arguments: every CTA of every cluster returns
         // together, so no CTA is left waiting at a cluster barrier
@@ -249,6 +254,7 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, floa
         const bool grid_ok = !VEC || ((a.ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(a.X) & 15) == 0);
         if (!whole || !grid_ok) {
             if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            pdl_wait();
             return;
         }
     }
@@ -313,6 +319,7 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, floa
 #pragma unroll 4
         for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
         const int64_t col = s * TN + threadIdx.x;
+        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
         if (col < a.N) c[col] = t;
     }
     cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
@@ -338,10 +345,14 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
         const bool whole = (a.M % TM == 0) && (a.N % TN == 0);
         if (!whole) {
             if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, kStatusBrokenPromise);
+            pdl_wait();
             return;
         }
     }
-    if (blockIdx.x >= a.units) return;
+    if (blockIdx.x >= a.units) {
+        pdl_wait();
+        return;
+    }
     const int tid = threadIdx.x;
     const int cl = tid % CL, rl = tid / CL;
     const int64_t my_units = (a.units - blockIdx.x + gridDim.x - 1) / gridDim.x;
@@ -416,6 +427,7 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
             __syncthreads();
             const int64_t j = s * TN + cl * 4;
             if (rl == 0 && j < a.N) {
+                pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     float tot = red[0][cl * 4 + e];
@@ -467,7 +479,7 @@ bool pow2_in(int v, int lo, int hi)
 // each block two tiles at 8192 x 8192 (32 x 128) and a TMA round trip per
 // 32 KB: 52.0 us kernel time (ncu) against 46.9 us persistent.
 template <int TM, int TN>
-tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, int sms, cudaStream_t s)
+tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, int sms, cudaStream_t s, bool pdl)
 {
     const void *k = aligned ? (const void *)colsum_staged<TM, TN, true> : (const void *)colsum_staged<TM, TN, false>;
     const int max_stages = staged_stages(TM, TN);
@@ -491,18 +503,14 @@ tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a
     });
     if (!attr_ok) return TM_ERR_CUDA;
     void *args[] = {const_cast<CUtensorMap *>(&map), const_cast<ColArgs *>(&a), &stages};
-    if (cudaLaunchKernel(k, dim3(flat_grid(grid)), dim3(kThreads), args, smem, s) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_kernel(k, dim3(flat_grid(grid)), dim3(kThreads), args, smem, s, pdl);
 }
 
 tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a, int sms,
-                        cudaStream_t s)
+                        cudaStream_t s, bool pdl)
 {
 #define TM_STAGED(tm_, tn_) \
-    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, sms, s);
+    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, sms, s, pdl);
     TM_STAGED(16, 64)
     TM_STAGED(32, 64)
     TM_STAGED(64, 64)
@@ -519,17 +527,13 @@ tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, co
 }
 
 template <int TN>
-tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, cudaStream_t s)
+tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, cudaStream_t s, bool pdl)
 {
     const void *k;
     if (vec) k = aligned ? (const void *)colsum_regdirect<TN, true, true> : (const void *)colsum_regdirect<TN, true, false>;
     else k = aligned ? (const void *)colsum_regdirect<TN, false, true> : (const void *)colsum_regdirect<TN, false, false>;
     void *args[] = {const_cast<ColArgs *>(&a)};
-    if (cudaLaunchKernel(k, dim3(flat_grid(a.units)), dim3(kThreads), args, 0, s) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_kernel(k, dim3(flat_grid(a.units)), dim3(kThreads), args, 0, s, pdl);
 }
 
 // The finish runs as a programmatic dependent of the partial-sum pass, which
@@ -545,7 +549,7 @@ tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, f
 // are launched with the cluster-dimension attribute; 16 needs the
 // non-portable cluster size).
 template <int TN, int CS>
-tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, cudaStream_t s)
+tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, cudaStream_t s, bool pdl)
 {
     const void *k;
     if (vec) k = aligned ? (const void *)colsum_cluster<TN, CS, true, true> : (const void *)colsum_cluster<TN, CS, true, false>;
@@ -565,23 +569,8 @@ tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, c
     }
     int64_t rows_per_cta = (a.M + CS - 1) / CS;
     const int64_t strips = (a.N + TN - 1) / TN;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(strips * CS));
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     void *args[] = {const_cast<ColArgs *>(&a), &c, &rows_per_cta};
-    if (cudaLaunchKernelExC(&cfg, k, args) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, 0, s, pdl, CS);
 }
 
 constexpr int kClusterCTAs = 8;  // CTAs per strip in the cluster variant
@@ -613,7 +602,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
 {
     if (!valid2d(X, ldx, M, N)) return TM_ERR_INVALID_ARG;
     if (N > 0 && c == nullptr) return TM_ERR_INVALID_ARG;
-    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC | TM_PDL)) return TM_ERR_INVALID_ARG;
     if (variant != TM_VAR_AUTO && variant != TM_VAR_NAIVE && variant != TM_VAR_STAGED &&
         variant != TM_VAR_REGDIRECT && variant != TM_VAR_CLUSTER)
         return TM_ERR_INVALID_ARG;
@@ -668,6 +657,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     tm_status st = device_info(&dev);
     if (st != TM_OK) return st;
     cudaStream_t s = as_stream(stream);
+    const bool pdl = (flags & TM_PDL) != 0;
     float *part = static_cast<float *>(workspace);
 
     // pick the variant (the TMA encoder comes from the driver on first use)
@@ -684,9 +674,11 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
 
     if (M > 0) {
         if (v == Variant::Naive) {
-            const int64_t programs = P * N;
-            colsum_naive<<<flat_grid(programs), kNaiveRows, 0, s>>>(X, ldx, M, N, part, npad, programs);
-            st = launch_status();
+            int64_t programs = P * N;
+            void *args[] = {(void *)&X, (void *)&ldx, (void *)&M, (void *)&N, (void *)&part, (void *)&npad,
+                            (void *)&programs};
+            st = launch_kernel((const void *)colsum_naive, dim3(flat_grid(programs)), dim3(kNaiveRows), args, 0, s,
+                               pdl);
         } else {
             ColArgs a;
             a.X = X;
@@ -703,9 +695,9 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
             a.status = dev->status;
             if (v == Variant::Cluster) {
                 switch (TN) {
-                case 64: st = launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, c, s); break;
-                case 128: st = launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, c, s); break;
-                default: st = launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, c, s); break;
+                case 64: st = launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, c, s, pdl); break;
+                case 128: st = launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, c, s, pdl); break;
+                default: st = launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, c, s, pdl); break;
                 }
                 return st;  // c is written by the cluster pass itself
             } else if (v == Variant::Staged) {
@@ -718,12 +710,12 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                     return TM_ERR_CUDA;
-                st = launch_staged(TM, TN, aligned, map, a, dev->sms, s);
+                st = launch_staged(TM, TN, aligned, map, a, dev->sms, s, pdl);
             } else {
                 switch (TN) {
-                case 64: st = launch_regdirect_t<64>(vec, aligned, a, s); break;
-                case 128: st = launch_regdirect_t<128>(vec, aligned, a, s); break;
-                default: st = launch_regdirect_t<256>(vec, aligned, a, s); break;
+                case 64: st = launch_regdirect_t<64>(vec, aligned, a, s, pdl); break;
+                case 128: st = launch_regdirect_t<128>(vec, aligned, a, s, pdl); break;
+                default: st = launch_regdirect_t<256>(vec, aligned, a, s, pdl); break;
                 }
             }
         }

@@ -168,6 +168,12 @@ __device__ __forceinline__ void cluster_sync()
 // launch begin once every block of this grid has issued it or exited.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The library's streaming kernels all follow one rule so that any of them may
+// be launched as a dependent (TM_PDL): pdl_trigger() at entry, pdl_wait() in
+// every thread before its first global store, and pdl_wait() before exit in a
+// thread that stored nothing.  Loads of the inputs may therefore run ahead of
+// the previous kernel; no write may, and no grid completes before the grid it
+// depends on, which keeps a chain of dependent launches in stream order.
 __device__ __forceinline__ uint32_t as_u(float f) { return __float_as_uint(f); }
 
 // ---------------------------------------------------------------- tile walk

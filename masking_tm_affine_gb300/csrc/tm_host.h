@@ -49,27 +49,45 @@ inline tm_status launch_status()
 
 inline cudaStream_t as_stream(tm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Launch `kernel` as a programmatic dependent of the previous kernel in the
-// stream (see pdl_wait in tm_device.cuh): its blocks may start while that
-// kernel drains; the kernel must pdl_wait() before reading what it produced.
-inline tm_status launch_dependent(const void *kernel, dim3 grid, dim3 block, void **args, size_t smem,
-                                  cudaStream_t s)
+// Launch `kernel`; with pdl, as a programmatic dependent of the previous
+// kernel in the stream (see pdl_wait in tm_device.cuh): its blocks may start
+// while that kernel drains, and each must pdl_wait() before it reads what that
+// kernel produced or writes anything.  cluster > 1 adds a cluster dimension.
+inline tm_status launch_kernel(const void *kernel, dim3 grid, dim3 block, void **args, size_t smem, cudaStream_t s,
+                               bool pdl, unsigned cluster = 1)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     if (cudaLaunchKernelExC(&cfg, kernel, args) != cudaSuccess) {
         cudaGetLastError();
         return TM_ERR_CUDA;
     }
     return TM_OK;
+}
+
+inline tm_status launch_dependent(const void *kernel, dim3 grid, dim3 block, void **args, size_t smem,
+                                  cudaStream_t s)
+{
+    return launch_kernel(kernel, grid, block, args, smem, s, true);
 }
 
 inline bool aligned_to(const void *p, uintptr_t bytes)

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
     constexpr int UB = U < 4 ? U : 4;                  // accesses in flight per batch
     static_assert(A % kThreads == 0 && U % UB == 0, "tile shape does not fit the block");
 
+    pdl_trigger();
     if constexpr (P == Path::Aligned) {
         // The promise, checked once at entry ("@aligned", "When the promise is
         // broken").  A pure function of the arguments, so every block takes the
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
         if (!whole || !grid_ok) {
             if (blockIdx.x == 0 && threadIdx.x == 0)
                 atomicOr(p.status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            pdl_wait();
             return;
         }
     }
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
                     for (int e = 0; e < EW; ++e) val[u].v[e] = 0u;  // a masked load reads 0
                 }
             }
+            pdl_wait();  // the loads above may run ahead of the previous kernel, the stores may not
 #pragma unroll
             for (int u = 0; u < UB; ++u) {
                 if (!live[u]) continue;                              // a masked store is skipped
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(kThreads) map2d_kernel(const Map2dArgs p)
             }
         }
     }
+    pdl_wait();
 }
 
 // Every element offset the ragged walk dereferences fits 31 bits: the last
@@ -229,7 +233,7 @@ bool offsets_fit_i32(const Map2dArgs &a)
 }
 
 template <int TM, int TN, Op OP>
-tm_status launch_tile(Path path, int ew, const Map2dArgs &a, cudaStream_t s)
+tm_status launch_tile(Path path, int ew, const Map2dArgs &a, cudaStream_t s, bool pdl)
 {
     const void *k = nullptr;
     if (path == Path::Aligned && ew == 8) k = (const void *)map2d_kernel<TM, TN, OP, Path::Aligned, 8>;
@@ -245,18 +249,14 @@ tm_status launch_tile(Path path, int ew, const Map2dArgs &a, cudaStream_t s)
     const int64_t G = V >= 4 * kThreads ? 1 : (4 * kThreads) / V;
     const int64_t groups = ((int64_t)a.ntiles + G - 1) / G;
     void *args[] = {const_cast<Map2dArgs *>(&a)};
-    if (cudaLaunchKernel(k, dim3(flat_grid(groups)), dim3(kThreads), args, 0, s) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_kernel(k, dim3(flat_grid(groups)), dim3(kThreads), args, 0, s, pdl);
 }
 
 template <Op OP>
-tm_status dispatch(int TM, int TN, Path path, int ew, const Map2dArgs &a, cudaStream_t s)
+tm_status dispatch(int TM, int TN, Path path, int ew, const Map2dArgs &a, cudaStream_t s, bool pdl)
 {
 #define TM_TILE(tm_, tn_) \
-    if (TM == tm_ && TN == tn_) return launch_tile<tm_, tn_, OP>(path, ew, a, s);
+    if (TM == tm_ && TN == tn_) return launch_tile<tm_, tn_, OP>(path, ew, a, s, pdl);
     TM_TILE(8, 8)
     TM_TILE(16, 16)
     TM_TILE(32, 32)
@@ -302,7 +302,7 @@ tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64
         }
         if (ch->layout == 1) params16 = true;  // one scalar parameter per row: no vector loads
     }
-    if (!flags_ok(flags, TM_ALIGNED | kPathBits)) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | kPathBits | TM_PDL)) return TM_ERR_INVALID_ARG;
     if (TM <= 0 || TN <= 0 || !tile_supported(TM, TN)) return TM_ERR_UNSUPPORTED_TILE;
     if (!overlap_ok(X, ldx, Y, ldy, M, N)) return TM_ERR_INVALID_ARG;
     if (M > 0 && N > 0 && (!aligned_to(X, 4) || !aligned_to(Y, 4))) return TM_ERR_MISALIGNED;
@@ -361,9 +361,10 @@ tm_status map2d(Op op, const float *X, int64_t ldx, float *Y, int64_t ldy, int64
     a.C = op == Op::Channel ? (uint32_t)ch->C : 1u;
     a.div_C = make_fastdiv(a.C);
     cudaStream_t s = as_stream(stream);
-    if (op == Op::Channel) return dispatch<Op::Channel>(TM, TN, path, ew, a, s);
-    return op == Op::Scale ? dispatch<Op::Scale>(TM, TN, path, ew, a, s)
-                           : dispatch<Op::Copy>(TM, TN, path, ew, a, s);
+    const bool pdl = (flags & TM_PDL) != 0;
+    if (op == Op::Channel) return dispatch<Op::Channel>(TM, TN, path, ew, a, s, pdl);
+    return op == Op::Scale ? dispatch<Op::Scale>(TM, TN, path, ew, a, s, pdl)
+                           : dispatch<Op::Copy>(TM, TN, path, ew, a, s, pdl);
 }
 
 }  // namespace
@@ -434,7 +435,7 @@ extern "C" tm_status tm_pad2d(const float *A, int64_t lda, int64_t M, int64_t N,
     a.div_C = make_fastdiv(1u);
     a.Msrc = M;
     a.Nsrc = N;
-    return launch_tile<TM, TN, Op::Pad>(vec ? Path::RaggedVec : Path::Scalar, 4, a, as_stream(stream));
+    return launch_tile<TM, TN, Op::Pad>(vec ? Path::RaggedVec : Path::Scalar, 4, a, as_stream(stream), false);
 }
 
 extern "C" int64_t tm_padded_extent(int64_t extent, const int32_t *tiles, int32_t ntiles)

@@ -31,12 +31,14 @@ __global__ void __launch_bounds__(kThreads) rowsum_kernel(const float *__restric
     constexpr int W = L > 32 ? L / 32 : 1;  // warps per row
     __shared__ float part[TM][W];
 
+    pdl_trigger();
     if constexpr (ALIGNED) {
         const bool whole = (M % TM == 0) && (N % TN == 0);
         const bool grid_ok = !VEC || ((ldx % 4 == 0) && (reinterpret_cast<uintptr_t>(X) & 15) == 0);
         if (!whole || !grid_ok) {
             if (blockIdx.x == 0 && threadIdx.x == 0)
                 atomicOr(status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            pdl_wait();
             return;
         }
     }
@@ -110,23 +112,22 @@ __global__ void __launch_bounds__(kThreads) rowsum_kernel(const float *__restric
             }
             __syncthreads();
         }
-        if (ln == 0 && live) r[row] = s;
+        if (ln == 0 && live) {
+            pdl_wait();  // the loads above may run ahead of the previous kernel, the store may not
+            r[row] = s;
+        }
     }
 }
 
 template <int TM>
 tm_status launch(bool vec, bool aligned, const float *X, int64_t ldx, int64_t M, int64_t N, float *r, int TN,
-                 unsigned *status, cudaStream_t s)
+                 unsigned *status, cudaStream_t s, bool pdl)
 {
     const void *k;
     if (vec) k = aligned ? (const void *)rowsum_kernel<TM, true, true> : (const void *)rowsum_kernel<TM, true, false>;
     else k = aligned ? (const void *)rowsum_kernel<TM, false, true> : (const void *)rowsum_kernel<TM, false, false>;
     void *args[] = {(void *)&X, (void *)&ldx, (void *)&M, (void *)&N, (void *)&r, (void *)&TN, (void *)&status};
-    if (cudaLaunchKernel(k, dim3(flat_grid((M + TM - 1) / TM)), dim3(kThreads), args, 0, s) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_kernel(k, dim3(flat_grid((M + TM - 1) / TM)), dim3(kThreads), args, 0, s, pdl);
 }
 
 bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
@@ -141,7 +142,7 @@ extern "C" tm_status tm_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N
 {
     if (!valid2d(X, ldx, M, N)) return TM_ERR_INVALID_ARG;
     if (M > 0 && r == nullptr) return TM_ERR_INVALID_ARG;
-    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC | TM_PDL)) return TM_ERR_INVALID_ARG;
     if (!pow2_in(TM, 1, 32) || !pow2_in(TN, 16, 4096)) return TM_ERR_UNSUPPORTED_TILE;
     if (M > 0 && !aligned_to(r, 4)) return TM_ERR_MISALIGNED;
     if (M > 0 && N > 0 && !aligned_to(X, 4)) return TM_ERR_MISALIGNED;
@@ -172,12 +173,13 @@ extern "C" tm_status tm_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N
     tm_status st = device_info(&dev);
     if (st != TM_OK) return st;
     cudaStream_t s = as_stream(stream);
+    const bool pdl = (flags & TM_PDL) != 0;
     switch (TM) {
-    case 1: return launch<1>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
-    case 2: return launch<2>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
-    case 4: return launch<4>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
-    case 8: return launch<8>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
-    case 16: return launch<16>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
-    default: return launch<32>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s);
+    case 1: return launch<1>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s, pdl);
+    case 2: return launch<2>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s, pdl);
+    case 4: return launch<4>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s, pdl);
+    case 8: return launch<8>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s, pdl);
+    case 16: return launch<16>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s, pdl);
+    default: return launch<32>(vec, aligned, X, ldx, M, N, r, TN, dev->status, s, pdl);
     }
 }

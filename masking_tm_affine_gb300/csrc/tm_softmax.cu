@@ -75,12 +75,14 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
     constexpr int W = L > 32 ? L / 32 : 1;
     __shared__ float part_m[BR][W], part_l[BR][W];
 
+    pdl_trigger();
     if constexpr (ALIGNED) {
         const bool whole = (M % BR == 0) && (N % BC == 0);
         const bool grid_ok = !VEC || ((lds % 4 == 0) && (reinterpret_cast<uintptr_t>(S) & 15) == 0);
         if (!whole || !grid_ok) {
             if (blockIdx.x == 0 && threadIdx.x == 0)
                 atomicOr(status, whole ? kStatusMisaligned : kStatusBrokenPromise);
+            pdl_wait();
             return;
         }
     }
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
             __syncthreads();
         }
         if (ln == 0 && live) {
+            pdl_wait();  // the loads above may run ahead of the previous kernel, the stores may not
             m_out[row] = mx;
             l_out[row] = sum;
         }
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
 
 template <int BR>
 tm_status launch(bool vec, bool aligned, const float *S, int64_t lds, int64_t M, int64_t N, float *m, float *l,
-                 int BC, int fill_zero, unsigned *status, cudaStream_t s)
+                 int BC, int fill_zero, unsigned *status, cudaStream_t s, bool pdl)
 {
     const void *k;
     if (vec)
@@ -185,11 +188,7 @@ tm_status launch(bool vec, bool aligned, const float *S, int64_t lds, int64_t M,
                     : (const void *)softmax_rowstats_kernel<BR, false, false>;
     void *args[] = {(void *)&S, (void *)&lds, (void *)&M, (void *)&N, (void *)&m,
                     (void *)&l, (void *)&BC, (void *)&fill_zero, (void *)&status};
-    if (cudaLaunchKernel(k, dim3(flat_grid((M + BR - 1) / BR)), dim3(kThreads), args, 0, s) != cudaSuccess) {
-        cudaGetLastError();
-        return TM_ERR_CUDA;
-    }
-    return TM_OK;
+    return launch_kernel(k, dim3(flat_grid((M + BR - 1) / BR)), dim3(kThreads), args, 0, s, pdl);
 }
 
 bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
@@ -211,7 +210,7 @@ extern "C" tm_status tm_softmax_rowstats(const float *S, int64_t lds, int64_t M,
     if (!valid2d(S, lds, M, N)) return TM_ERR_INVALID_ARG;
     if (M > 0 && (m == nullptr || l == nullptr)) return TM_ERR_INVALID_ARG;
     if (fill != TM_FILL_NEG_INF && fill != TM_FILL_ZERO) return TM_ERR_INVALID_ARG;
-    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC)) return TM_ERR_INVALID_ARG;
+    if (!flags_ok(flags, TM_ALIGNED | TM_PATH_SCALAR | TM_PATH_VEC | TM_PDL)) return TM_ERR_INVALID_ARG;
     if (!pow2_in(BR, 1, 32) || !pow2_in(BC, 16, 4096)) return TM_ERR_UNSUPPORTED_TILE;
     if (M > 0 && (!aligned_to(m, 4) || !aligned_to(l, 4))) return TM_ERR_MISALIGNED;
     if (M > 0 && N > 0 && !aligned_to(S, 4)) return TM_ERR_MISALIGNED;
@@ -248,12 +247,13 @@ extern "C" tm_status tm_softmax_rowstats(const float *S, int64_t lds, int64_t M,
     if (st != TM_OK) return st;
     cudaStream_t s = as_stream(stream);
     const int fz = fill == TM_FILL_ZERO ? 1 : 0;
+    const bool pdl = (flags & TM_PDL) != 0;
     switch (BR) {
-    case 1: return launch<1>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s);
-    case 2: return launch<2>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s);
-    case 4: return launch<4>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s);
-    case 8: return launch<8>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s);
-    case 16: return launch<16>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s);
-    default: return launch<32>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s);
+    case 1: return launch<1>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s, pdl);
+    case 2: return launch<2>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s, pdl);
+    case 4: return launch<4>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s, pdl);
+    case 8: return launch<8>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s, pdl);
+    case 16: return launch<16>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s, pdl);
+    default: return launch<32>(vec, aligned, S, lds, M, N, m, l, BC, fz, dev->status, s, pdl);
     }
 }

@@ -32,6 +32,7 @@ TM_ALIGNED = 0x1
 TM_PATH_SCALAR = 0x10
 TM_PATH_VEC = 0x20
 TM_PATH_TMA = 0x40
+TM_PDL = 0x200  # overlapped launch; tm_affine takes it OR-ed into the variant
 
 # tm_variant
 TM_VAR_AUTO = 0

@@ -116,6 +116,35 @@ def test_reduction_host_validation(lib):
     assert st("tm_tile_walk_probe", 10, 0, P0, None) == tm.TM_ERR_INVALID_ARG
 
 
+def test_overlap_flag_host_validation(lib):
+    """TM_PDL is accepted wherever flags are (and OR-ed into tm_affine's variant):
+    the other checks still run and decide the status; tm_gemm does not take it."""
+    A, D = tm.TM_ALIGNED, tm.TM_PDL
+    assert st("tm_affine", P0 + 4, P1, 5, tm.TM_VAR_VEC4 | D, None) == tm.TM_ERR_MISALIGNED
+    assert st("tm_affine", P0, P1, 5, 99 | D, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_affine", P0, P1, 5, 0x400, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_affine", P0, P1, 0, tm.TM_VAR_AUTO | D, None) == tm.TM_OK
+    assert st("tm_scale2d", P0, 8192, P1, 8192, 8192, 8100, 1.5, 32, 128, A | D, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_copy2d", P0, 8192, P1, 8192, 8190, 8192, 32, 128, A | D, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_copy2d", P0, 8, P1, 8, 0, 8, 8, 8, D, None) == tm.TM_OK
+    assert st("tm_channel_affine", P0, 256, 8192, 256, None, None, 256, tm.TM_CHANNELS_LAST, P1, 256, 32, 128,
+              D | 0x8, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_channel_affine", P0, 256, 8190, 256, None, None, 256, tm.TM_CHANNELS_LAST, P1, 256, 32, 128,
+              A | D, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_rowsum", P0, 4096, 4096, 4000, P1, 8, 512, A | D, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_rowmax_masked", P0, 1000, 8192, 1000, P1, 8, 64, 0, A | D, None) == tm.TM_ERR_BROKEN_PROMISE
+    assert st("tm_softmax_rowstats", P0, 1000, 8192, 1000, P1, P1 + (1 << 20), 8, 64, 0, A | D, None) \
+        == tm.TM_ERR_BROKEN_PROMISE
+    ws = tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128)
+    assert st("tm_colsum", P0, 4096, 4096, 4096, P1, None, ws, 32, 128, 0, D, None) == tm.TM_ERR_WORKSPACE
+    assert st("tm_colsum", P0, 4096, 4096, 4000, P1, P1 + (1 << 30), ws, 32, 128, 0, A | D, None) \
+        == tm.TM_ERR_BROKEN_PROMISE
+    W = 0x7F0200000000
+    gws = tm.tm_gemm_workspace_bytes(4100, 4100, 1000, 256)
+    assert st("tm_gemm", P0, 1000, P1, 4100, W + (1 << 34), 4100, 4100, 4100, 1000, 1.5, 0.5, 256, 256, 32, D,
+              W, gws, None) == tm.TM_ERR_INVALID_ARG
+
+
 def test_colsum_workspace_plan(lib):
     # one partial row per chunk; NAIVE: one per 256-row program block
     assert tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128, tm.TM_VAR_NAIVE) == 16 * 4096 * 4
