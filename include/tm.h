@@ -130,7 +130,8 @@ int tm_version(void);
  *   a, out   device pointers to n floats (out == a allowed, no other overlap)
  *   n        element count, >= 0
  *   variant  TM_VAR_AUTO (widest access the alignment allows), _SCALAR,
- *            _VEC_UNALIGNED, _VEC4 (a, out 16-byte aligned), _VEC8 (32-byte)
+ *            _VEC_UNALIGNED, _VEC4 (a, out 16-byte aligned), _VEC8 (32-byte);
+ *            may be OR-ed with TM_PDL (an overlapped launch)
  * Errors: INVALID_ARG (n < 0, NULL with n > 0, bad variant, partial overlap),
  *         MISALIGNED (VEC4/VEC8 with misaligned pointers), CUDA.
  */
@@ -143,7 +144,7 @@ tm_status tm_affine(const float *a, float *out, int64_t n, tm_variant variant, t
  * written ("Slicing, bounds and masking", "Masking").
  *   X, ldx   device input [M, ldx]     Y, ldy   device output [M, ldy]
  *   TM, TN   tile: (8,8) (16,16) (32,32) (64,64) (32,128) (128,128)
- *   flags    TM_ALIGNED and/or one TM_PATH_* bit
+ *   flags    TM_ALIGNED and/or one TM_PATH_* bit, and/or TM_PDL
  * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
  */
 tm_status tm_scale2d(const float *X, int64_t ldx, float *Y, int64_t ldy, int64_t M, int64_t N,
@@ -219,7 +220,8 @@ tm_status tm_pad2d(const float *A, int64_t lda, int64_t M, int64_t N, float *B, 
  *   X, ldx   device input [M, ldx]     r   device output, M floats
  *   TM       rows per block: 1, 2, 4, 8, 16, 32
  *   TN       columns per tile: 128, 256, 512, 1024
- *   flags    TM_ALIGNED (no remainder tile and no row mask), TM_PATH_SCALAR, TM_PATH_VEC
+ *   flags    TM_ALIGNED (no remainder tile and no row mask), TM_PATH_SCALAR, TM_PATH_VEC,
+ *            TM_PDL
  * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
  */
 tm_status tm_rowsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *r, int32_t TM,
@@ -251,7 +253,9 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  *               (NAIVE ignores them: its programs are 256 rows x 1 column)
  *   variant     TM_VAR_AUTO (= REGDIRECT, the fastest measured), _NAIVE,
  *               _STAGED, _REGDIRECT, _CLUSTER
- *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR
+ *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR,
+ *               TM_PDL (the first pass overlaps the previous kernel; the
+ *               finish pass of a two-pass variant always overlaps the first)
  * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE,
  *         WORKSPACE, CUDA; a stalled TMA pipeline is reported by tm_check as
  *         TM_ERR_TIMEOUT.
@@ -272,7 +276,7 @@ tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c,
  *   BR       rows per block (one warp per row): 1, 2, 4, 8, 16, 32
  *   BC       columns per tile: 16, 32, 64, 128, 256, 512
  *   flags    TM_ALIGNED (M % BR == 0, N % BC == 0: no remainder, no row mask),
- *            TM_PATH_SCALAR, TM_PATH_VEC
+ *            TM_PATH_SCALAR, TM_PATH_VEC, TM_PDL
  * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE, CUDA.
  */
 tm_status tm_rowmax_masked(const float *S, int64_t lds, int64_t M, int64_t N, float *m, int32_t BR,

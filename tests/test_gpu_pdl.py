@@ -199,3 +199,20 @@ def test_back_to_back_column_sums_share_a_workspace(cuda, oracle, variant):
     for k in range(3):
         for c in (cs[k], cs[3 + k]):
             assert sums_close(host(c), wants[k], wants[k]), (variant, k)
+
+
+def test_overlapped_launch_on_the_default_stream(cuda, oracle):
+    """TM_PDL on the legacy default stream (a NULL stream handle), after another kernel there."""
+    x = synth.workload_input("ragged_4100")
+    M, N = x.shape
+    X = dev(x)
+    Y, B = torch.empty_like(X), torch.empty_like(X)
+    torch.cuda.synchronize()
+    tm.tm_copy2d(X, N, B, N, M, N, 64, 64, 0, 0)
+    tm.tm_scale2d(X, N, Y, N, M, N, 1.5, 64, 64, P, 0)
+    tm.tm_check(0)
+    torch.cuda.synchronize()
+    want = np.empty_like(x)
+    oracle.scale2d(x, N, want, N, M, N, 1.5)
+    assert same_f32(host(Y), want)
+    assert np.array_equal(host(B).view(np.uint32), x.view(np.uint32))
