@@ -216,3 +216,35 @@ def test_overlapped_launch_on_the_default_stream(cuda, oracle):
     oracle.scale2d(x, N, want, N, M, N, 1.5)
     assert same_f32(host(Y), want)
     assert np.array_equal(host(B).view(np.uint32), x.view(np.uint32))
+
+
+def test_overlapped_step_replays_from_a_cuda_graph(cuda, oracle):
+    """The bench step (six overlapped calls) captured once into a CUDA graph,
+    whose dependent launches become programmatic edges, and replayed: once on
+    the batch, once after a new batch was copied into the same X."""
+    import bench
+    dev_ = torch.device("cuda", 0)
+    x = synth.workload_input(bench.WORKLOAD)
+    bufs, ws_bytes = bench.make_buffers(tm, x, dev_)
+    stream = torch.cuda.Stream(device=dev_)
+    step = bench.make_step(tm, bufs, ws_bytes, stream)
+    with torch.cuda.stream(stream):
+        for _, launch in step:          # once outside the graph (first-use set-up happens here)
+            launch()
+    tm.tm_check(stream.cuda_stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _, launch in step:
+            launch()
+    for k in ("A1", "Y", "B", "r", "c", "m"):
+        bufs[k].fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    tm.tm_check()
+    bench.verify_step(bufs, x, oracle)
+    x2 = synth.normal((bench.M, bench.N), seed=33)
+    bufs["X"].copy_(torch.from_numpy(x2.reshape(-1)))
+    g.replay()
+    torch.cuda.synchronize()
+    tm.tm_check()
+    bench.verify_step(bufs, x2, oracle)
