@@ -339,7 +339,12 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
  * about 3x the speed).  A first pass writes the split operands, K-major and
  * zero-padded to whole tiles, into the caller's workspace; the zero padding
  * is the masked remainder tile's fill, so the tensor-core loop itself runs
- * over whole tiles only.  beta == 0 does not read C (NaN in C stays out).
+ * over whole tiles only.  When the tiles fill at most half of the last round
+ * of CTAs (pairs) and K is long enough, each of that round's tiles is cut
+ * along K into parts run side by side (split-K): the later parts go to the
+ * workspace and the CTA that ran the first part adds them in K order before
+ * the output, so results stay deterministic.  beta == 0 does not read C (NaN
+ * in C stays out).
  * K == 0 gives C = beta * C.
  *   A, lda   device input [M, lda]    B, ldb   device input [K, ldb]
  *   C, ldc   device in/out [M, ldc]; C must not overlap A, B or the workspace
@@ -356,12 +361,14 @@ tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, f
  *   outside [M, N] (the ld gap included) is written.
  *   workspace, ws_bytes   device scratch of at least
  *            tm_gemm_workspace_bytes(M, N, K, TN) bytes, 1024-byte aligned,
- *            overlapping no operand; contents on entry do not matter.  It is in
- *            use until the call's kernels finish on `stream`: calls that may
- *            run at the same time need separate workspaces.
+ *            overlapping no operand; contents on entry do not matter.  It holds
+ *            the split operands and the split-K partial tiles, and is in use
+ *            until the call's kernels finish on `stream`: calls that may run
+ *            at the same time need separate workspaces.
  * Accuracy: |C - exact| <= (3*2^-22 + 3*K*2^-23) * |alpha| * sum_k |a_ik||b_kj|
  *   + 2^-23 * (|alpha * (A B)_ij| + |beta c_ij|) (3xTF32; tensor-core
- *   accumulation is taken as fp32 with truncation).  Integer-valued inputs
+ *   accumulation is taken as fp32 with truncation, one rounding per k, which
+ *   also covers the few additions of split-K parts).  Integer-valued inputs
  *   whose partial sums stay below 2^24 give exact results.
  * Errors: INVALID_ARG (extents, NULL, ld, overlap, unknown flag, a padded
  *   extent or the tile count beyond 2^31 - 1), UNSUPPORTED_TILE, MISALIGNED

@@ -61,6 +61,8 @@ struct SplitArgs {
     int64_t lda, ldb, M, N, K, Mp, Np, Kp;
     float *ahi, *alo, *bhi, *blo;
     unsigned blocks_a, blocks_b;
+    unsigned *flags;  // the gemm's split-K flags, zeroed here (the gemm starts after this pass)
+    int nflags;
 };
 
 __device__ __forceinline__ void split_store(float *hi, float *lo, int64_t at, float x)
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(256) split_operands(const SplitArgs a)
 {
     __shared__ float t[32][33];
     pdl_trigger();  // the gemm's prologue may start once every block has started
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < a.nflags; i += blockDim.x) a.flags[i] = 0u;
     if (blockIdx.x < a.blocks_a) {
         for (int64_t i = blockIdx.x; i < a.Mp; i += a.blocks_a)
             for (int64_t k = threadIdx.x; k < a.Kp; k += blockDim.x) {
@@ -210,6 +214,54 @@ struct GemmArgs {
     int ntiles;   // tiles_m * tiles along N
     int vec_c;    // C base 16-byte aligned, ldc % 4 == 0 and N % 4 == 0: the epilogue moves C by TMA
     unsigned *status;
+    // split-K of the last round: tiles [0, dp_tiles) run whole, round-robin
+    // over the units; each later tile is cut along K into sk_split equal
+    // parts, part q of tile dp_tiles + j run by unit j * sk_split + q, all
+    // parts at the same time (0: no split)
+    int dp_tiles;
+    int sk_split;
+    float *part;      // a unit's partial accumulator: rows [unit * tile rows, + tile rows) x BN
+    unsigned *flags;  // per unit: epilogue warps that have written its partial
+};
+
+constexpr int kMaxSms = 256;     // split-K partial rows: at most this many 128-row accumulators
+constexpr int kSkMinSaved = 48;  // split-K only when it takes this many K stages off the critical path
+
+// The work of one unit (CTA or CTA pair), in order: its data-parallel tiles
+// (every units-th tile from its own index), then its part of a split tile, as
+// items [kb, ke) of one tile.  Producer, MMA issuer and epilogues all walk
+// the same sequence.  Part 0 finishes the tile: it adds the other parts,
+// written by the next sk_split - 1 units, in K order.
+struct Items {
+    int next_dp, step, dp_tiles, KT, sk_tile, sk_kb, sk_ke;
+    bool sk_left;
+    __device__ Items(const GemmArgs &g, int unit, int units)
+        : next_dp(unit), step(units), dp_tiles(g.dp_tiles), KT(g.KT), sk_tile(0), sk_kb(0), sk_ke(0),
+          sk_left(g.sk_split > 0 && unit < (g.ntiles - g.dp_tiles) * g.sk_split)
+    {
+        if (sk_left) {
+            const int q = unit % g.sk_split;
+            sk_tile = g.dp_tiles + unit / g.sk_split;
+            sk_kb = q * g.KT / g.sk_split;
+            sk_ke = (q + 1) * g.KT / g.sk_split;
+        }
+    }
+    __device__ bool next(int &tile, int &kb, int &ke)
+    {
+        if (next_dp < dp_tiles) {
+            tile = next_dp;
+            kb = 0;
+            ke = KT;
+            next_dp += step;
+            return true;
+        }
+        if (!sk_left) return false;
+        sk_left = false;
+        tile = sk_tile;
+        kb = sk_kb;
+        ke = sk_ke;
+        return true;
+    }
 };
 
 template <int BN, int BK, bool THREE>
@@ -284,6 +336,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Stream-K partials: written and read at L2 (other SMs produce and consume
+// them), published with a release add and observed with an acquire load.
+__device__ __forceinline__ void st_cg_v4(float *p, const u32x4 &x)
+{
+    asm volatile("st.global.cg.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(x.v[0]), "r"(x.v[1]), "r"(x.v[2]),
+                 "r"(x.v[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ u32x4 ld_cg_v4(const float *p)
+{
+    u32x4 r;
+    asm volatile("ld.global.cg.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add_u32(unsigned *p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void tma_store(const CUtensorMap *map, int x, int y, uint32_t src)
@@ -369,11 +452,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // ---------------- TMA producer: this CTA's operand tiles of every K stage
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = unit; tile < g.ntiles && ok; tile += units) {
+            Items items(g, unit, units);
+            int tile, kb, ke;
+            while (ok && items.next(tile, kb, ke)) {
                 int m0, n0;
                 tile_coords(tile, g.tiles_m, tiles_n, TMR, BN, m0, n0);
                 const int am = m0 + (int)rank * GBM, bn = n0 + (int)rank * BH;
-                for (int kt = 0; kt < g.KT; ++kt, ++it) {
+                for (int kt = kb; kt < ke; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
                     if (it >= STAGES && !mbar_wait_bounded(smem_u32(&s.empty[st]), ((it / STAGES) - 1) & 1u)) {
                         gemm_fail(&s.abort, g.status);
@@ -428,8 +513,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             constexpr uint32_t id = idesc_tf32(TMR, BN);
             uint32_t it = 0;
             bool ok = true;
-            int t = 0;
-            for (int tile = unit; tile < g.ntiles && ok; tile += units, ++t) {
+            Items items(g, unit, units);
+            int tile, kb, ke;
+            for (int t = 0; ok && items.next(tile, kb, ke); ++t) {
                 const uint32_t ab = (uint32_t)t & 1u;
                 if (t >= 2 && !mbar_wait_bounded(smem_u32(&s.acc_empty[ab]), ((uint32_t)(t / 2) - 1) & 1u)) {
                     gemm_fail(&s.abort, g.status);
@@ -437,7 +523,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t d = tmem + ab * BN;
-                for (int kt = 0; kt < g.KT; ++kt, ++it) {
+                for (int kt = kb; kt < ke; ++kt, ++it) {
                     const uint32_t st = it % STAGES;
                     if (!mbar_wait_bounded(smem_u32(&s.full[st]), (it / STAGES) & 1u) || gemm_aborted(&s.abort)) {
                         if (!gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
@@ -450,7 +536,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 8; ++k) {
                         const uint32_t off = (uint32_t)k * 32;  // 8 tf32 = 32 bytes inside the swizzled row
-                        umma_tf32<PAIR>(d, smem_desc<BK>(ahi + off), smem_desc<BK>(bhi + off), id, (kt | k) != 0);
+                        umma_tf32<PAIR>(d, smem_desc<BK>(ahi + off), smem_desc<BK>(bhi + off), id,
+                                        (kt != kb || k != 0) ? 1u : 0u);  // the item's first MMA overwrites
                         if (THREE) {
                             umma_tf32<PAIR>(d, smem_desc<BK>(ahi + off), smem_desc<BK>(blo + off), id, 1u);
                             umma_tf32<PAIR>(d, smem_desc<BK>(alo + off), smem_desc<BK>(bhi + off), id, 1u);
@@ -472,9 +559,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t acc_empty1 = PAIR ? cluster_addr(smem_u32(&s.acc_empty[1]), 0) : smem_u32(&s.acc_empty[1]);
         uint32_t cpar = 0;        // bit j: parity of the next completion of cbar[eg][j]
         uint32_t loads_out = 0;   // bit j: a load into cbuf[eg][j] is in flight
-        int t = 0;
-        for (int tile = unit; tile < g.ntiles; tile += units, ++t) {
+        constexpr unsigned kEpiWarps = PAIR ? 8u : 4u;  // epilogue warps of a unit: a partial's arrivals
+        Items items(g, unit, units);
+        int tile, kb, ke;
+        for (int t = 0; items.next(tile, kb, ke); ++t) {
             const uint32_t ab = (uint32_t)t & 1u;
+            const bool contrib = kb != 0;              // a later part of a tile another unit finishes
+            const bool finish = kb == 0 && ke < g.KT;  // this unit finishes the tile with the later parts
+            const int last = unit + g.sk_split;        // (finish) the later parts' units: unit + 1 .. last - 1
+            // Unit u's partial accumulator is laid out as this thread sees it: for
+            // each CTA rank, epilogue warp and 32-column chunk c, eight 512-byte
+            // pieces, piece j holding columns c + 4j .. c + 4j + 3 of the warp's
+            // 32 rows, lane after lane -- every warp access is 512 contiguous bytes.
+            auto part_chunk = [&](int u, int c) {
+                return g.part + ((((int64_t)u * (TMR / GBM) + rank) * 4 + eg) * (BN / 32) + c / 32) * 1024 + lane * 4;
+            };
+            auto add4 = [](uint32_t(&r)[32], const u32x4 (&v)[8]) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) r[4 * j + e] = as_u(as_f(r[4 * j + e]) + as_f(v[j].v[e]));
+            };
+            auto load_chunk = [&](int u, int c, u32x4 (&v)[8]) {
+                const float *q = part_chunk(u, c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = ld_cg_v4(q + 128 * j);
+            };
+            // add the partials of the units after this one (their stages follow
+            // in K order); from the second one on when the first is prefetched
+            auto add_partials = [&](uint32_t(&r)[32], int c, int first) {
+                for (int u2 = first; u2 < last; ++u2) {
+                    u32x4 v[8];
+                    load_chunk(u2, c, v);
+                    add4(r, v);
+                }
+            };
             int m0i, n0i;
             tile_coords(tile, g.tiles_m, tiles_n, TMR, BN, m0i, n0i);
             const int64_t m0 = m0i + (int64_t)rank * GBM, n0 = n0i;  // this CTA's 128 rows
@@ -488,7 +607,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // C of chunks 0 and 1 heads for this warp's staging buffers (both
             // free: the last tile ended with its stores' reads complete), the
             // rest into L2, while this tile's MMAs run
-            if (use_c && tma_path && lane == 0) {
+            if (use_c && !contrib && tma_path && lane == 0) {
                 for (int ci = 0; ci < 2 && ci < nchunks; ++ci) {
                     const uint32_t bar = smem_u32(&s.cbar[eg][ci]);
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 4096;" ::"r"(bar) : "memory");
@@ -496,7 +615,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     loads_out |= 1u << ci;
                 }
             }
-            if (use_c && row_in) {
+            if (use_c && !contrib && row_in) {
                 for (int c = tma_path ? 64 : 0; c < ncols; c += 32)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(crow + c));
             }
@@ -507,10 +626,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t tbase = tmem + ((uint32_t)(eg * 32) << 16) + ab * BN;
             bool ok = true;
-            if (tma_path) {
+            if (finish) {
+                // wait until every later unit's epilogue warps have written their partials
+                bool good = true;
+                if (lane == 0) {
+                    for (int u2 = unit + 1; good && u2 < last; ++u2) {
+                        const long long w0 = clock64();
+                        while (ld_acquire_u32(&g.flags[u2]) < kEpiWarps) {
+                            if (gemm_aborted(&s.abort) || clock64() - w0 > kWaitCycles) {
+                                good = false;
+                                break;
+                            }
+                        }
+                    }
+                    if (!good && !gemm_aborted(&s.abort)) gemm_fail(&s.abort, g.status);
+                }
+                ok = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+                __threadfence();
+            }
+            if (contrib) {
+                // the raw accumulator rows into this unit's partial slot (all rows and
+                // columns: padding included), then this warp counts itself in
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + (uint32_t)c, r);
+                    float *q = part_chunk(unit, c);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_cg_v4(q + 128 * j, {{r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]}});
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) red_release_add_u32(&g.flags[unit], 1u);
+            } else if (!ok) {
+                // a partial never came: leave C alone
+            } else if (tma_path) {
                 // TMA path: C moves in 32 x 32 chunks through this warp's two
                 // staging buffers; TMA clips rows >= M and columns >= N on the
-                // store and reads them as 0 on the load.
+                // store and reads them as 0 on the load.  A finishing unit
+                // loads the next chunk of the first later unit's partial while
+                // it adds the current one.
+                u32x4 nxt[8];
+                if (finish) load_chunk(unit + 1, 0, nxt);
                 for (int ci = 0; ci < nchunks; ++ci) {
                     const int bsel = ci & 1;
                     if (ci >= 1 && lane == 0) {
@@ -525,6 +682,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     uint32_t r[32];
                     tmem_ld32(tbase + (uint32_t)(32 * ci), r);
+                    if (finish) {
+                        u32x4 cur[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+                        if (ci + 1 < nchunks) load_chunk(unit + 1, 32 * (ci + 1), nxt);
+                        add4(r, cur);
+                        add_partials(r, 32 * ci, unit + 2);
+                    }
                     if (use_c) {
                         if (!mbar_wait_bounded(smem_u32(&s.cbar[eg][bsel]), (cpar >> bsel) & 1u)) {
                             gemm_fail(&s.abort, g.status);
@@ -564,6 +729,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int c = 0; c < ncols; c += 32) {  // warp-uniform: the TMEM load is .sync.aligned
                     uint32_t r[32];
                     tmem_ld32(tbase + (uint32_t)c, r);
+                    if (finish) add_partials(r, c, unit + 1);
                     if (!row_in) continue;
                     float *p = crow + c;
 #pragma unroll
@@ -633,7 +799,7 @@ bool kmajor_map(CUtensorMap *m, float *base, int64_t rows, int64_t Kp, int box_r
 struct GemmPlan {
     int64_t Mp, Np, Kp;
     size_t bytes;     // workspace
-    size_t off[4];    // a_hi, a_lo, b_hi, b_lo
+    size_t off[6];    // a_hi, a_lo, b_hi, b_lo, split-K partials, split-K flags
 };
 
 GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
@@ -648,7 +814,17 @@ GemmPlan gemm_plan(int64_t M, int64_t N, int64_t K, int TN)
     p.off[1] = up(a);
     p.off[2] = p.off[1] + up(a);
     p.off[3] = p.off[2] + up(b);
-    p.bytes = p.off[3] + up(b);
+    // split-K partials: one accumulator per unit (units x tile rows <= the
+    // 128-row tiles of C, and <= kMaxSms 128-row accumulators); one flag per unit
+    // (none when K is too short for split-K: s parts save KT (s - 1) / s
+    // stages, fewer than kSkMinSaved unless KT > kSkMinSaved)
+    const int64_t n128 = (p.Mp / GBM) * (p.Np / TN);
+    const size_t part = p.Kp / 16 > kSkMinSaved
+                            ? (size_t)((n128 < kMaxSms ? n128 : kMaxSms) * GBM * TN) * sizeof(float)
+                            : 0;
+    p.off[4] = p.off[3] + up(b);
+    p.off[5] = p.off[4] + up(part);
+    p.bytes = p.off[5] + up(kMaxSms * sizeof(unsigned));
     return p;
 }
 
@@ -801,6 +977,8 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     sa.alo = three ? alo : nullptr;
     sa.bhi = bhi;
     sa.blo = three ? blo : nullptr;
+    sa.flags = reinterpret_cast<unsigned *>(ws + pl.off[5]);
+    sa.nflags = kMaxSms;
     {
         // A: up to 8 blocks per SM over rows (each streams whole padded rows);
         // B: up to 32 per SM over 32 x 32 tiles (each tile is a short
@@ -851,13 +1029,33 @@ extern "C" tm_status tm_gemm(const float *A, int64_t lda, const float *B, int64_
     g.status = dev->status;
     const bool aligned = (flags & TM_ALIGNED) != 0;
     // persistent: one CTA per SM, or one 2-CTA cluster per SM pair
-    if (TM == 2 * GBM) {
-        const int pairs = dev->sms / 2;
-        const unsigned grid = 2u * (unsigned)(g.ntiles < pairs ? g.ntiles : pairs);
-        return launch_gemm_tiles<true>(TN, TK, three, aligned, maps, g, grid, s);
+    const bool pair = TM == 2 * GBM;
+    const int sms = dev->sms < kMaxSms ? dev->sms : kMaxSms;
+    const int slots = pair ? sms / 2 : sms;
+    const int units = g.ntiles < slots ? g.ntiles : slots;
+    // split-K of the last round: when its rem tiles would leave at least
+    // half of the units idle, each is cut along K into s = units / rem parts
+    // run side by side (so the units that share A or B rows read them at the
+    // same K, as in the whole rounds).  The round then takes KT / s stages
+    // instead of KT; it pays when that saves at least kSkMinSaved stages
+    // (the parts' cost -- partials written and read back, a finishing
+    // epilogue that waits for them -- measured ~10 stages of 3xTF32, ~30 of
+    // the single pass).  gemm_8192: 36 tiles on 76 pairs, s = 2, 128 stages
+    // saved; gemm_4100: 61 tiles on 76 pairs, no split.
+    const int rem = g.ntiles % units;
+    g.dp_tiles = g.ntiles;
+    g.sk_split = 0;
+    if (g.ntiles > units && rem != 0) {
+        const int split = units / rem;
+        if (split >= 2 && (int64_t)g.KT * (split - 1) >= (int64_t)kSkMinSaved * split) {
+            g.dp_tiles = g.ntiles - rem;
+            g.sk_split = split;
+        }
     }
-    const unsigned grid = (unsigned)(g.ntiles < dev->sms ? g.ntiles : dev->sms);
-    return launch_gemm_tiles<false>(TN, TK, three, aligned, maps, g, grid, s);
+    g.part = reinterpret_cast<float *>(ws + pl.off[4]);
+    g.flags = reinterpret_cast<unsigned *>(ws + pl.off[5]);
+    if (pair) return launch_gemm_tiles<true>(TN, TK, three, aligned, maps, g, 2u * (unsigned)units, s);
+    return launch_gemm_tiles<false>(TN, TK, three, aligned, maps, g, (unsigned)units, s);
 }
 
 extern "C" tm_status tm_wait_timeout_probe(tm_stream_t stream)

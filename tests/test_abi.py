@@ -176,9 +176,16 @@ def test_padding_helpers_match_oracle(lib, oracle):
 def test_gemm_host_validation(lib):
     W = 0x7F0200000000  # 1024-byte aligned fake workspace
     ws = tm.tm_gemm_workspace_bytes(4100, 4100, 1000, 256)
-    # operands zero-padded to whole tiles (rows of A to 256, either TM): [4352, 1024] hi + lo twice
-    assert ws == 2 * 4352 * 1024 * 4 + 2 * 4352 * 1024 * 4
-    assert tm.tm_gemm_workspace_bytes(4100, 4100, 0, 256) == 4 * 4352 * 32 * 4
+    # operands zero-padded to whole tiles (rows of A to 256, either TM): [4352, 1024] hi + lo twice;
+    # then split-K partials for at most 256 accumulators of 128 x TN rows (there are 34 x 17 such
+    # tiles here) and 256 flags
+    assert ws == 2 * 4352 * 1024 * 4 + 2 * 4352 * 1024 * 4 + 256 * 128 * 256 * 4 + 1024
+    # short K: no split-K, no partials
+    assert tm.tm_gemm_workspace_bytes(4100, 4100, 0, 256) == 4 * 4352 * 32 * 4 + 1024
+    # few tiles: partials only for as many 128-row accumulators as C has (2 x 1 here)
+    assert tm.tm_gemm_workspace_bytes(200, 200, 1000, 256) == 4 * 256 * 1024 * 4 + 2 * 128 * 256 * 4 + 1024
+    # K of at most 48 * 16: no split-K, no partials
+    assert tm.tm_gemm_workspace_bytes(200, 200, 768, 256) == 4 * 256 * 768 * 4 + 1024
     assert tm.tm_gemm_workspace_bytes(0, 4, 4, 256) == 0 and tm.tm_gemm_workspace_bytes(4, 4, 4, 64) == 0
 
     def g(A=P0, lda=1000, B=P1, ldb=4100, C=W + (1 << 34), ldc=4100, M=4100, N=4100, K=1000, TM=128, TN=256,

@@ -231,3 +231,35 @@ def test_gemm_unaligned_bases(cuda, oracle, TM, lead):
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, 1.5, 0.5)
     assert np.array_equal(got[:, :N], want.view(np.uint32))
     assert np.array_equal(got[:, N:], Ch.view(np.uint32).reshape(M, ldc)[:, N:])
+
+
+# Tile counts that leave at most half of the last round of units (152 CTAs, or 76 CTA pairs, on GB300)
+# busy, with enough K stages for split-K (it must take >= 48 stages off the critical path): each of that
+# round's tiles is cut along K into units // tiles parts -- 3 here for 2560 x 2560, 2 for 2500 x 2600 --
+# run side by side, and finished by the unit that ran the first part.
+SK_CASES = [(2560, 2560, 4096, 32), (2560, 2560, 4096, 16), (2500, 2600, 3200, 32)]
+
+
+@pytest.mark.parametrize("M,N,K,TK", SK_CASES)
+@pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
+@pytest.mark.parametrize("TM", [128, 256])
+def test_gemm_split_k_integers_exact(cuda, oracle, M, N, K, TK, flags, TM):
+    a, b, c = ints((M, K), 31), ints((K, N), 32), ints((M, N), 33)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, 256, flags, ldc=N + 4, TK=TK, TM=TM)
+    rows = np.unique(np.r_[np.arange(0, M, 29), np.arange(M - 70, M)])
+    want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, rows, N, K, 1.5, 0.5)
+    got = out.reshape(M, ldc)[rows, :N]
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("TM", [128, 256])
+def test_gemm_split_k_deterministic(cuda, TM):
+    """Real-valued operands: two calls give the same bits (a split tile's
+    parts are added in K order, whichever unit finishes first)."""
+    M, N, K = 2500, 2600, 3200
+    a = synth.uniform((M, K), -1.0, 1.0, 41)
+    b = synth.uniform((K, N), -1.0, 1.0, 42)
+    c = synth.uniform((M, N), -1.0, 1.0, 43)
+    first = run(a, b, c, 1.5, 0.5, 256, TM=TM)[0]
+    second = run(a, b, c, 1.5, 0.5, 256, TM=TM)[0]
+    assert np.array_equal(first.view(np.uint32), second.view(np.uint32))
