@@ -555,6 +555,34 @@ def run_reference(args):
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# --------------------------------------------------------------------- L2 flush
+class L2Flush:
+    """Evicts L2 between timed launches with a 512 MiB write (larger than the
+    126 MB L2).  mode "dirty" stops there: the timed launch first writes back
+    the flush's dirty lines as it fills L2 (pessimistic for short kernels).
+    mode "clean" then reads 256 MiB of another buffer, so the launch starts
+    from a cold L2 of clean lines, as under ncu's cache control; a kernel with
+    outputs may then leave up to an L2 of them dirty at its end, written back
+    after the timed region (optimistic for maps under ~256 MiB)."""
+
+    def __init__(self, dev, mode="dirty"):
+        import torch
+        self.mode = mode
+        self.w = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if mode == "clean" else None
+
+    def __call__(self):
+        self.w.zero_()
+        if self.r is not None:
+            self.r.sum()
+
+    @property
+    def note(self):
+        if self.mode == "clean":
+            return "flushed before each launch (512 MiB write, then 256 MiB read: cold, clean L2)"
+        return "flushed before each launch (512 MiB write: cold L2 full of the flush's dirty lines)"
+
+
 # --------------------------------------------------------------------- size sweep
 def run_sweep(args):
     """Y = 1.5*X over tensors of 2^10 .. 2^30 bytes (and the affine map over the
@@ -565,7 +593,7 @@ def run_sweep(args):
     tm.load()
     dev = torch.device("cuda", 0)
     peak, _ = measured_peak()
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, args.flush)
     stream = torch.cuda.current_stream(dev)
     out = []
     for lg in range(10, 31):
@@ -584,7 +612,7 @@ def run_sweep(args):
                          ("affine", lambda: tm.tm_affine(X, A1, E, tm.TM_VAR_AUTO, stream.cuda_stream))):
             ts = []
             for rep in range(args.sweep_reps + 3):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 fn()
@@ -594,7 +622,7 @@ def run_sweep(args):
                     ts.append(e0.elapsed_time(e1) * 1e-3)
             t = statistics.median(ts)
             res[name] = {"us": round(t * 1e6, 2), "GBps": round(gbps(8 * E, t), 1), "frac": round(gbps(8 * E, t) / peak, 4)}
-        out.append({"bytes_per_tensor": 1 << lg, "shape": list(shape), **res})
+        out.append({"bytes_per_tensor": 1 << lg, "shape": list(shape), **res, "l2": flush.note})
         del X, Y, A1
     tm.tm_check()
     return out
@@ -685,7 +713,7 @@ def run_gemm_case(name, args, dev, stream, flush):
         for rep in range(args.reps + 3):
             C.copy_(C0)
             if not args.no_flush:
-                flush.zero_()
+                flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             tm.tm_gemm(A, K, B, N, C, N, M, N, K, w["alpha"], w["beta"], ws, wsb, TM_, TN_, TK_, fl, s)
@@ -701,7 +729,7 @@ def run_gemm_case(name, args, dev, stream, flush):
                "tensor_TFLOPs": round(passes * flops / t / 1e12, 2),
                "frac_of_tf32_peak": round(passes * flops / t / 1e12 / peak, 4), "tf32_peak": round(peak, 1),
                "peak_source": peak_src, "reps": args.reps,
-               "l2": "flushed before each launch" if not args.no_flush else "warm"}
+               "l2": flush.note if not args.no_flush else "warm"}
         if args.oracle:
             row["oracle"] = time_oracle_gemm(w, a, b, c)
         out.append(row)
@@ -714,7 +742,7 @@ def run_gemm_case(name, args, dev, stream, flush):
         for rep in range(min(args.reps, 10) + 3):
             C.copy_(C0)
             if not args.no_flush:
-                flush.zero_()
+                flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             torch.addmm(C, A, B, beta=w["beta"], alpha=w["alpha"], out=C)
@@ -790,7 +818,7 @@ def time_oracle_case(kern, w, x, budget_s: float = 1.5) -> dict:
 
 def run_cases(args):
     """Time one kernel on one workload: median of CUDA-event times over
-    --reps launches, L2 flushed (a 512 MiB write) before every launch."""
+    --reps launches, L2 flushed (L2Flush) before every launch."""
     import torch
 
     from masking_tm_affine_gb300 import synth, tm
@@ -800,7 +828,7 @@ def run_cases(args):
     peak, _ = measured_peak()
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, args.flush)
     names = list(CASES) if args.case == "all" else [args.case]
     out = []
     for name in names:
@@ -886,7 +914,7 @@ def run_cases(args):
             ts = []
             for rep in range(args.reps + 3):
                 if not args.no_flush:
-                    flush.zero_()
+                    flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 fn()
@@ -895,9 +923,11 @@ def run_cases(args):
                 if rep >= 3:
                     ts.append(e0.elapsed_time(e1) * 1e-3)
             t = statistics.median(ts)
+            tmean = statistics.fmean(ts)  # events tick in ~2 us steps: the mean resolves short kernels better
             row = {"case": name, "kernel": kern, "variant": v, "tile": args.tile, "bytes": nbytes, "us": round(t * 1e6, 2),
-                        "GBps": round(gbps(nbytes, t), 1), "frac": round(gbps(nbytes, t) / peak, 4),
-                        "reps": args.reps, "l2": "flushed before each launch" if not args.no_flush else "warm"}
+                   "GBps": round(gbps(nbytes, t), 1), "frac": round(gbps(nbytes, t) / peak, 4),
+                   "us_mean": round(tmean * 1e6, 2), "GBps_mean": round(gbps(nbytes, tmean), 1),
+                   "reps": args.reps, "l2": flush.note if not args.no_flush else "warm"}
             if args.oracle:
                 row["oracle"] = time_oracle_case(kern, w, x)
             out.append(row)
@@ -923,6 +953,8 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--tile", help="--case: tile override, e.g. 1x1024 (rows x columns)")
     ap.add_argument("--no-flush", action="store_true", help="--case: do not flush L2 between launches")
+    ap.add_argument("--flush", choices=["dirty", "clean"], default="dirty",
+                    help="--case/--sweep: leave the flush's lines dirty (default) or clean (see L2Flush)")
     ap.add_argument("--oracle", action="store_true", help="--case: also time the oracle on the same workload")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
