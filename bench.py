@@ -586,7 +586,8 @@ class L2Flush:
 # --------------------------------------------------------------------- size sweep
 def run_sweep(args):
     """Y = 1.5*X over tensors of 2^10 .. 2^30 bytes (and the affine map over the
-    same sizes), median of CUDA-event times with L2 flushed between reps."""
+    same sizes, AUTO and VEC4), median of CUDA-event times with L2 flushed
+    between reps."""
     import torch
 
     from masking_tm_affine_gb300 import tm
@@ -609,7 +610,8 @@ def run_sweep(args):
         res = {}
         for name, fn in (("scale2d", lambda: tm.tm_scale2d(X, shape[1], Y, shape[1], shape[0], shape[1], ALPHA,
                                                           32, 128, flags, stream.cuda_stream)),
-                         ("affine", lambda: tm.tm_affine(X, A1, E, tm.TM_VAR_AUTO, stream.cuda_stream))):
+                         ("affine", lambda: tm.tm_affine(X, A1, E, tm.TM_VAR_AUTO, stream.cuda_stream)),
+                         ("affine_vec4", lambda: tm.tm_affine(X, A1, E, tm.TM_VAR_VEC4, stream.cuda_stream))):
             ts = []
             for rep in range(args.sweep_reps + 3):
                 flush()
