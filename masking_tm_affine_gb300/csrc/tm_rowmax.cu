@@ -23,7 +23,7 @@ namespace libtm {
 namespace {
 
 template <int BR, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) rowmax_kernel(const float *__restrict__ S, int64_t lds, int64_t M,
+__global__ void __launch_bounds__(kThreads, 8) rowmax_kernel(const float *__restrict__ S, int64_t lds, int64_t M,
                                                           int64_t N, float *__restrict__ m, int BC, int fill_zero,
                                                           unsigned *status)
 {
@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kThreads) rowmax_kernel(const float *__restric
     constexpr int EW = VEC ? 4 : 1;
     constexpr int U = VEC ? 8 : 16;    // accesses in flight per lane
     constexpr int W = L > 32 ? L / 32 : 1;
+    constexpr int kPre = 2;  // remainder-tile vectors a lane loads up front
     __shared__ float part[BR][W];
 
     pdl_trigger();
@@ -55,6 +56,30 @@ __global__ void __launch_bounds__(kThreads) rowmax_kernel(const float *__restric
         float mx = -INFINITY;
         if (live) {
             const float *sr = S + row * lds;
+            // The remainder tile's loads go out first, with the whole tiles'
+            // (when they fit kPre vectors per lane): a short row is then one
+            // DRAM round trip, not two.
+            const int64_t kt = walk.whole * BC;
+            const bool pre = !ALIGNED && walk.masked && BC <= kPre * L * EW;
+            uint32_t rw[kPre][EW];
+            if (pre) {
+#pragma unroll
+                for (int r = 0; r < kPre; ++r) {
+                    const int iota = (ln + r * L) * EW;
+                    const int64_t j = kt + iota;
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) rw[r][e] = 0u;  // a masked load reads 0
+                    if (iota < BC && j < N) {
+                        if constexpr (VEC) {
+                            const u32x4 t = ld_nc_v4(sr + j);  // N % 4 == 0: a vector is wholly in or out
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) rw[r][e] = t.v[e];
+                        } else {
+                            rw[r][0] = ld_nc_b32(sr + j);
+                        }
+                    }
+                }
+            }
             // whole tiles: no mask.  U loads in flight per lane; in a partial
             // last batch the lanes past the prefix hold -inf, the max identity
             for (int64_t v = ln; v < prefix; v += (int64_t)L * U) {
@@ -81,8 +106,19 @@ __global__ void __launch_bounds__(kThreads) rowmax_kernel(const float *__restric
                     for (int e = 0; e < EW; ++e) mx = fmaxf(mx, as_f(w[q][e]));
             }
             // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
-            if (!ALIGNED && walk.masked) {
-                const int64_t kt = walk.whole * BC;
+            if (pre) {
+#pragma unroll
+                for (int r = 0; r < kPre; ++r) {
+                    const int iota = (ln + r * L) * EW;
+                    if (iota >= BC) continue;
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) {
+                        float v = as_f(rw[r][e]);
+                        if (!fill_zero) v = (iota + e < N - kt) ? v : -INFINITY;
+                        mx = fmaxf(mx, v);
+                    }
+                }
+            } else if (!ALIGNED && walk.masked) {
                 for (int iota = ln * EW; iota < BC; iota += L * EW) {
                     const int64_t j = kt + iota;
                     float s[EW];

@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
     constexpr int EW = VEC ? 4 : 1;
     constexpr int U = VEC ? 4 : 16;    // accesses in flight per lane (16 values per batch: fewer registers)
     constexpr int W = L > 32 ? L / 32 : 1;
+    constexpr int kPre = 1;  // remainder-tile vectors a lane loads up front
     __shared__ float part_m[BR][W], part_l[BR][W];
 
     pdl_trigger();
@@ -97,6 +98,29 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
         float mx = -INFINITY, sum = 0.0f;
         if (live) {
             const float *sr = S + row * lds;
+            // The remainder tile's loads go out first, with the whole tiles'
+            // (when they fit kPre vectors per lane): one DRAM round trip fewer.
+            const int64_t kt = walk.whole * BC;
+            const bool pre = !ALIGNED && walk.masked && BC <= kPre * L * EW;
+            uint32_t rw[kPre][EW];
+            if (pre) {
+#pragma unroll
+                for (int r = 0; r < kPre; ++r) {
+                    const int iota = (ln + r * L) * EW;
+                    const int64_t j = kt + iota;
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) rw[r][e] = 0u;  // a masked load reads 0
+                    if (iota < BC && j < N) {
+                        if constexpr (VEC) {
+                            const u32x4 t = ld_nc_v4(sr + j);  // N % 4 == 0: a vector is wholly in or out
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) rw[r][e] = t.v[e];
+                        } else {
+                            rw[r][0] = ld_nc_b32(sr + j);
+                        }
+                    }
+                }
+            }
             // whole tiles: no mask.  U loads in flight per lane; in a partial
             // last batch the lanes past the prefix hold -inf, which is never the
             // maximum and adds exp(-inf) = 0
@@ -126,8 +150,20 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
                 absorb(mx, sum, vals);
             }
             // the remainder tile: masked load (reads 0), then where(iota < N - kt, s, -inf)
-            if (!ALIGNED && walk.masked) {
-                const int64_t kt = walk.whole * BC;
+            if (pre) {
+#pragma unroll
+                for (int r = 0; r < kPre; ++r) {
+                    const int iota = (ln + r * L) * EW;
+                    if (iota >= BC) continue;
+                    float sv[EW];
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) {
+                        sv[e] = as_f(rw[r][e]);
+                        if (!fill_zero) sv[e] = (iota + e < N - kt) ? sv[e] : -INFINITY;
+                    }
+                    absorb(mx, sum, sv);
+                }
+            } else if (!ALIGNED && walk.masked) {
                 for (int iota = ln * EW; iota < BC; iota += L * EW) {
                     const int64_t j = kt + iota;
                     float s[EW];
