@@ -237,15 +237,17 @@ def test_gemm_unaligned_bases(cuda, oracle, TM, lead):
 # busy, with enough K stages for split-K (it must take >= 48 stages off the critical path): each of that
 # round's tiles is cut along K into units // tiles parts -- 3 here for 2560 x 2560, 2 for 2500 x 2600 --
 # run side by side, and finished by the unit that ran the first part.
-SK_CASES = [(2560, 2560, 4096, 32), (2560, 2560, 4096, 16), (2500, 2600, 3200, 32)]
+# With TN = 128 and N = 1152 the last round holds 14 of 76 pair tiles (28 of 152 CTA tiles): 5 parts each.
+SK_CASES = [(2560, 2560, 4096, 32, 256), (2560, 2560, 4096, 16, 256), (2500, 2600, 3200, 32, 256),
+            (2560, 1152, 4096, 32, 128)]
 
 
-@pytest.mark.parametrize("M,N,K,TK", SK_CASES)
+@pytest.mark.parametrize("M,N,K,TK,TN", SK_CASES)
 @pytest.mark.parametrize("flags", [0, tm.TM_GEMM_TF32])
 @pytest.mark.parametrize("TM", [128, 256])
-def test_gemm_split_k_integers_exact(cuda, oracle, M, N, K, TK, flags, TM):
+def test_gemm_split_k_integers_exact(cuda, oracle, M, N, K, TK, TN, flags, TM):
     a, b, c = ints((M, K), 31), ints((K, N), 32), ints((M, N), 33)
-    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, 256, flags, ldc=N + 4, TK=TK, TM=TM)
+    out, Ah, Bh, Ch, lda, ldb, ldc = run(a, b, c, 1.5, 0.5, TN, flags, ldc=N + 4, TK=TK, TM=TM)
     rows = np.unique(np.r_[np.arange(0, M, 29), np.arange(M - 70, M)])
     want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, rows, N, K, 1.5, 0.5)
     got = out.reshape(M, ldc)[rows, :N]
