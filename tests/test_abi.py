@@ -213,3 +213,50 @@ def test_gemm_host_validation(lib):
     assert g(ws_ptr=P1) == tm.TM_ERR_INVALID_ARG                       # workspace overlaps B
     assert g(M=2**31, ws_bytes=1 << 62) == tm.TM_ERR_INVALID_ARG        # padded M beyond 2^31 - 1
     assert g(M=0) == tm.TM_OK and g(N=0) == tm.TM_OK                   # empty: nothing launched
+
+
+C_PROGRAM = r"""
+#include "tm.h"
+#include <stdio.h>
+#include <string.h>
+
+int main(void)
+{
+    /* host-side checks only: nothing here reaches the GPU */
+    int bad = 0;
+    bad |= tm_version() < 10000;
+    bad |= strcmp(tm_status_string(TM_OK), "TM_OK") != 0;
+    bad |= tm_affine(NULL, NULL, -1, TM_VAR_AUTO, NULL) != TM_ERR_INVALID_ARG;
+    bad |= tm_scale2d(NULL, 8, NULL, 8, 4, 8, 1.5f, 32, 128, TM_ALIGNED | TM_PDL, NULL) != TM_ERR_INVALID_ARG;
+    bad |= tm_rowsum(NULL, 8, 0, 8, NULL, 8, 128, 0, NULL) != TM_OK;            /* empty: no launch */
+    bad |= tm_padded_extent(1000, (const int32_t[]){16, 64}, 2) != 1024;
+    bad |= tm_row_stride(1001, 16) != 1004;
+    bad |= tm_gemm_workspace_bytes(0, 4, 4, 256) != 0;
+    printf("%s\n", bad ? "FAIL" : "ok");
+    return bad;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib):
+    """include/tm.h compiles as strict C99 and a C program links against
+    libtm.so and calls it (host-side checks only)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from masking_tm_affine_gb300 import build
+    work = os.path.join(build.BUILD, "abi_check")  # the package's (ignored) build folder
+    os.makedirs(work, exist_ok=True)
+    src = os.path.join(work, "abi_check.c")
+    with open(src, "w") as f:
+        f.write(C_PROGRAM)
+    exe = os.path.join(work, "abi_check")
+    libdir = os.path.dirname(build.LIB)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-ltm", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", run.stdout + run.stderr
