@@ -137,3 +137,75 @@ def test_softmax_and_affine_random(cuda, oracle, case):
     assert same_f32(Mx.payload_f32(), m_want)
     assert np.all(np.abs(L.payload_f32().astype(np.float64) - l_want) <= 1e-5 * np.abs(l_want))
     assert same_f32(OD.payload_f32(), oracle.affine(a))
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_gemm_random_integers_exact(cuda, oracle, case):
+    """Integer-valued operands (every product and partial sum exact): random
+    extents, strides, offsets, tiles, modes and alpha, beta, bit for bit."""
+    rng = np.random.default_rng(5000 + case)
+    M, N, K = (int(rng.integers(1, 400)) for _ in range(3))
+    lda, ldb, ldc = K + int(rng.integers(4)), N + int(rng.integers(4)), N + int(rng.integers(5))
+    TM = int(rng.choice([128, 256]))
+    TN = int(rng.choice([128, 256]))
+    TK = int(rng.choice([16, 32]))
+    flags = tm.TM_GEMM_TF32 if rng.random() < 0.3 else 0
+    alpha, beta = float(rng.choice([1.0, -2.0, 0.5])), float(rng.choice([0.0, 1.0, 0.25]))
+    ints = lambda shape: np.round(synth.uniform(shape, -8.5, 8.5, int(rng.integers(1 << 30)))).astype(np.float32)
+    a, b, c = ints((M, K)), ints((K, N)), ints((M, N))
+    Ah, Bh, Ch = synth.pad_rows(a, lda), synth.pad_rows(b, ldb), synth.pad_rows(c, ldc)
+    AD, BD, CD = DevBuf(Ah, int(rng.integers(4))), DevBuf(Bh, int(rng.integers(4))), DevBuf(Ch, int(rng.integers(4)))
+    import torch
+    wsb = tm.tm_gemm_workspace_bytes(M, N, K, TN)
+    raw = torch.empty(wsb + 1024, dtype=torch.uint8, device="cuda")
+    ws = (raw.data_ptr() + 1023) // 1024 * 1024
+    tm.tm_gemm(AD.ptr, lda, BD.ptr, ldb, CD.ptr, ldc, M, N, K, alpha, beta, ws, wsb, TM, TN, TK, flags)
+    tm.tm_check()
+    assert AD.guards_intact() and BD.guards_intact() and CD.guards_intact()
+    want = oracle.gemm_rows(Ah, lda, Bh, ldb, Ch, ldc, np.arange(M), N, K, alpha, beta)
+    got = CD.payload_f32().reshape(M, ldc)
+    assert np.array_equal(got[:, :N].view(np.uint32), want.view(np.uint32)), (M, N, K, TM, TN, TK, flags)
+    # the ld gap of C is never written
+    assert np.array_equal(CD.payload_u32().reshape(M, ldc)[:, N:], Ch.view(np.uint32).reshape(M, ldc)[:, N:])
+
+
+@pytest.mark.parametrize("case", range(30))
+def test_channel_affine_and_pad_random(cuda, oracle, case):
+    rng = np.random.default_rng(6000 + case)
+    # channel affine: either layout, either parameter vector absent, random tile and strides
+    layout = [tm.TM_CHANNELS_LAST, tm.TM_CHANNELS_FIRST][case % 2]
+    C = int(rng.integers(1, 300))
+    R, K = (int(rng.integers(1, 500)), C) if layout == tm.TM_CHANNELS_LAST else \
+        (C * int(rng.integers(1, 6)), int(rng.integers(1, 500)))
+    if layout == tm.TM_CHANNELS_LAST and rng.random() < 0.3:
+        K = int(rng.integers(1, C + 1))  # fewer columns than channels
+    ldx, ldy = K + int(rng.integers(5)), K + int(rng.integers(5))
+    TM, TN = MAP_TILES[int(rng.integers(len(MAP_TILES)))]
+    sc = synth.uniform((C,), 0.5, 2.0, int(rng.integers(1 << 30))) if rng.random() < 0.8 else None
+    bi = synth.normal((C,), int(rng.integers(1 << 30))) if (sc is None or rng.random() < 0.8) else None
+    x = synth.normal((R, K), int(rng.integers(1 << 30)))
+    X = synth.pad_rows(x, ldx)
+    XD, YD = DevBuf(X, int(rng.integers(4))), DevBuf(np.full(R * ldy, CANARY, dtype=np.uint32), int(rng.integers(4)))
+    lead_p = int(rng.integers(4))
+    SD = None if sc is None else DevBuf(sc, lead_p)
+    BD = None if bi is None else DevBuf(bi, lead_p)
+    tm.tm_channel_affine(XD.ptr, ldx, R, K, None if SD is None else SD.ptr, None if BD is None else BD.ptr, C, layout,
+                         YD.ptr, ldy, TM, TN, 0)
+    # pad2d: random source and padded extents and strides
+    M, N = int(rng.integers(0, 300)), int(rng.integers(0, 300))
+    Mp, Np = M + int(rng.integers(0, 40)), N + int(rng.integers(0, 40))
+    lda, ldb = max(N, 1) + int(rng.integers(4)), max(Np, 1) + int(rng.integers(4))
+    a = synth.normal((max(M, 1), max(N, 1)), int(rng.integers(1 << 30)))[:M, :N]
+    A = synth.pad_rows(a, lda) if M and N else np.zeros(max(M * lda, 1), np.float32)
+    AD = DevBuf(A, int(rng.integers(4)))
+    PD = DevBuf(np.full(max(Mp * ldb, 1), CANARY, dtype=np.uint32), int(rng.integers(4)))
+    tm.tm_pad2d(AD.ptr, lda, M, N, PD.ptr, ldb, Mp, Np)
+    tm.tm_check()
+    assert XD.guards_intact() and YD.guards_intact() and AD.guards_intact() and PD.guards_intact()
+    want = np.full(R * ldy, CANARY, dtype=np.uint32).view(np.float32)
+    oracle.channel_affine(X, ldx, R, K, sc, bi, C, layout, want, ldy)
+    assert same_f32(YD.payload_f32(), want), (layout, C, R, K, ldx, ldy, TM, TN, sc is None, bi is None)
+    want_p = np.full(max(Mp * ldb, 1), CANARY, dtype=np.uint32)
+    if Mp and Np:
+        oracle.pad2d(A, lda, M, N, want_p, ldb, Mp, Np)
+    assert np.array_equal(PD.payload_u32(), want_p), (M, N, lda, Mp, Np, ldb)
