@@ -106,7 +106,7 @@ typedef enum tm_variant {
     TM_VAR_NAIVE = 5,     /* the column walk: 256-lane programs over rows, stride ld between lanes */
     TM_VAR_STAGED = 6,    /* TMA tiles staged in shared memory, columns reduced from there */
     TM_VAR_REGDIRECT = 7, /* lanes over columns: coalesced row segments straight into registers */
-    TM_VAR_CLUSTER = 8    /* REGDIRECT's layout in one pass: 8-CTA clusters split a strip's rows and add
+    TM_VAR_CLUSTER = 8    /* REGDIRECT's layout in one pass: clusters of 8 or 16 CTAs split a strip's rows and add
                              their partials over distributed shared memory (no workspace) */
 } tm_variant;
 
@@ -251,8 +251,11 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  *   TM, TN      row tile x column strip: TM in 8..256 (powers of two),
  *               TN in 64, 128, 256; TM*TN <= 8192 for STAGED
  *               (NAIVE ignores them: its programs are 256 rows x 1 column)
- *   variant     TM_VAR_AUTO (= REGDIRECT, the fastest measured), _NAIVE,
- *               _STAGED, _REGDIRECT, _CLUSTER
+ *   variant     TM_VAR_AUTO (the fastest measured: CLUSTER with 16 CTAs per
+ *               strip when there are few strips, e.g. [4096, 4096] at
+ *               TN 128, else REGDIRECT), _NAIVE, _STAGED, _REGDIRECT,
+ *               _CLUSTER (8 or 16 CTAs per strip, 16 when that stays within
+ *               about one wave); the workspace AUTO sizes is passed either way
  *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR,
  *               TM_PDL (the first pass overlaps the previous kernel; the
  *               finish pass of a two-pass variant always overlaps the first)

@@ -577,7 +577,17 @@ tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, c
     return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, 0, s, pdl, CS);
 }
 
-constexpr int kClusterCTAs = 8;  // CTAs per strip in the cluster variant
+// CTAs per strip in the cluster variant: 8, or 16 (non-portable clusters)
+// when even 16 per strip stay within about one wave -- fewer rows per CTA,
+// fewer dependent load batches ([4096, 4096]: 17.5 -> ~15 us by kernel
+// time; at [8192, 8192] 16 per strip made 1.35 waves and 50 us against 43).
+constexpr int kClusterCTAs = 8;
+constexpr int kClusterCTAsTall = 16;
+
+int cluster_ctas(int64_t strips, int sms)
+{
+    return strips * kClusterCTAsTall <= 4LL * sms ? kClusterCTAsTall : kClusterCTAs;
+}
 
 enum class Variant { Naive, RegDirect, Staged, Cluster };
 
@@ -637,7 +647,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
         const uintptr_t clo = reinterpret_cast<uintptr_t>(c), chi = clo + (uintptr_t)N * 4;
         if (!(xhi <= clo || chi <= xlo)) return TM_ERR_INVALID_ARG;
         pl = plan_chunks(M, N, TM, TN);
-        if ((N + TN - 1) / TN * kClusterCTAs > INT32_MAX) return TM_ERR_INVALID_ARG;
+        if ((N + TN - 1) / TN * kClusterCTAsTall > INT32_MAX) return TM_ERR_INVALID_ARG;
     } else if (M > 0 && N > 0) {
         const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant == TM_VAR_NAIVE ? TM_VAR_NAIVE : TM_VAR_AUTO);
         if (workspace == nullptr || ws_bytes < need || !aligned_to(workspace, 16)) return TM_ERR_WORKSPACE;
@@ -672,6 +682,10 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     else if (variant == TM_VAR_STAGED) {
         if (tensor_map_encoder() == nullptr) return TM_ERR_CUDA;
         v = Variant::Staged;
+    } else if (M > 0 && N > 0 && cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall) {
+        // few strips: one pass of 16-CTA clusters beats two passes ([4096, 4096], 32 x 128: 14.2 us by
+        // kernel time against 12.5 + 3.5 for REGDIRECT and its finish)
+        v = Variant::Cluster;
     } else v = Variant::RegDirect;  // measured faster than STAGED at every tile on GB300 (e.g. 51.9 vs 66.2 us
                                     // at 8192 x 8192, 32 x 128), and level with CLUSTER inside the bench step
                                     // (46.3 vs 46.4 us) while CLUSTER needs enough strips to fill the GPU
@@ -698,10 +712,20 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
             a.TM = TM;
             a.status = dev->status;
             if (v == Variant::Cluster) {
+                const bool tall = cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall;
                 switch (TN) {
-                case 64: st = launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, c, s, pdl); break;
-                case 128: st = launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, c, s, pdl); break;
-                default: st = launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, c, s, pdl); break;
+                case 64:
+                    st = tall ? launch_cluster_t<64, kClusterCTAsTall>(vec, aligned, a, c, s, pdl)
+                              : launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, c, s, pdl);
+                    break;
+                case 128:
+                    st = tall ? launch_cluster_t<128, kClusterCTAsTall>(vec, aligned, a, c, s, pdl)
+                              : launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, c, s, pdl);
+                    break;
+                default:
+                    st = tall ? launch_cluster_t<256, kClusterCTAsTall>(vec, aligned, a, c, s, pdl)
+                              : launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, c, s, pdl);
+                    break;
                 }
                 return st;  // c is written by the cluster pass itself
             } else if (v == Variant::Staged) {
