@@ -29,7 +29,11 @@
 //      buffer out of TMEM (32x32b loads) and write alpha * acc + beta * C
 //      (through TMA when C's layout allows), while the next tile accumulates.
 //      Every wait is bounded; a stalled pipeline sets the status word and the
-//      CTA drains and frees its TMEM before it exits.
+//      CTA drains and frees its TMEM before it exits.  When the output tiles
+//      fill at most half of the last round of units and K is long, each of
+//      that round's tiles is cut along K into parts run side by side
+//      (split-K); the unit that ran part 0 adds the others, read back from the
+//      workspace in K order, before its epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
