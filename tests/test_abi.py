@@ -260,3 +260,39 @@ def test_header_is_plain_c_and_links(lib):
     assert r.returncode == 0, r.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0 and run.stdout.strip() == "ok", run.stdout + run.stderr
+
+
+def _prototypes():
+    """Each declared function's C parameter types, from include/tm.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b[\w ]+?\*?\s*\b(tm_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = " ".join(m.group(2).split())
+        protos[m.group(1)] = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+    return protos
+
+
+def _ctype_of(param):
+    """The ctypes type a C parameter maps to under this binding's conventions."""
+    import ctypes
+    decl = param.rsplit(" ", 1)[0] if not param.endswith("*") else param
+    if "*" in param or "tm_stream_t" in param:
+        return ctypes.c_void_p
+    for key, ct in (("int64_t", ctypes.c_int64), ("int32_t", ctypes.c_int32), ("uint32_t", ctypes.c_uint32),
+                    ("size_t", ctypes.c_size_t), ("float", ctypes.c_float), ("tm_variant", ctypes.c_int),
+                    ("tm_fill", ctypes.c_int), ("tm_status", ctypes.c_int)):
+        if decl.split()[0] == key:
+            return ct
+    raise AssertionError("unmapped parameter type: %r" % param)
+
+
+def test_binding_signatures_match_the_header():
+    """Every binding signature has the header's parameter count and types, so a
+    change to include/tm.h cannot silently misalign the ctypes calls."""
+    protos = _prototypes()
+    assert set(protos) == set(tm.SIGNATURES)
+    for name, params in protos.items():
+        _, argtypes = tm.SIGNATURES[name]
+        assert len(params) == len(argtypes), (name, params, argtypes)
+        for p, at in zip(params, argtypes):
+            assert _ctype_of(p) == at, (name, p, at)
