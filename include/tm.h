@@ -131,7 +131,12 @@ int tm_version(void);
  *   n        element count, >= 0
  *   variant  TM_VAR_AUTO (widest access the alignment allows), _SCALAR,
  *            _VEC_UNALIGNED, _VEC4 (a, out 16-byte aligned), _VEC8 (32-byte);
- *            may be OR-ed with TM_PDL (an overlapped launch)
+ *            may be OR-ed with TM_PDL (an overlapped launch).  This is the one
+ *            place in the ABI where a flag bit rides in an enum argument:
+ *            tm_affine keeps the boundary's signature, which has no flags
+ *            word.  C callers OR the two; C++ callers cast the result back,
+ *            e.g. (tm_variant)(TM_VAR_VEC4 | TM_PDL).  No other enum value
+ *            has the TM_PDL bit set, and no other entry point reads it there.
  * Errors: INVALID_ARG (n < 0, NULL with n > 0, bad variant, partial overlap),
  *         MISALIGNED (VEC4/VEC8 with misaligned pointers), CUDA.
  */
@@ -315,15 +320,19 @@ tm_status tm_softmax_rowstats(const float *S, int64_t lds, int64_t M, int64_t N,
  *   the workspace.  Returns TM_ERR_WORKSPACE (nothing launched) when the
  *   arguments need more scratch than TM_NOALLOC_SCRATCH_BYTES, i.e. when
  *   tm_colsum_workspace_bytes(M, N, TM, TN, variant) exceeds it.
- *   The first call on each device (with M, N > 0) looks up the array's device
- *   address with cudaGetSymbolAddress while that device is current; make that
- *   first call before any stream capture.
+ *   TM_VAR_CLUSTER needs no scratch and so runs at any shape.
+ *   The first call on each device that needs scratch looks up the array's
+ *   device address with cudaGetSymbolAddress while that device is current,
+ *   and keeps it for the life of the process; make that first call before
+ *   any stream capture.  The cached address (like the status word's) belongs
+ *   to the device's primary context: the library assumes the runtime API's
+ *   primary contexts and no cudaDeviceReset while it is loaded.
  *   All calls share the one array: calls whose kernels may overlap on the GPU
  *   (different streams, no ordering between them) race and give wrong sums;
  *   serialize them.  The array keeps the last call's partial sums; every word
  *   a call reads it wrote first, so no clearing is needed.
  */
-#define TM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20) /* 4 MiB per device */
+#define TM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20) /* 8 MiB per device */
 tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, int32_t TM,
                             int32_t TN, tm_variant variant, uint32_t flags, tm_stream_t stream);
 

@@ -10,6 +10,8 @@
 // Variants:
 //   NAIVE     -- the page's walk: a 256-lane program per (256-row block,
 //                column); lanes step down a column, ld apart.  Kept as the foil.
+//                Its partials go to the workspace and colsum_finish adds them
+//                (two passes).
 //   REGDIRECT -- lanes over columns: a warp reads a contiguous row segment of a
 //                TN-column strip with 16-byte loads and walks down the rows,
 //                accumulating in registers.  No shared-memory staging needed;
@@ -20,9 +22,19 @@
 //                of shared memory.  Ragged edges come free: TMA fills
 //                out-of-bounds elements with 0, the masked-load value of
 //                "Slicing, bounds and masking" ("Masking").
-// Every variant writes one partial sum per (row chunk, column) into the
-// caller's workspace; colsum_finish then adds the partials of each column in
-// ascending chunk order.  No atomics: the result is the same run to run.
+//   CLUSTER   -- REGDIRECT's layout with a strip's row chunks spread over the
+//                CTAs of a thread-block cluster, whose partials meet in
+//                distributed shared memory: one pass, no workspace.
+//
+// REGDIRECT and STAGED run in one pass.  The matrix is cut into units of one
+// TN-column strip by one row chunk; a unit's TN column sums go to the
+// workspace as the unit's partial, and the unit takes a ticket from its
+// strip's arrival counter.  The block that takes a strip's last ticket adds
+// the strip's P partials in ascending chunk order and writes c.  No block
+// waits for another, and the order of every addition is fixed whichever block
+// finishes a strip, so results are the same run to run.  The counters start
+// at zero: a one-block kernel clears them before the pass (so the workspace's
+// contents on entry do not matter), and the pass is its dependent launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,7 +57,6 @@ struct ColPlan {
     int64_t CT;     // row tiles per chunk
     int64_t P;      // chunks (partials per column)
     int64_t units;  // S * P
-    int64_t npad;   // partial row length: N rounded up to 4
 };
 
 ColPlan plan_chunks(int64_t M, int64_t N, int64_t TM, int64_t TN)
@@ -61,23 +72,144 @@ ColPlan plan_chunks(int64_t M, int64_t N, int64_t TM, int64_t TN)
     if (pl.CT < min_ct) pl.CT = min_ct;
     pl.P = (pl.RT + pl.CT - 1) / pl.CT;
     pl.units = pl.S * pl.P;
-    pl.npad = (N + 3) & ~int64_t(3);
     return pl;
+}
+
+// Bytes of the arrival counters ahead of the partials: one word per strip,
+// rounded up so the partials start 256-byte aligned.
+int64_t counter_bytes(int64_t S) { return (S * 4 + 255) & ~int64_t(255); }
+
+// Scratch of the one-pass variants: counters, then [S][P][TN] partials.  None
+// when each strip is a single chunk (the unit's sums are c itself).
+int64_t onepass_bytes(const ColPlan &pl, int64_t TN)
+{
+    return pl.P <= 1 ? 0 : counter_bytes(pl.S) + pl.S * pl.P * TN * (int64_t)sizeof(float);
 }
 
 struct ColArgs {
     const float *X;
     int64_t ldx, M, N;
-    float *part;    // [P][npad]
-    int64_t npad;
-    int64_t S, RT, CT, units;
+    float *part;    // [S][P][TN] partial sums, strip-major (unused when P == 1)
+    unsigned *cnt;  // [S] arrival counters, cleared by colsum_arm (unused when P == 1)
+    float *c;       // [N] the result
+    int64_t S, RT, CT, P, units;
     int TM;
+    int discard;    // the partials' lines are 128-byte aligned: drop them from L2 once added
     unsigned *status;
 };
 
 __device__ __forceinline__ void report(unsigned *status, unsigned bit)
 {
     atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ one-pass finish
+// Clears the strips' arrival counters.  The pass over X is launched as this
+// kernel's dependent, so its loads start at once; its first write (a partial
+// or a ticket) waits until the clearing has completed.
+__global__ void __launch_bounds__(256) colsum_arm(unsigned *cnt, int64_t S)
+{
+    pdl_trigger();
+    pdl_wait();  // an earlier call's last blocks may still be taking tickets from these counters
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < S; i += (int64_t)gridDim.x * 256) cnt[i] = 0u;
+}
+
+// c[j0 .. j0 + TN) from the strip's P partials ps[p][TN], added in ascending
+// chunk order: FL lanes of 4 columns, FR row lanes each adding chunks fr,
+// fr + FR, ..., then the FR lane sums in order.  Every thread of the block
+// calls this.  Kept out of line: it runs once per strip, and inlined it would
+// cost the streaming loop registers.
+template <int TN>
+__device__ __noinline__ void finish_strip(const float *ps, int64_t P, float *c, int64_t N, int64_t j0, int discard,
+                                          float (*fin)[TN])
+{
+    constexpr int FL = TN / 4, FR = kThreads / FL;
+    const int fl = threadIdx.x % FL, fr = threadIdx.x / FL;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int64_t p = fr;
+    for (; p + FR < P; p += 2 * FR) {
+        const u32x4 w0 = ld_l2_v4(ps + p * TN + fl * 4);
+        const u32x4 w1 = ld_l2_v4(ps + (p + FR) * TN + fl * 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += as_f(w0.v[e]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += as_f(w1.v[e]);
+    }
+    if (p < P) {
+        const u32x4 w = ld_l2_v4(ps + p * TN + fl * 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
+    }
+    *reinterpret_cast<float4 *>(&fin[fr][fl * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    __syncthreads();  // every partial of the strip has been read
+    if (fr == 0) {
+        float4 t = *reinterpret_cast<const float4 *>(&fin[0][fl * 4]);
+#pragma unroll
+        for (int q = 1; q < FR; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(&fin[q][fl * 4]);
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        const float tv[4] = {t.x, t.y, t.z, t.w};
+        const int64_t j = j0 + fl * 4;
+        pdl_wait();
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j + e < N) c[j + e] = tv[e];
+    }
+    if (discard) {
+        // nothing reads these partials again: their dirty lines need not reach DRAM
+        const char *base = reinterpret_cast<const char *>(ps);
+        const int64_t lines = P * TN * (int64_t)sizeof(float) / 128;
+        for (int64_t l = threadIdx.x; l < lines; l += kThreads) discard_l2_line(base + l * 128);
+    }
+}
+
+// The end of unit (strip s, chunk p): red[0 .. RL) holds each row lane's
+// column sums.  Threads 0 .. TN/4 - 1 add the row lanes in order, 4 columns
+// each; with one chunk per strip that is c itself, else the unit's partial,
+// and the block that brings the strip's last partial runs finish_strip.
+// Every thread of the block calls this; red is reused by the finish.
+template <int TN, int RL>
+__device__ __forceinline__ void end_unit(const ColArgs &a, int64_t s, int64_t p, float (*red)[TN], int *last)
+{
+    const int t = threadIdx.x;
+    if (t < TN / 4) {
+        float4 v = *reinterpret_cast<const float4 *>(&red[0][t * 4]);
+#pragma unroll
+        for (int q = 1; q < RL; ++q) {
+            const float4 w = *reinterpret_cast<const float4 *>(&red[q][t * 4]);
+            v.x += w.x;
+            v.y += w.y;
+            v.z += w.z;
+            v.w += w.w;
+        }
+        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
+        if (a.P == 1) {
+            const float tv[4] = {v.x, v.y, v.z, v.w};
+            const int64_t j = s * TN + t * 4;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < a.N) a.c[j + e] = tv[e];
+        } else {
+            // columns past N hold 0 and stay inside the unit's TN-wide partial
+            const u32x4 w = {{as_u(v.x), as_u(v.y), as_u(v.z), as_u(v.w)}};
+            st_v4(a.part + (s * a.P + p) * TN + t * 4, w);
+            __threadfence();  // the partial is visible GPU-wide before the ticket below
+        }
+    }
+    if (a.P == 1) return;  // the same for every thread of the block
+    __syncthreads();
+    if (t == 0) {
+        const unsigned ticket = atomicAdd(a.cnt + s, 1u);
+        *last = ticket == (unsigned)(a.P - 1);
+        if (*last) __threadfence();  // and the other units' partials before the reads of the finish
+    }
+    __syncthreads();
+    if (*last)  // red's sums were all read before the first barrier above: the finish reuses it
+        finish_strip<TN>(a.part + s * a.P * TN, a.P, a.c, a.N, s * TN, a.discard, red);
 }
 
 // ------------------------------------------------------------------ NAIVE
@@ -105,6 +237,7 @@ __global__ void __launch_bounds__(kNaiveRows) colsum_naive(const float *__restri
         }
         __syncthreads();
     }
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ finish
@@ -150,15 +283,16 @@ __global__ void __launch_bounds__(256) colsum_finish(const float *__restrict__ p
 
 // ------------------------------------------------------------------ REGDIRECT
 template <int TN, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
+__global__ void __launch_bounds__(kThreads, 8) colsum_regdirect(const ColArgs a)
 {
     constexpr int EW = VEC ? 4 : 1;
     constexpr int CL = TN / EW;           // column lanes
     constexpr int RL = kThreads / CL;     // row lanes
     constexpr int UNR = 8;                // rows in flight per thread
     static_assert(CL * RL == kThreads, "strip does not fit the block");
-    __shared__ float red[RL][TN];
-    pdl_trigger();  // the finish may launch once every block has started
+    __shared__ __align__(16) float red[kThreads * 4 / TN][TN];  // row-lane sums, then the finish's lanes
+    __shared__ int last;
+    pdl_trigger();  // a dependent next call may launch once every block has started
 
     if constexpr (ALIGNED) {
         const bool whole = (a.M % a.TM == 0) && (a.N % TN == 0);
@@ -215,18 +349,10 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
 #pragma unroll
         for (int e = 0; e < EW; ++e) red[rl][cl * EW + e] = acc[e];
         __syncthreads();
-        if (rl == 0 && col_in) {
-            pdl_wait();  // the loads above may run ahead of the previous kernel, the stores may not
-#pragma unroll
-            for (int e = 0; e < EW; ++e) {
-                float t = red[0][cl * EW + e];
-#pragma unroll
-                for (int q = 1; q < RL; ++q) t += red[q][cl * EW + e];
-                a.part[p * a.npad + j + e] = t;
-            }
-        }
+        end_unit<TN, RL>(a, s, p, red, &last);
         __syncthreads();
     }
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ CLUSTER (one pass)
@@ -236,7 +362,7 @@ __global__ void __launch_bounds__(kThreads) colsum_regdirect(const ColArgs a)
 // rank 0 adds the CS partials over distributed shared memory, in rank order,
 // and writes c.  No workspace and no second pass.
 template <int TN, int CS, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, float *__restrict__ c, int64_t rows_per_cta)
+__global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, int64_t rows_per_cta)
 {
     constexpr int EW = VEC ? 4 : 1;
     constexpr int CL = TN / EW;           // column lanes
@@ -320,9 +446,10 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, floa
         for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
         const int64_t col = s * TN + threadIdx.x;
         pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
-        if (col < a.N) c[col] = t;
+        if (col < a.N) a.c[col] = t;
     }
     cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
+    pdl_wait();      // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ STAGED (TMA)
@@ -330,16 +457,18 @@ template <int TM, int TN, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
                                                           int stages)
 {
-    pdl_trigger();  // the finish may launch once every block has started
+    pdl_trigger();  // a dependent next call may launch once every block has started
     constexpr int CL = TN / 4;            // column lanes, 4 columns each
     constexpr int RL = kThreads / CL;     // row lanes
     constexpr int TILE = TM * TN;         // floats per stage
     static_assert(TM % RL == 0, "tile height must cover the row lanes");
+    static_assert(RL == kThreads * 4 / TN, "the row lanes are the finish's lanes");
     extern __shared__ __align__(128) unsigned char smem[];
     float *tiles = reinterpret_cast<float *>(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * TILE * sizeof(float));
-    __shared__ float red[RL][TN];
+    __shared__ __align__(16) float red[RL][TN];
     __shared__ int abort_flag;
+    __shared__ int last;
 
     if constexpr (ALIGNED) {
         const bool whole = (a.M % TM == 0) && (a.N % TN == 0);
@@ -418,24 +547,14 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
             phase ^= 1u << st;
         }
         if (k % a.CT == a.CT - 1 || k == slots - 1) {
-            // end of a unit: add the row lanes in order, write this chunk's partial
+            // end of a unit: its partial (TMA zero-filled the columns past N), its ticket
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 red[rl][cl * 4 + e] = acc[e];
                 acc[e] = 0.0f;
             }
             __syncthreads();
-            const int64_t j = s * TN + cl * 4;
-            if (rl == 0 && j < a.N) {
-                pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float tot = red[0][cl * 4 + e];
-#pragma unroll
-                    for (int q = 1; q < RL; ++q) tot += red[q][cl * 4 + e];
-                    if (j + e < a.N) a.part[p * a.npad + j + e] = tot;
-                }
-            }
+            end_unit<TN, RL>(a, s, p, red, &last);
         }
         __syncthreads();  // every read of stage st (and of red) is done
         if (abort_flag) {
@@ -448,6 +567,7 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
         // let copies still in flight land before the block's shared memory goes away
         for (int st = 0; st < stages; ++st) mbar_wait_bounded(smem_u32(&full[st]), (phase >> st) & 1u);
     }
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ host side
@@ -540,20 +660,30 @@ tm_status launch_regdirect_t(bool vec, bool aligned, const ColArgs &a, cudaStrea
     return launch_kernel(k, dim3(flat_grid(a.units)), dim3(kThreads), args, 0, s, pdl);
 }
 
-// The finish runs as a programmatic dependent of the partial-sum pass, which
-// releases it as soon as its last block has started: the finish's blocks are
-// resident and waiting (pdl_wait) when the partial sums land.
+// NAIVE's second pass (and the whole of an M == 0 call, P = 0: c = 0), run as
+// a programmatic dependent of the partial-sum pass, which releases it as soon
+// as its last block has started: the finish's blocks are resident and waiting
+// (pdl_wait) when the partial sums land.
 tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, float *c, cudaStream_t s)
 {
     void *args[] = {const_cast<float **>(&part), &npad, &P, &N, &c};
     return launch_dependent((const void *)colsum_finish, dim3(flat_grid((N + 31) / 32)), dim3(256), args, 0, s);
 }
 
+// The counter clearing ahead of a one-pass call (see colsum_arm).
+tm_status launch_arm(unsigned *cnt, int64_t S, int sms, cudaStream_t s, bool pdl)
+{
+    int64_t blocks = (S + 255) / 256;
+    if (blocks > 4LL * sms) blocks = 4LL * sms;
+    void *args[] = {&cnt, &S};
+    return launch_kernel((const void *)colsum_arm, dim3(flat_grid(blocks)), dim3(256), args, 0, s, pdl);
+}
+
 // The cluster variant: CS CTAs per TN-column strip (2-CTA .. 16-CTA clusters
 // are launched with the cluster-dimension attribute; 16 needs the
 // non-portable cluster size).
 template <int TN, int CS>
-tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, cudaStream_t s, bool pdl)
+tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, cudaStream_t s, bool pdl)
 {
     const void *k;
     if (vec) k = aligned ? (const void *)colsum_cluster<TN, CS, true, true> : (const void *)colsum_cluster<TN, CS, true, false>;
@@ -573,7 +703,7 @@ tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, float *c, c
     }
     int64_t rows_per_cta = (a.M + CS - 1) / CS;
     const int64_t strips = (a.N + TN - 1) / TN;
-    void *args[] = {const_cast<ColArgs *>(&a), &c, &rows_per_cta};
+    void *args[] = {const_cast<ColArgs *>(&a), &rows_per_cta};
     return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, 0, s, pdl, CS);
 }
 
@@ -606,8 +736,7 @@ extern "C" size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, in
     }
     if (variant != TM_VAR_AUTO && variant != TM_VAR_STAGED && variant != TM_VAR_REGDIRECT) return 0;
     if (!pow2_in(TM, 8, 256) || !(TN == 64 || TN == 128 || TN == 256)) return 0;
-    const ColPlan pl = plan_chunks(M, N, TM, TN);
-    return (size_t)(pl.P * pl.npad * (int64_t)sizeof(float));
+    return (size_t)onepass_bytes(plan_chunks(M, N, TM, TN), TN);
 }
 
 extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, void *workspace,
@@ -636,31 +765,24 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
 
     const bool vec = !(flags & TM_PATH_SCALAR) && vec16 && (aligned || N % 4 == 0);
 
-    // scratch: partial sums per (chunk, column)
-    int64_t P = 0;
+    // scratch: the requested variant's (AUTO sizes for REGDIRECT even when it
+    // then runs CLUSTER); X, c and the scratch must not overlap
     const int64_t npad = (N + 3) & ~int64_t(3);
     ColPlan pl{};
-    if (M > 0 && N > 0 && variant == TM_VAR_CLUSTER) {
-        // no workspace: only X and c must not overlap
+    size_t need = 0;
+    if (M > 0 && N > 0) {
         uintptr_t xlo, xhi;
         span2d(X, ldx, M, N, &xlo, &xhi);
         const uintptr_t clo = reinterpret_cast<uintptr_t>(c), chi = clo + (uintptr_t)N * 4;
         if (!(xhi <= clo || chi <= xlo)) return TM_ERR_INVALID_ARG;
-        pl = plan_chunks(M, N, TM, TN);
-        if ((N + TN - 1) / TN * kClusterCTAsTall > INT32_MAX) return TM_ERR_INVALID_ARG;
-    } else if (M > 0 && N > 0) {
-        const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant == TM_VAR_NAIVE ? TM_VAR_NAIVE : TM_VAR_AUTO);
-        if (workspace == nullptr || ws_bytes < need || !aligned_to(workspace, 16)) return TM_ERR_WORKSPACE;
-        uintptr_t xlo, xhi, wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
-        span2d(X, ldx, M, N, &xlo, &xhi);
-        const uintptr_t clo = reinterpret_cast<uintptr_t>(c), chi = clo + (uintptr_t)N * 4;
-        if (!(xhi <= wlo || whi <= xlo) || !(chi <= wlo || whi <= clo) || !(xhi <= clo || chi <= xlo))
-            return TM_ERR_INVALID_ARG;
-        if (variant == TM_VAR_NAIVE) P = (M + kNaiveRows - 1) / kNaiveRows;
-        else {
-            pl = plan_chunks(M, N, TM, TN);
-            P = pl.P;
+        need = tm_colsum_workspace_bytes(M, N, TM, TN, variant);
+        if (need > 0) {
+            if (workspace == nullptr || ws_bytes < need || !aligned_to(workspace, 16)) return TM_ERR_WORKSPACE;
+            const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+            if (!(xhi <= wlo || whi <= xlo) || !(chi <= wlo || whi <= clo)) return TM_ERR_INVALID_ARG;
         }
+        if (variant != TM_VAR_NAIVE) pl = plan_chunks(M, N, TM, TN);
+        if (variant == TM_VAR_CLUSTER && (N + TN - 1) / TN * kClusterCTAsTall > INT32_MAX) return TM_ERR_INVALID_ARG;
     }
     const bool tma_shape = vec16 && M <= INT32_MAX && N <= INT32_MAX && staged_tile(TM, TN) &&
                            !(flags & (TM_PATH_SCALAR | TM_PATH_VEC));
@@ -672,7 +794,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     if (st != TM_OK) return st;
     cudaStream_t s = as_stream(stream);
     const bool pdl = (flags & TM_PDL) != 0;
-    float *part = static_cast<float *>(workspace);
+    if (M == 0) return launch_finish(nullptr, npad, 0, N, c, s);  // the sum of nothing: c = 0
 
     // pick the variant (the TMA encoder comes from the driver on first use)
     Variant v;
@@ -682,74 +804,82 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     else if (variant == TM_VAR_STAGED) {
         if (tensor_map_encoder() == nullptr) return TM_ERR_CUDA;
         v = Variant::Staged;
-    } else if (M > 0 && N > 0 && cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall) {
-        // few strips: one pass of 16-CTA clusters beats two passes ([4096, 4096], 32 x 128: 14.2 us by
-        // kernel time against 12.5 + 3.5 for REGDIRECT and its finish)
+    } else if (cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall) {
+        // few strips: one pass of 16-CTA clusters ([4096, 4096], 32 x 128: 14.2 us by kernel time)
         v = Variant::Cluster;
     } else v = Variant::RegDirect;  // measured faster than STAGED at every tile on GB300 (e.g. 51.9 vs 66.2 us
                                     // at 8192 x 8192, 32 x 128), and level with CLUSTER inside the bench step
-                                    // (46.3 vs 46.4 us) while CLUSTER needs enough strips to fill the GPU
+                                    // while CLUSTER needs enough strips to fill the GPU
 
-    if (M > 0) {
-        if (v == Variant::Naive) {
-            int64_t programs = P * N;
-            void *args[] = {(void *)&X, (void *)&ldx, (void *)&M, (void *)&N, (void *)&part, (void *)&npad,
-                            (void *)&programs};
-            st = launch_kernel((const void *)colsum_naive, dim3(flat_grid(programs)), dim3(kNaiveRows), args, 0, s,
-                               pdl);
-        } else {
-            ColArgs a;
-            a.X = X;
-            a.ldx = ldx;
-            a.M = M;
-            a.N = N;
-            a.part = part;
-            a.npad = pl.npad;
-            a.S = pl.S;
-            a.RT = pl.RT;
-            a.CT = pl.CT;
-            a.units = pl.units;
-            a.TM = TM;
-            a.status = dev->status;
-            if (v == Variant::Cluster) {
-                const bool tall = cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall;
-                switch (TN) {
-                case 64:
-                    st = tall ? launch_cluster_t<64, kClusterCTAsTall>(vec, aligned, a, c, s, pdl)
-                              : launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, c, s, pdl);
-                    break;
-                case 128:
-                    st = tall ? launch_cluster_t<128, kClusterCTAsTall>(vec, aligned, a, c, s, pdl)
-                              : launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, c, s, pdl);
-                    break;
-                default:
-                    st = tall ? launch_cluster_t<256, kClusterCTAsTall>(vec, aligned, a, c, s, pdl)
-                              : launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, c, s, pdl);
-                    break;
-                }
-                return st;  // c is written by the cluster pass itself
-            } else if (v == Variant::Staged) {
-                CUtensorMap map;
-                const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
-                const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
-                const cuuint32_t box[2] = {(cuuint32_t)TN, (cuuint32_t)TM};
-                const cuuint32_t estr[2] = {1, 1};
-                if (tensor_map_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(X), dims, strides,
-                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-                    return TM_ERR_CUDA;
-                st = launch_staged(TM, TN, aligned, map, a, dev->sms, s, pdl);
-            } else {
-                switch (TN) {
-                case 64: st = launch_regdirect_t<64>(vec, aligned, a, s, pdl); break;
-                case 128: st = launch_regdirect_t<128>(vec, aligned, a, s, pdl); break;
-                default: st = launch_regdirect_t<256>(vec, aligned, a, s, pdl); break;
-                }
-            }
-        }
+    if (v == Variant::Naive) {
+        float *part = static_cast<float *>(workspace);
+        const int64_t P = (M + kNaiveRows - 1) / kNaiveRows;
+        int64_t programs = P * N;
+        void *args[] = {(void *)&X, (void *)&ldx, (void *)&M, (void *)&N, (void *)&part, (void *)&npad,
+                        (void *)&programs};
+        st = launch_kernel((const void *)colsum_naive, dim3(flat_grid(programs)), dim3(kNaiveRows), args, 0, s, pdl);
         if (st != TM_OK) return st;
+        return launch_finish(part, npad, P, N, c, s);
     }
-    return launch_finish(part, npad, P, N, c, s);
+
+    ColArgs a;
+    a.X = X;
+    a.ldx = ldx;
+    a.M = M;
+    a.N = N;
+    a.c = c;
+    a.S = pl.S;
+    a.RT = pl.RT;
+    a.CT = pl.CT;
+    a.P = pl.P;
+    a.units = pl.units;
+    a.TM = TM;
+    a.status = dev->status;
+    a.cnt = nullptr;
+    a.part = nullptr;
+    a.discard = 0;
+    if (v == Variant::Cluster) {
+        const bool tall = cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall;
+        switch (TN) {
+        case 64:
+            return tall ? launch_cluster_t<64, kClusterCTAsTall>(vec, aligned, a, s, pdl)
+                        : launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, s, pdl);
+        case 128:
+            return tall ? launch_cluster_t<128, kClusterCTAsTall>(vec, aligned, a, s, pdl)
+                        : launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, s, pdl);
+        default:
+            return tall ? launch_cluster_t<256, kClusterCTAsTall>(vec, aligned, a, s, pdl)
+                        : launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, s, pdl);
+        }
+    }
+
+    // one pass: clear the counters first (the pass is their clearing's dependent)
+    bool pass_pdl = pdl;
+    if (pl.P > 1) {
+        a.cnt = static_cast<unsigned *>(workspace);
+        a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pl.S));
+        a.discard = aligned_to(workspace, 128) ? 1 : 0;
+        st = launch_arm(a.cnt, pl.S, dev->sms, s, pdl);
+        if (st != TM_OK) return st;
+        pass_pdl = true;
+    }
+    if (v == Variant::Staged) {
+        CUtensorMap map;
+        const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+        const cuuint64_t strides[1] = {(cuuint64_t)ldx * sizeof(float)};
+        const cuuint32_t box[2] = {(cuuint32_t)TN, (cuuint32_t)TM};
+        const cuuint32_t estr[2] = {1, 1};
+        if (tensor_map_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(X), dims, strides, box,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TM_ERR_CUDA;
+        return launch_staged(TM, TN, aligned, map, a, dev->sms, s, pass_pdl);
+    }
+    switch (TN) {
+    case 64: return launch_regdirect_t<64>(vec, aligned, a, s, pass_pdl);
+    case 128: return launch_regdirect_t<128>(vec, aligned, a, s, pass_pdl);
+    default: return launch_regdirect_t<256>(vec, aligned, a, s, pass_pdl);
+    }
 }
 
 // ------------------------------------------------------------------ no-allocation entry point
@@ -806,14 +936,18 @@ tm_status scratch_address(void **out)
 extern "C" tm_status tm_colsum_noalloc(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, int32_t TM,
                                        int32_t TN, tm_variant variant, uint32_t flags, tm_stream_t stream)
 {
-    const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant == TM_VAR_NAIVE ? TM_VAR_NAIVE : TM_VAR_AUTO);
+    // The requested variant's own requirement: CLUSTER keeps its partials on
+    // chip and needs none, so it runs at any shape; the others are limited by
+    // the array's size.  (0 also for arguments tm_colsum itself rejects.)
+    const size_t need = tm_colsum_workspace_bytes(M, N, TM, TN, variant);
     if (need > TM_NOALLOC_SCRATCH_BYTES) return TM_ERR_WORKSPACE;  // beyond the built-in scratch
     void *scratch = nullptr;
-    if (M > 0 && N > 0) {
+    if (need > 0) {
         const tm_status st = scratch_address(&scratch);
         if (st != TM_OK) return st;
     }
     // Every partial-sum word the second pass reads is written earlier in the
     // same call, so the array's leftover contents never need clearing.
-    return tm_colsum(X, ldx, M, N, c, scratch, TM_NOALLOC_SCRATCH_BYTES, TM, TN, variant, flags, stream);
+    return tm_colsum(X, ldx, M, N, c, scratch, need > 0 ? TM_NOALLOC_SCRATCH_BYTES : 0, TM, TN, variant, flags,
+                     stream);
 }

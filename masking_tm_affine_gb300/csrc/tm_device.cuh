@@ -96,6 +96,25 @@ __device__ __forceinline__ void st_v8(void *p, const u32x8 &x)
 
 __device__ __forceinline__ float as_f(uint32_t u) { return __uint_as_float(u); }
 
+// Data written earlier by other blocks of the same grid (partial sums): read
+// at L2, the point of coherence, never from a possibly stale L1 line.
+__device__ __forceinline__ u32x4 ld_l2_v4(const void *p)
+{
+    u32x4 r;
+    asm volatile("ld.global.cg.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
+
+// Drop the 128-byte L2 line at p (128-byte aligned) without writing it back:
+// for scratch that nothing reads again, so its dirty lines cost no DRAM write.
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ---------------------------------------------------------------- mbarriers
 // Bounded waits on shared-memory mbarriers (the TMA pipelines of the staged
 // column sum and the gemm).  A wait gives up after kWaitCycles SM clock cycles

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 8) rowmax_kernel(const float *__rest
             m[row] = mx;
         }
     }
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 template <int BR>

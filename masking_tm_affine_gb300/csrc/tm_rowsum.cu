@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads) rowsum_kernel(const float *__restric
             r[row] = s;
         }
     }
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 template <int TM>

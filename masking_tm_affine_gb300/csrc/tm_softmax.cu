@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float 
             l_out[row] = sum;
         }
     }
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 template <int BR>

@@ -191,7 +191,7 @@ def tm_colsum(X, ldx: int, M: int, N: int, c, workspace, ws_bytes: int, TM: int 
                          _stream(stream)), "tm_colsum")
 
 
-TM_NOALLOC_SCRATCH_BYTES = 4 << 20  # include/tm.h
+TM_NOALLOC_SCRATCH_BYTES = 8 << 20  # include/tm.h
 
 
 def tm_colsum_noalloc(X, ldx: int, M: int, N: int, c, TM: int = 32, TN: int = 128,

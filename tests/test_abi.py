@@ -145,14 +145,36 @@ def test_overlap_flag_host_validation(lib):
               W, gws, None) == tm.TM_ERR_INVALID_ARG
 
 
+def colsum_plan(M, N, TM, TN, target_units=8192, min_rows=64):
+    """The one-pass column sum's chunk plan: S strips of TN columns, P row
+    chunks of CT row tiles each (about target_units units, at least min_rows
+    rows per chunk)."""
+    S, RT = -(-N // TN), -(-M // TM)
+    P = min(max(-(-target_units // S), 1), RT)
+    CT = max(-(-RT // P), -(-min_rows // TM))
+    return S, -(-RT // CT)
+
+
 def test_colsum_workspace_plan(lib):
-    # one partial row per chunk; NAIVE: one per 256-row program block
+    # NAIVE: one partial row (N rounded up to 4) per 256-row program block
     assert tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128, tm.TM_VAR_NAIVE) == 16 * 4096 * 4
+    assert tm.tm_colsum_workspace_bytes(4100, 1001, 32, 128, tm.TM_VAR_NAIVE) == 17 * 1004 * 4
     assert tm.tm_colsum_workspace_bytes(0, 4096, 32, 128) == 0
     assert tm.tm_colsum_workspace_bytes(100, 0, 32, 128) == 0
     assert tm.tm_colsum_workspace_bytes(100, 10, 33, 128) == 0
-    w = tm.tm_colsum_workspace_bytes(4100, 1001, 32, 128)
-    assert w % (1004 * 4) == 0      # rows padded to a multiple of 4 columns
+    assert tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128, tm.TM_VAR_CLUSTER) == 0
+    # one pass: a word per strip (rounded up to 256 bytes), then a TN-wide
+    # partial per (strip, chunk); none when every strip is one chunk
+    for M, N, TM, TN in [(4100, 1001, 32, 128), (4096, 4096, 32, 128), (8192, 8192, 32, 128), (8192, 1000, 8, 64),
+                         (3, 1 << 20, 8, 256), (1 << 20, 3, 256, 64)]:
+        S, P = colsum_plan(M, N, TM, TN)
+        want = 0 if P == 1 else -(-4 * S // 256) * 256 + S * P * TN * 4
+        for v in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+            assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, v) == want, (M, N, TM, TN, v)
+    assert colsum_plan(4100, 1001, 32, 128) == (8, 65)
+    assert tm.tm_colsum_workspace_bytes(4100, 1001, 32, 128) == 256 + 8 * 65 * 128 * 4
+    assert tm.tm_colsum_workspace_bytes(64, 4096, 32, 128) == 0  # one 64-row chunk per strip
+    assert tm.tm_colsum_workspace_bytes(8192, 8192, 32, 128) == 256 + (4 << 20)
 
 
 def test_padding_helpers_match_oracle(lib, oracle):

@@ -145,16 +145,27 @@ def test_sums_empty_extents(cuda):
     assert np.all(R.words() == 0xDEADBEEF)
 
 
-def test_colsum_workspace_errors(cuda):
-    x = np.ones((64, 128), np.float32)
+def test_colsum_workspace_errors(cuda, oracle):
+    M, N = 1000, 128                      # 16 row chunks: the one-pass variants need scratch
+    x = np.ones((M, N), np.float32)
     XD = DevBuf(x)
-    C = DevBuf.empty(128)
-    ws = tm.tm_colsum_workspace_bytes(64, 128, 32, 128)
+    C = DevBuf.empty(N)
+    ws = tm.tm_colsum_workspace_bytes(M, N, 32, 128)
+    assert ws > 0
     W = DevBuf.empty(ws // 4, lead=1)     # misaligned scratch
-    with pytest.raises(tm.TmError) as e:
-        tm.tm_colsum(XD.ptr, 128, 64, 128, C.ptr, W.ptr, ws, 32, 128)
-    assert e.value.status == tm.TM_ERR_WORKSPACE
+    for ptr, nbytes in [(W.ptr, ws), (W.ptr - 4, ws - 4), (None, 0)]:
+        for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+            with pytest.raises(tm.TmError) as e:
+                tm.tm_colsum(XD.ptr, N, M, N, C.ptr, ptr, nbytes, 32, 128, variant)
+            assert e.value.status == tm.TM_ERR_WORKSPACE
     assert np.all(C.words() == 0xDEADBEEF)
+    # one chunk per strip: no scratch at all, c written directly
+    assert tm.tm_colsum_workspace_bytes(64, N, 32, 128) == 0
+    for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+        C = DevBuf.empty(N)
+        tm.tm_colsum(XD.ptr, N, 64, N, C.ptr, None, 0, 32, 128, variant)
+        tm.tm_check()
+        assert C.guards_intact() and np.all(C.payload_f32() == 64.0), variant
 
 
 def test_colsum_cluster_needs_no_workspace(cuda, oracle):

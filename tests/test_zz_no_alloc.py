@@ -1,13 +1,18 @@
 """tm_colsum_noalloc: the column sum for callers that cannot allocate device
-memory (framework-hosted code whose allocator owns the device, fixed memory
-budgets, paths where cudaMalloc's device-wide synchronization is not
-allowed).  Its partial sums live in the library's own static device array.
+memory -- code hosted inside a framework whose allocator owns every device
+byte, loops under a fixed memory budget that must not fail halfway, and paths
+where cudaMalloc's device-wide synchronization is not allowed.  Its scratch
+(arrival counters and partial sums) lives in the library's own static device
+array.
 
-Checked through the C ABI against tm_colsum with a caller workspace, on two
-calls in a row (the second sees the first call's leftovers in the shared
-array), within the tolerance of the other column-sum tests.  This file is
-collected last so that a failure here never hides another test's result; it
-also passes on its own in a fresh process.
+Each call goes through the C ABI and is checked against the fp64 oracle and
+against tm_colsum with a caller workspace, within the 1e-5 relative tolerance
+of the other column-sum tests.  Calls come in pairs in a row on one stream:
+the first, on the [8192, 8192] matrix, fills most of the array with its
+counters and partials, so a second call that read a word it had not written
+first -- a counter not cleared, a partial not stored -- would come out wrong.
+This file is collected last so that a failure here never hides another
+test's result; it also passes on its own in a fresh process.
 """
 import numpy as np
 import pytest
@@ -17,50 +22,76 @@ from masking_tm_affine_gb300 import synth, tm
 
 REL = 1e-5  # the tolerance of tests/test_gpu_sums.py
 
+VARIANTS = [tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED, tm.TM_VAR_CLUSTER, tm.TM_VAR_NAIVE]
+
+# (matrix, M, N, ld, TM, TN): the first fills the scratch (AUTO runs REGDIRECT
+# there: 64 strips are too many for the cluster form), the second is ragged
+# with 3e38 poison in its ld gap
+BIG = (8192, 8192, 8192, 32, 128)
+SMALL = (1500, 1001, 1004, 16, 64)
+
+
+@pytest.fixture(scope="module")
+def inputs():
+    big = synth.normal((BIG[0], BIG[1]), 31)
+    small = synth.normal((SMALL[0], SMALL[1]), 32)
+    return [(big, synth.pad_rows(big, BIG[2])), (small, synth.pad_rows(small, SMALL[2]))]
+
+
+def within(got, x, want):
+    scale = np.abs(x.astype(np.float64)).sum(axis=0)
+    return bool(np.all(np.abs(got.astype(np.float64) - want) <= REL * scale))
+
 
 def with_workspace(XD, ld, M, N, TM, TN, variant):
     C = DevBuf.empty(N)
-    ws = tm.tm_colsum_workspace_bytes(M, N, TM, TN, variant if variant == tm.TM_VAR_NAIVE else tm.TM_VAR_AUTO)
-    W = DevBuf.empty(max(ws // 4, 1))
-    rc = tm.load().tm_colsum(XD.ptr, ld, M, N, C.ptr, W.ptr, ws, TM, TN, variant, 0, None)
+    ws = tm.tm_colsum_workspace_bytes(M, N, TM, TN, variant)
+    W = DevBuf.empty(max(ws // 4, 4))
+    rc = tm.load().tm_colsum(XD.ptr, ld, M, N, C.ptr, W.ptr, max(ws, 16), TM, TN, variant, 0, None)
     assert rc == tm.TM_OK, tm.status_string(rc)
     assert tm.load().tm_check(None) == tm.TM_OK
-    return C
+    return C.payload_f32()
 
 
-def without_workspace(XD, ld, M, N, TM, TN, variant):
+@pytest.mark.gpu
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("second_flags", [0, tm.TM_PDL])
+def test_noalloc_two_calls_in_a_row(cuda, oracle, inputs, variant, second_flags):
+    XDs = [DevBuf(X) for _, X in inputs]
+    Cs = [DevBuf.empty(BIG[1]), DevBuf.empty(SMALL[1])]
+    for k, ((M, N, ld, TM, TN), flags) in enumerate(zip((BIG, SMALL), (0, second_flags))):
+        assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, variant) <= tm.TM_NOALLOC_SCRATCH_BYTES
+        # no synchronization between the two: stream order alone keeps them apart
+        rc = tm.load().tm_colsum_noalloc(XDs[k].ptr, ld, M, N, Cs[k].ptr, TM, TN, variant, flags, None)
+        assert rc == tm.TM_OK, tm.status_string(rc)
+    assert tm.load().tm_check(None) == tm.TM_OK
+    for k, ((x, X), (M, N, ld, TM, TN)) in enumerate(zip(inputs, (BIG, SMALL))):
+        got = Cs[k].payload_f32()
+        assert Cs[k].guards_intact() and XDs[k].guards_intact(), (variant, k)
+        assert within(got, x, oracle.colsum(X, ld, M, N)), (variant, k)
+        assert within(got, x, with_workspace(XDs[k], ld, M, N, TM, TN, variant).astype(np.float64)), (variant, k)
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_problems_beyond_its_scratch(cuda, oracle):
+    # [256, 2^19] at 8 x 256 tiles: 2048 strips of 4 chunks, a 1 KB partial
+    # each, 8 MiB plus the counters -- beyond the array, so rejected before
+    # anything runs, output untouched ...
+    M, N, TM, TN = 256, 1 << 19, 8, 256
+    x = synth.uniform((M, N), 0.0, 1.0, 33)
+    XD = DevBuf(x)
+    for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+        assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, variant) > tm.TM_NOALLOC_SCRATCH_BYTES
+        C = DevBuf.empty(N)
+        rc = tm.load().tm_colsum_noalloc(XD.ptr, N, M, N, C.ptr, TM, TN, variant, 0, None)
+        assert rc == tm.TM_ERR_WORKSPACE, variant
+        assert tm.load().tm_check(None) == tm.TM_OK
+        assert np.all(C.words() == 0xDEADBEEF)
+    # ... except by CLUSTER, which keeps its partials on chip and needs none
+    assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, tm.TM_VAR_CLUSTER) == 0
     C = DevBuf.empty(N)
-    rc = tm.load().tm_colsum_noalloc(XD.ptr, ld, M, N, C.ptr, TM, TN, variant, 0, None)
+    rc = tm.load().tm_colsum_noalloc(XD.ptr, N, M, N, C.ptr, TM, TN, tm.TM_VAR_CLUSTER, 0, None)
     assert rc == tm.TM_OK, tm.status_string(rc)
     assert tm.load().tm_check(None) == tm.TM_OK
     assert C.guards_intact()
-    return C
-
-
-@pytest.mark.gpu
-@pytest.mark.parametrize("variant", [tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_NAIVE])
-def test_noalloc_matches_workspace_entry_two_calls(cuda, variant):
-    # call 1: the [4096, 4096] coalescing workload; call 2: a ragged
-    # [1500, 1001] matrix, whose sums must not pick up call 1's leftovers
-    cases = [(synth.workload_input("coalesce_4096"), 4096, 4096, 4096, 32, 128),
-             (synth.normal((1500, 1001), 21), 1500, 1001, 1001, 16, 64)]
-    for x, M, N, ld, TM, TN in cases:
-        XD = DevBuf(x)
-        ref = with_workspace(XD, ld, M, N, TM, TN, variant).payload_f32().astype(np.float64)
-        got = without_workspace(XD, ld, M, N, TM, TN, variant).payload_f32().astype(np.float64)
-        scale = np.abs(x.astype(np.float64)).sum(axis=0)
-        assert np.all(np.abs(got - ref) <= REL * scale), (variant, M, N)
-
-
-@pytest.mark.gpu
-def test_noalloc_rejects_problems_beyond_its_scratch(cuda):
-    # one partial row of 2^21 columns is 8 MiB > the 4 MiB array: rejected
-    # before anything runs, output untouched
-    M, N = 8, 1 << 21
-    assert tm.tm_colsum_workspace_bytes(M, N, 8, 64) > tm.TM_NOALLOC_SCRATCH_BYTES
-    XD = DevBuf(np.ones(M * N, np.float32))
-    C = DevBuf.empty(N)
-    rc = tm.load().tm_colsum_noalloc(XD.ptr, N, M, N, C.ptr, 8, 64, tm.TM_VAR_AUTO, 0, None)
-    assert rc == tm.TM_ERR_WORKSPACE
-    assert tm.load().tm_check(None) == tm.TM_OK
-    assert np.all(C.words() == 0xDEADBEEF)
+    assert within(C.payload_f32(), x, oracle.colsum(x, N, M, N))
