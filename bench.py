@@ -8,13 +8,19 @@ One step is one pass of the whole hot path over one batch: the fp32
   scale2d     Y = 1.5*X, 32 x 128 tiles, aligned promise
   copy2d      B = X, 64 x 64 tiles, aligned promise
   rowsum      r = sum over each row (a block per row, 1024-column tiles)
-  colsum      c = sum over each column (32 x 128 strips, AUTO variant)
+  colsum      c = sum over each column (32 x 128 strips, AUTO variant: one
+              pass of the register-direct walk, the last block of each strip
+              adding its partials)
   rowmax      m = ragged row max (a block per row), 64-column tiles, -inf fill
 
 Metric: achieved HBM GB/s (GB = 1e9 bytes, the pages' convention) over the
 algorithmic bytes (each input byte read once, each output byte written once),
 and its fraction of the measured HBM peak.  Inputs are larger than L2 (256 MiB
-vs 126 MB), so no flush runs between steps.
+vs 126 MB), so no flush runs between steps.  The JSON line also carries
+`configs`: every kernel on the workload its target is stated on (the 1M
+affine map, the aligned and ragged 2-D maps, the 64 MB row and column sums,
+the ragged row max), a lone launch after an L2 flush and back-to-back
+overlapped launches, each output checked against the oracle first.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--sweep]
 """
@@ -39,7 +45,7 @@ WORKLOAD = "scale_8192"
 M = N = 8192
 ALPHA = 1.5
 FALLBACK_HBM_GBS = 6800.0
-STEP_LAUNCHES = 7  # affine, scale2d, copy2d, rowsum, colsum (partials + finish), rowmax
+STEP_LAUNCHES = 7  # affine, scale2d, copy2d, rowsum, colsum (counter clearing + one pass), rowmax
 ROWSUM_TILE = (1, 1024)   # rows per block x columns per tile
 COLSUM_TILE = (32, 128)   # row tile x column strip
 ROWMAX_BR = 1             # rows per block (column tile BC = 64)
@@ -141,6 +147,15 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- traffic
+def traffic_source():
+    """Where and when the committed DRAM-traffic figures were captured."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            return json.load(f).get("_captured")
+    except Exception:
+        return None
+
+
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, when it was taken
     on the current source of that kernel (else None)."""
@@ -312,27 +327,42 @@ def run_gpu(args):
         verify_step(bufs, x, oracle)
 
     # timed region: K steps of overlapped launches, one event pair around them
-    # (an event between two kernels would end the overlap)
+    # (an event between two kernels would end the overlap), barrier and
+    # synchronize on both sides.  The region runs again until at least
+    # --min-timed-s have passed (and at least 3 times), so the clock sampler
+    # sees the GPU under this load; `value` comes from the median region.
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.6)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def region():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for k in range(args.steps):
+                for _, fn in step:
+                    fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        return e0.elapsed_time(e1) * 1e-3
+
     wall0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for k in range(args.steps):
-            for _, fn in step:
-                fn()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
+    regions = [region()]
+    n_regions = max(3, int(args.min_timed_s / max(regions[0], 1e-6)) + 1)
+    if world > 1:  # every rank runs the same number of regions
+        nr = torch.tensor([n_regions], dtype=torch.int64, device=dev)
+        torch.distributed.all_reduce(nr, op=torch.distributed.ReduceOp.MAX)
+        n_regions = int(nr.item())
+    while len(regions) < n_regions:
+        regions.append(region())
     wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
     tm.tm_check(stream.cuda_stream)
-    elapsed = e0.elapsed_time(e1) * 1e-3
+    elapsed = statistics.median(regions)
 
     # per-kernel pass: the same K steps launched plainly, an event pair around
     # every launch, for each kernel's own duration (the roofline's denominator)
@@ -365,6 +395,9 @@ def run_gpu(args):
         return None
 
     peak, peak_src = measured_peak()
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = run_configs(tm, dev, peak, reps=args.reps, verify=not args.no_verify, x_step=x)
     kernels = {}
     for n in names:
         t = per_kernel_s[n]
@@ -398,9 +431,15 @@ def run_gpu(args):
         },
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(dom_ach, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(dom_ach / peak, 4),
-                     "traffic": recorded_traffic(dom), "peak_source": peak_src + ", of measured"
-                     if peak_src.startswith("measured") else peak_src},
+                     "traffic": recorded_traffic(dom), "traffic_source": traffic_source(),
+                     "peak_source": peak_src + ", of measured" if peak_src.startswith("measured") else peak_src},
+        "timed_regions": {"count": len(regions), "median_ms": round(elapsed * 1e3, 4),
+                          "min_ms": round(min(regions) * 1e3, 4), "max_ms": round(max(regions) * 1e3, 4),
+                          "how": "the K-step region (barrier, synchronize, one event pair, K steps, synchronize) "
+                                 "run back to back until >= %.1f s had passed; value and ms_per_step are the "
+                                 "median region's, gpu_launches counts one region" % args.min_timed_s},
         "kernels": kernels,
+        "configs": configs,
         "kernel_pass": {"ms_per_step": round(plain_s * 1e3, 4), "GBps": round(gbps(step_bytes, plain_s), 1),
                         "steps": kp, "how": "the same steps launched plainly, an event pair around every launch: "
                                             "the source of `kernels` and of the roofline's duration"},
@@ -497,6 +536,169 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
             "path": "pinned host X -> device, the six C-ABI calls, every output -> pinned host"
                     + (", one stream" if mode == "serial" else
                        "; copy-in, kernels and copy-out of consecutive steps overlap on three streams")}
+
+
+# --------------------------------------------------------------------- per-config block
+# Every workload the targets are stated on, each kernel on its own input,
+# both paths where a config has two.  (key, config, workload, kernel, path,
+# target fraction of the measured peak or None where the config is reported
+# only; C1's >= 0.85 applies at sweep sizes >= 256 MiB, see --sweep.)
+CONFIG_ENTRIES = [
+    ("C1_affine_auto", "C1", "affine_1m", "affine", "auto", None),
+    ("C1_affine_vec4", "C1", "affine_1m", "affine", "vec4", None),
+    ("C2_scale2d_aligned", "C2", "scale_8192", "scale2d", "aligned", 0.85),
+    ("C2_scale2d_ragged_vec", "C2", "scale_8192", "scale2d", "ragged_vec", None),
+    ("C3_copy2d_ragged", "C3", "ragged_4100", "copy2d", "ragged", 0.75),
+    ("C3_scale2d_ragged", "C3", "ragged_4100", "scale2d", "ragged", 0.75),
+    ("C4_rowsum", "C4", "coalesce_4096", "rowsum", "vec", 0.85),
+    ("C4_colsum_auto", "C4", "coalesce_4096", "colsum", "auto", 0.70),
+    ("C4_colsum_staged", "C4", "coalesce_4096", "colsum", "staged", 0.70),
+    ("C5_rowmax_masked", "C5", "rowmax_8192", "rowmax_masked", "neg_inf", None),
+]
+AMORTIZED_BYTES = 512 << 20  # rotating copies of the inputs and outputs: 4x the L2
+
+
+def config_kernel(tm, kern, path, w, x, dev):
+    """One kernel of a config: (describe, out_elems, call(X, O, W, stream, pdl),
+    algorithmic bytes, workspace elems, check(out_host) -> bool)."""
+    import numpy as np
+    import oracle
+    if kern == "affine":
+        n = x.size
+        var = {"auto": tm.TM_VAR_AUTO, "vec4": tm.TM_VAR_VEC4}[path]
+        want = oracle.affine(x).view(np.uint32)
+        return ("tm_affine %s, n=%d" % (path.upper(), n), n,
+                lambda X, O, W, s, pdl: tm.tm_affine(X, O, n, var | (tm.TM_PDL if pdl else 0), s),
+                8 * n, 0, lambda o: np.array_equal(o.view(np.uint32), want))
+    M, N = x.shape
+    if kern in ("scale2d", "copy2d"):
+        TM_, TN_ = w["TM"], w["TN"]
+        fl = tm.TM_ALIGNED if path == "aligned" else 0
+        if kern == "scale2d":
+            want = np.empty(M * N, np.float32)
+            oracle.scale2d(x, N, want, N, M, N, ALPHA)
+            want = want.view(np.uint32)
+            call = lambda X, O, W, s, pdl: tm.tm_scale2d(X, N, O, N, M, N, ALPHA, TM_, TN_,
+                                                         fl | (tm.TM_PDL if pdl else 0), s)
+        else:
+            want = np.empty(M * N, np.uint32)
+            oracle.copy2d(x, N, want, N, M, N)
+            call = lambda X, O, W, s, pdl: tm.tm_copy2d(X, N, O, N, M, N, TM_, TN_, fl | (tm.TM_PDL if pdl else 0), s)
+        how = "aligned promise (no masks, 32-byte vectors)" if fl else \
+            "no promise: ragged path (16-byte vectors, one predicate each)"
+        return ("tm_%s [%d,%d] %dx%d tiles, %s" % (kern, M, N, TM_, TN_, how), M * N, call, 8 * M * N, 0,
+                lambda o: np.array_equal(o.view(np.uint32), want))
+    absx = np.abs(x.astype(np.float64))
+    if kern == "rowsum":
+        want, tol = oracle.rowsum(x, N, M, N), 1e-5 * absx.sum(axis=1)
+        return ("tm_rowsum [%d,%d] 2x512 tiles" % (M, N), M,
+                lambda X, O, W, s, pdl: tm.tm_rowsum(X, N, M, N, O, 2, 512, tm.TM_PDL if pdl else 0, s),
+                4 * M * N + 4 * M, 0, lambda o: bool(np.all(np.abs(o - want) <= tol)))
+    if kern == "colsum":
+        var = {"auto": tm.TM_VAR_AUTO, "staged": tm.TM_VAR_STAGED}[path]
+        ws = tm.tm_colsum_workspace_bytes(M, N, 32, 128, var)
+        want, tol = oracle.colsum(x, N, M, N), 1e-5 * absx.sum(axis=0)
+        return ("tm_colsum %s [%d,%d] 32x128 (workspace %d B)" % (path.upper(), M, N, ws), N,
+                lambda X, O, W, s, pdl: tm.tm_colsum(X, N, M, N, O, W, ws, 32, 128, var, tm.TM_PDL if pdl else 0, s),
+                4 * M * N + 4 * N, max(ws // 4, 4), lambda o: bool(np.all(np.abs(o - want) <= tol)))
+    if kern == "rowmax_masked":
+        BC = w["BC"]
+        want = oracle.rowmax_masked(x, N, M, N, BC)
+        return ("tm_rowmax_masked [%d,%d] 8 rows x %d-column tiles, -inf fill (where/iota remainder tile of %d)"
+                % (M, N, BC, N % BC), M,
+                lambda X, O, W, s, pdl: tm.tm_rowmax_masked(X, N, M, N, O, 8, BC, tm.TM_FILL_NEG_INF,
+                                                            tm.TM_PDL if pdl else 0, s),
+                4 * M * N + 4 * M, 0, lambda o: bool(np.array_equal(o, want) and np.all(o < 0)))
+    raise ValueError(kern)
+
+
+def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
+    """Each entry of CONFIG_ENTRIES two ways: a lone launch after an L2 flush
+    (median of `reps`), and back-to-back overlapped launches (TM_PDL) captured
+    in one CUDA graph, over rotating copies of the input and output that
+    together exceed 4x the L2, so neither side is served from L2.  Every
+    output is checked against the oracle before it is timed (and the last
+    copy written again after the back-to-back run)."""
+    import torch
+
+    from masking_tm_affine_gb300 import synth
+    out = {}
+    flush = L2Flush(dev, "dirty")
+    inputs = {}
+    for key, cfg, wl, kern, path, target in CONFIG_ENTRIES:
+        if wl not in inputs:
+            inputs[wl] = x_step if (wl == WORKLOAD and x_step is not None) else synth.workload_input(wl)
+        x = inputs[wl]
+        w = synth.WORKLOADS[wl]
+        desc, on, call, nbytes, wn, check = config_kernel(tm, kern, path, w, x, dev)
+        X0 = torch.from_numpy(x.reshape(-1)).to(dev)
+        in_out = X0.numel() * 4 + on * 4
+        R = max(1, -(-AMORTIZED_BYTES // in_out))
+        Xs = [X0] + [X0.clone() for _ in range(R - 1)]
+        Os = [torch.full((on,), float("nan"), dtype=torch.float32, device=dev) for _ in range(R)]
+        W = torch.empty(max(wn, 4), dtype=torch.float32, device=dev)
+        stream = torch.cuda.current_stream(dev)
+        s = stream.cuda_stream
+        call(Xs[0], Os[0], W, s, False)
+        tm.tm_check(s)
+        ok = check(Os[0].cpu().numpy()) if verify else None
+        if verify and not ok:
+            raise AssertionError("%s: output differs from the oracle" % key)
+        # lone launches, L2 flushed before each
+        ts = []
+        for rep in range(reps + 3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(Xs[0], Os[0], W, s, False)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        lone = statistics.median(ts)
+        lone_mean = statistics.fmean(ts)
+        # back to back: n overlapped calls in one graph, rotating over R copies
+        n = max(100, min(1000, int(2e-3 / max(lone_mean, 1e-6)) + 1))
+        n = -(-n // R) * R
+        side = torch.cuda.Stream(device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            call(Xs[0], Os[0], W, side.cuda_stream, False)  # warm the call path on the capture stream
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g, stream=side):
+            cs = side.cuda_stream
+            for i in range(n):
+                call(Xs[i % R], Os[i % R], W, cs, True)
+        ts = []
+        for rep in range(5):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= 2:
+                ts.append(e0.elapsed_time(e1) * 1e-3 / n)
+        tm.tm_check(s)
+        amort = statistics.median(ts)
+        if verify and not check(Os[(n - 1) % R].cpu().numpy()):
+            raise AssertionError("%s: back-to-back output differs from the oracle" % key)
+        row = {"config": cfg, "workload": wl, "kernel": desc, "bytes": nbytes,
+               "lone": {"us": round(lone * 1e6, 2), "us_mean": round(lone_mean * 1e6, 2),
+                        "GBps": round(gbps(nbytes, lone), 1), "frac": round(gbps(nbytes, lone) / peak, 4),
+                        "reps": reps, "l2": "512 MiB dirty flush before each launch"},
+               "back_to_back": {"us_per_call": round(amort * 1e6, 3), "GBps": round(gbps(nbytes, amort), 1),
+                                "frac": round(gbps(nbytes, amort) / peak, 4), "calls": n, "copies": R,
+                                "how": "TM_PDL calls in one CUDA graph; inputs and outputs rotate over the copies "
+                                       "(%d MiB in all), so none is read from L2" % (R * in_out >> 20)},
+               "target": target, "verified": ok}
+        if target is not None:
+            row["target_met"] = {"lone": row["lone"]["frac"] >= target,
+                                 "back_to_back": row["back_to_back"]["frac"] >= target}
+        out[key] = row
+        del Xs, Os, W, X0, g
+        torch.cuda.empty_cache()
+    return out
 
 
 # --------------------------------------------------------------------- reference arm
@@ -941,7 +1143,7 @@ def run_cases(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true", help="print the 1 KB..1 GB size sweep instead")
@@ -958,6 +1160,9 @@ def main(argv=None):
     ap.add_argument("--flush", choices=["dirty", "clean"], default="dirty",
                     help="--case/--sweep: leave the flush's lines dirty (default) or clean (see L2Flush)")
     ap.add_argument("--oracle", action="store_true", help="--case: also time the oracle on the same workload")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="repeat the K-step timed region until this many seconds have passed (at least 3 times)")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config block")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
