@@ -245,14 +245,20 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  * fix from "Seeing it in a real kernel" (stage a tile in fast on-chip memory
  * and read it there in any order).
  * Row chunks write partial sums to `workspace`; a second pass adds them in a
- * fixed order, so the result is deterministic run to run.  TM_VAR_CLUSTER
- * instead adds the partials of a strip's row chunks on chip (a thread-block
- * cluster's distributed shared memory), also in a fixed order, in one pass.
+ * fixed order, so the result is deterministic run to run.  When every
+ * TN-column strip is a single row chunk -- tm_colsum_workspace_bytes returns
+ * 0: at most max(64, TM) rows, or 8192 strips and more -- the first pass
+ * writes c itself and needs no workspace.
+ * TM_VAR_CLUSTER instead adds the partials of a strip's row chunks on chip
+ * (a thread-block cluster's distributed shared memory), also in a fixed
+ * order, in one pass.
  *   X, ldx      device input [M, ldx]        c   device output, N floats
  *   workspace   device scratch of >= tm_colsum_workspace_bytes(...) bytes,
- *               16-byte aligned, owned by the caller; its contents on entry do
- *               not matter and on exit are unspecified.  TM_VAR_CLUSTER needs
- *               none (0 bytes; NULL allowed)
+ *               16-byte aligned (128-byte alignment lets the second pass drop
+ *               the partials from L2 without writing them back), owned by the
+ *               caller; its contents on entry do not matter and on exit are
+ *               unspecified.  NULL allowed when tm_colsum_workspace_bytes is 0
+ *               (TM_VAR_CLUSTER always, the others for single-chunk strips)
  *   TM, TN      row tile x column strip: TM in 8..256 (powers of two),
  *               TN in 64, 128, 256; TM*TN <= 8192 for STAGED
  *               (NAIVE ignores them: its programs are 256 rows x 1 column)

@@ -26,15 +26,15 @@
 //                CTAs of a thread-block cluster, whose partials meet in
 //                distributed shared memory: one pass, no workspace.
 //
-// REGDIRECT and STAGED run in one pass.  The matrix is cut into units of one
-// TN-column strip by one row chunk; a unit's TN column sums go to the
-// workspace as the unit's partial, and the unit takes a ticket from its
-// strip's arrival counter.  The block that takes a strip's last ticket adds
-// the strip's P partials in ascending chunk order and writes c.  No block
-// waits for another, and the order of every addition is fixed whichever block
-// finishes a strip, so results are the same run to run.  The counters start
-// at zero: a one-block kernel clears them before the pass (so the workspace's
-// contents on entry do not matter), and the pass is its dependent launch.
+// REGDIRECT and STAGED cut the matrix into units of one TN-column strip by
+// one row chunk.  A unit's TN column sums go to the workspace as its partial,
+// strip-major (a strip's partials are contiguous); colsum_finish_strips then
+// adds each column's partials in ascending chunk order -- a fixed order, so
+// results are the same run to run -- and drops the partials' lines from L2
+// without writing them back.  When a strip is a single chunk its sums are c
+// itself and no second pass runs.  (A one-pass form, in which the block that
+// brought a strip's last partial added them all, measured slower: every block
+// then waited for a counter round trip before it could leave its SM.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -75,26 +75,20 @@ ColPlan plan_chunks(int64_t M, int64_t N, int64_t TM, int64_t TN)
     return pl;
 }
 
-// Bytes of the arrival counters ahead of the partials: one word per strip,
-// rounded up so the partials start 256-byte aligned.
-int64_t counter_bytes(int64_t S) { return (S * 4 + 255) & ~int64_t(255); }
-
-// Scratch of the one-pass variants: counters, then [S][P][TN] partials.  None
-// when each strip is a single chunk (the unit's sums are c itself).
-int64_t onepass_bytes(const ColPlan &pl, int64_t TN)
+// Scratch of REGDIRECT and STAGED: [S][P][TN] partials; none when each strip
+// is a single chunk (the unit's sums are c itself).
+int64_t partial_bytes(const ColPlan &pl, int64_t TN)
 {
-    return pl.P <= 1 ? 0 : counter_bytes(pl.S) + pl.S * pl.P * TN * (int64_t)sizeof(float);
+    return pl.P <= 1 ? 0 : pl.S * pl.P * TN * (int64_t)sizeof(float);
 }
 
 struct ColArgs {
     const float *X;
     int64_t ldx, M, N;
-    float *part;    // [S][P][TN] partial sums, strip-major (unused when P == 1)
-    unsigned *cnt;  // [S] arrival counters, cleared by colsum_arm (unused when P == 1)
-    float *c;       // [N] the result
+    float *part;  // [S][P][TN] partial sums, strip-major (unused when P == 1)
+    float *c;     // [N] the result
     int64_t S, RT, CT, P, units;
     int TM;
-    int discard;    // the partials' lines are 128-byte aligned: drop them from L2 once added
     unsigned *status;
 };
 
@@ -103,113 +97,101 @@ __device__ __forceinline__ void report(unsigned *status, unsigned bit)
     atomicOr(status, bit);
 }
 
-// ------------------------------------------------------------------ one-pass finish
-// Clears the strips' arrival counters.  The pass over X is launched as this
-// kernel's dependent, so its loads start at once; its first write (a partial
-// or a ticket) waits until the clearing has completed.
-__global__ void __launch_bounds__(256) colsum_arm(unsigned *cnt, int64_t S)
-{
-    pdl_trigger();
-    pdl_wait();  // an earlier call's last blocks may still be taking tickets from these counters
-    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < S; i += (int64_t)gridDim.x * 256) cnt[i] = 0u;
-}
-
-// c[j0 .. j0 + TN) from the strip's P partials ps[p][TN], added in ascending
-// chunk order: FL lanes of 4 columns, FR row lanes each adding chunks fr,
-// fr + FR, ..., then the FR lane sums in order.  Every thread of the block
-// calls this.  Kept out of line: it runs once per strip, and inlined it would
-// cost the streaming loop registers.
-template <int TN>
-__device__ __noinline__ void finish_strip(const float *ps, int64_t P, float *c, int64_t N, int64_t j0, int discard,
-                                          float (*fin)[TN])
-{
-    constexpr int FL = TN / 4, FR = kThreads / FL;
-    const int fl = threadIdx.x % FL, fr = threadIdx.x / FL;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int64_t p = fr;
-    for (; p + FR < P; p += 2 * FR) {
-        const u32x4 w0 = ld_l2_v4(ps + p * TN + fl * 4);
-        const u32x4 w1 = ld_l2_v4(ps + (p + FR) * TN + fl * 4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += as_f(w0.v[e]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += as_f(w1.v[e]);
-    }
-    if (p < P) {
-        const u32x4 w = ld_l2_v4(ps + p * TN + fl * 4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
-    }
-    *reinterpret_cast<float4 *>(&fin[fr][fl * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    __syncthreads();  // every partial of the strip has been read
-    if (fr == 0) {
-        float4 t = *reinterpret_cast<const float4 *>(&fin[0][fl * 4]);
-#pragma unroll
-        for (int q = 1; q < FR; ++q) {
-            const float4 v = *reinterpret_cast<const float4 *>(&fin[q][fl * 4]);
-            t.x += v.x;
-            t.y += v.y;
-            t.z += v.z;
-            t.w += v.w;
-        }
-        const float tv[4] = {t.x, t.y, t.z, t.w};
-        const int64_t j = j0 + fl * 4;
-        pdl_wait();
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (j + e < N) c[j + e] = tv[e];
-    }
-    if (discard) {
-        // nothing reads these partials again: their dirty lines need not reach DRAM
-        const char *base = reinterpret_cast<const char *>(ps);
-        const int64_t lines = P * TN * (int64_t)sizeof(float) / 128;
-        for (int64_t l = threadIdx.x; l < lines; l += kThreads) discard_l2_line(base + l * 128);
-    }
-}
-
 // The end of unit (strip s, chunk p): red[0 .. RL) holds each row lane's
 // column sums.  Threads 0 .. TN/4 - 1 add the row lanes in order, 4 columns
-// each; with one chunk per strip that is c itself, else the unit's partial,
-// and the block that brings the strip's last partial runs finish_strip.
-// Every thread of the block calls this; red is reused by the finish.
+// each, into c when every strip is one chunk, else into the unit's TN-wide
+// partial (columns past N hold 0 there).
 template <int TN, int RL>
-__device__ __forceinline__ void end_unit(const ColArgs &a, int64_t s, int64_t p, float (*red)[TN], int *last)
+__device__ __forceinline__ void store_unit(const ColArgs &a, int64_t s, int64_t p, const float (*red)[TN])
 {
     const int t = threadIdx.x;
-    if (t < TN / 4) {
-        float4 v = *reinterpret_cast<const float4 *>(&red[0][t * 4]);
+    if (t >= TN / 4) return;
+    float4 v = *reinterpret_cast<const float4 *>(&red[0][t * 4]);
 #pragma unroll
-        for (int q = 1; q < RL; ++q) {
-            const float4 w = *reinterpret_cast<const float4 *>(&red[q][t * 4]);
-            v.x += w.x;
-            v.y += w.y;
-            v.z += w.z;
-            v.w += w.w;
+    for (int q = 1; q < RL; ++q) {
+        const float4 w = *reinterpret_cast<const float4 *>(&red[q][t * 4]);
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+    }
+    pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
+    if (a.P == 1) {
+        const float tv[4] = {v.x, v.y, v.z, v.w};
+        const int64_t j = s * TN + t * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j + e < a.N) a.c[j + e] = tv[e];
+    } else {
+        const u32x4 w = {{as_u(v.x), as_u(v.y), as_u(v.z), as_u(v.w)}};
+        st_v4(a.part + (s * a.P + p) * TN + t * 4, w);
+    }
+}
+
+// ------------------------------------------------------------------ finish (strip-major partials)
+// c[j] = sum over chunks p (ascending) of the partials of REGDIRECT / STAGED.
+// A block takes 32 columns: 8 lanes of 4 columns by 32 row lanes; row lane r
+// adds chunks r, r + 32, r + 64, ..., issuing its loads together (one L2 round
+// trip for up to 128 chunks), then the 32 lane sums are added in order.  The
+// partials are read once: with 128-byte aligned lines they are then dropped
+// from L2, so they never cost a DRAM write.
+constexpr int kFinCL = 8, kFinRL = 32;
+__global__ void __launch_bounds__(256, 6) colsum_finish_strips(const float *__restrict__ part, int64_t P, int64_t TN,
+                                                            int64_t N, float *__restrict__ c, int discard)
+{
+    __shared__ float4 lane[kFinRL][kFinCL];
+    pdl_trigger();  // a dependent next call may launch once every block has started
+    pdl_wait();     // launched as a dependent of the partial-sum pass: its writes first
+    const int cl = threadIdx.x % kFinCL, r = threadIdx.x / kFinCL;
+    const int64_t blocks = (N + 31) / 32;
+    for (int64_t b = blockIdx.x; b < blocks; b += gridDim.x) {
+        const int64_t j0 = b * 32, s = j0 / TN;
+        const float *col = part + s * P * TN + (j0 - s * TN);  // this block's 32 columns of chunk 0
+        // a strip's partials span P * TN < 2^23 floats (P > 1 only below 8192
+        // strips, and S * P stays under 16384 units): 32-bit offsets suffice
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t step = kFinRL * (uint32_t)TN;       // from chunk p to chunk p + 32
+        uint32_t off = (uint32_t)r * (uint32_t)TN + cl * 4;  // chunk r, this lane's 4 columns
+        int n = r < P ? (int)((P - 1 - r) / kFinRL) + 1 : 0;  // chunks of this row lane
+        for (; n >= 4; n -= 4, off += 4 * step) {
+            const u32x4 w0 = ld_l2_v4(col + off), w1 = ld_l2_v4(col + off + step);
+            const u32x4 w2 = ld_l2_v4(col + off + 2 * step), w3 = ld_l2_v4(col + off + 3 * step);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += as_f(w0.v[e]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += as_f(w1.v[e]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += as_f(w2.v[e]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += as_f(w3.v[e]);
         }
-        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
-        if (a.P == 1) {
-            const float tv[4] = {v.x, v.y, v.z, v.w};
-            const int64_t j = s * TN + t * 4;
+        for (; n > 0; --n, off += step) {
+            const u32x4 w = ld_l2_v4(col + off);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
+        }
+        lane[r][cl] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();  // every partial of these columns has been read
+        if (r == 0) {
+            float4 t = lane[0][cl];
+#pragma unroll 8
+            for (int q = 1; q < kFinRL; ++q) {
+                const float4 v = lane[q][cl];
+                t.x += v.x;
+                t.y += v.y;
+                t.z += v.z;
+                t.w += v.w;
+            }
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+            const int64_t j = j0 + cl * 4;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (j + e < a.N) a.c[j + e] = tv[e];
-        } else {
-            // columns past N hold 0 and stay inside the unit's TN-wide partial
-            const u32x4 w = {{as_u(v.x), as_u(v.y), as_u(v.z), as_u(v.w)}};
-            st_v4(a.part + (s * a.P + p) * TN + t * 4, w);
-            __threadfence();  // the partial is visible GPU-wide before the ticket below
+                if (j + e < N) c[j + e] = tv[e];
         }
+        if (discard)  // one 128-byte line per chunk: nothing reads it again
+            for (int64_t q = threadIdx.x; q < P; q += 256) discard_l2_line(col + q * TN);
+        __syncthreads();
     }
-    if (a.P == 1) return;  // the same for every thread of the block
-    __syncthreads();
-    if (t == 0) {
-        const unsigned ticket = atomicAdd(a.cnt + s, 1u);
-        *last = ticket == (unsigned)(a.P - 1);
-        if (*last) __threadfence();  // and the other units' partials before the reads of the finish
-    }
-    __syncthreads();
-    if (*last)  // red's sums were all read before the first barrier above: the finish reuses it
-        finish_strip<TN>(a.part + s * a.P * TN, a.P, a.c, a.N, s * TN, a.discard, red);
 }
 
 // ------------------------------------------------------------------ NAIVE
@@ -290,9 +272,8 @@ __global__ void __launch_bounds__(kThreads, 8) colsum_regdirect(const ColArgs a)
     constexpr int RL = kThreads / CL;     // row lanes
     constexpr int UNR = 8;                // rows in flight per thread
     static_assert(CL * RL == kThreads, "strip does not fit the block");
-    __shared__ __align__(16) float red[kThreads * 4 / TN][TN];  // row-lane sums, then the finish's lanes
-    __shared__ int last;
-    pdl_trigger();  // a dependent next call may launch once every block has started
+    __shared__ __align__(16) float red[RL][TN];
+    pdl_trigger();  // the finish may launch once every block has started
 
     if constexpr (ALIGNED) {
         const bool whole = (a.M % a.TM == 0) && (a.N % TN == 0);
@@ -349,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 8) colsum_regdirect(const ColArgs a)
 #pragma unroll
         for (int e = 0; e < EW; ++e) red[rl][cl * EW + e] = acc[e];
         __syncthreads();
-        end_unit<TN, RL>(a, s, p, red, &last);
+        store_unit<TN, RL>(a, s, p, red);
         __syncthreads();
     }
     pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
@@ -454,21 +435,19 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, int6
 
 // ------------------------------------------------------------------ STAGED (TMA)
 template <int TM, int TN, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
+__global__ void __launch_bounds__(kThreads, 6) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
                                                           int stages)
 {
-    pdl_trigger();  // a dependent next call may launch once every block has started
+    pdl_trigger();  // the finish may launch once every block has started
     constexpr int CL = TN / 4;            // column lanes, 4 columns each
     constexpr int RL = kThreads / CL;     // row lanes
     constexpr int TILE = TM * TN;         // floats per stage
     static_assert(TM % RL == 0, "tile height must cover the row lanes");
-    static_assert(RL == kThreads * 4 / TN, "the row lanes are the finish's lanes");
     extern __shared__ __align__(128) unsigned char smem[];
     float *tiles = reinterpret_cast<float *>(smem);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * TILE * sizeof(float));
     __shared__ __align__(16) float red[RL][TN];
     __shared__ int abort_flag;
-    __shared__ int last;
 
     if constexpr (ALIGNED) {
         const bool whole = (a.M % TM == 0) && (a.N % TN == 0);
@@ -547,14 +526,14 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
             phase ^= 1u << st;
         }
         if (k % a.CT == a.CT - 1 || k == slots - 1) {
-            // end of a unit: its partial (TMA zero-filled the columns past N), its ticket
+            // end of a unit: its partial (TMA zero-filled the columns past N)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 red[rl][cl * 4 + e] = acc[e];
                 acc[e] = 0.0f;
             }
             __syncthreads();
-            end_unit<TN, RL>(a, s, p, red, &last);
+            store_unit<TN, RL>(a, s, p, red);
         }
         __syncthreads();  // every read of stage st (and of red) is done
         if (abort_flag) {
@@ -670,13 +649,14 @@ tm_status launch_finish(const float *part, int64_t npad, int64_t P, int64_t N, f
     return launch_dependent((const void *)colsum_finish, dim3(flat_grid((N + 31) / 32)), dim3(256), args, 0, s);
 }
 
-// The counter clearing ahead of a one-pass call (see colsum_arm).
-tm_status launch_arm(unsigned *cnt, int64_t S, int sms, cudaStream_t s, bool pdl)
+// The second pass of REGDIRECT and STAGED, also a programmatic dependent of
+// the partial-sum pass.
+tm_status launch_finish_strips(const float *part, int64_t P, int64_t TN, int64_t N, float *c, cudaStream_t s)
 {
-    int64_t blocks = (S + 255) / 256;
-    if (blocks > 4LL * sms) blocks = 4LL * sms;
-    void *args[] = {&cnt, &S};
-    return launch_kernel((const void *)colsum_arm, dim3(flat_grid(blocks)), dim3(256), args, 0, s, pdl);
+    int discard = aligned_to(part, 128) ? 1 : 0;
+    void *args[] = {const_cast<float **>(&part), &P, &TN, &N, &c, &discard};
+    return launch_dependent((const void *)colsum_finish_strips, dim3(flat_grid((N + 31) / 32)), dim3(256), args, 0,
+                            s);
 }
 
 // The cluster variant: CS CTAs per TN-column strip (2-CTA .. 16-CTA clusters
@@ -736,7 +716,7 @@ extern "C" size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, in
     }
     if (variant != TM_VAR_AUTO && variant != TM_VAR_STAGED && variant != TM_VAR_REGDIRECT) return 0;
     if (!pow2_in(TM, 8, 256) || !(TN == 64 || TN == 128 || TN == 256)) return 0;
-    return (size_t)onepass_bytes(plan_chunks(M, N, TM, TN), TN);
+    return (size_t)partial_bytes(plan_chunks(M, N, TM, TN), TN);
 }
 
 extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, void *workspace,
@@ -835,9 +815,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     a.units = pl.units;
     a.TM = TM;
     a.status = dev->status;
-    a.cnt = nullptr;
-    a.part = nullptr;
-    a.discard = 0;
+    a.part = pl.P > 1 ? static_cast<float *>(workspace) : nullptr;
     if (v == Variant::Cluster) {
         const bool tall = cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall;
         switch (TN) {
@@ -853,16 +831,6 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
         }
     }
 
-    // one pass: clear the counters first (the pass is their clearing's dependent)
-    bool pass_pdl = pdl;
-    if (pl.P > 1) {
-        a.cnt = static_cast<unsigned *>(workspace);
-        a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + counter_bytes(pl.S));
-        a.discard = aligned_to(workspace, 128) ? 1 : 0;
-        st = launch_arm(a.cnt, pl.S, dev->sms, s, pdl);
-        if (st != TM_OK) return st;
-        pass_pdl = true;
-    }
     if (v == Variant::Staged) {
         CUtensorMap map;
         const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
@@ -873,13 +841,16 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
                                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return TM_ERR_CUDA;
-        return launch_staged(TM, TN, aligned, map, a, dev->sms, s, pass_pdl);
+        st = launch_staged(TM, TN, aligned, map, a, dev->sms, s, pdl);
+    } else {
+        switch (TN) {
+        case 64: st = launch_regdirect_t<64>(vec, aligned, a, s, pdl); break;
+        case 128: st = launch_regdirect_t<128>(vec, aligned, a, s, pdl); break;
+        default: st = launch_regdirect_t<256>(vec, aligned, a, s, pdl); break;
+        }
     }
-    switch (TN) {
-    case 64: return launch_regdirect_t<64>(vec, aligned, a, s, pass_pdl);
-    case 128: return launch_regdirect_t<128>(vec, aligned, a, s, pass_pdl);
-    default: return launch_regdirect_t<256>(vec, aligned, a, s, pass_pdl);
-    }
+    if (st != TM_OK || pl.P == 1) return st;  // one chunk per strip: the pass wrote c itself
+    return launch_finish_strips(a.part, pl.P, TN, N, c, s);
 }
 
 // ------------------------------------------------------------------ no-allocation entry point

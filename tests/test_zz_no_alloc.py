@@ -2,15 +2,15 @@
 memory -- code hosted inside a framework whose allocator owns every device
 byte, loops under a fixed memory budget that must not fail halfway, and paths
 where cudaMalloc's device-wide synchronization is not allowed.  Its scratch
-(arrival counters and partial sums) lives in the library's own static device
+(the partial sums of its first pass) lives in the library's own static device
 array.
 
 Each call goes through the C ABI and is checked against the fp64 oracle and
 against tm_colsum with a caller workspace, within the 1e-5 relative tolerance
 of the other column-sum tests.  Calls come in pairs in a row on one stream:
-the first, on the [8192, 8192] matrix, fills most of the array with its
-counters and partials, so a second call that read a word it had not written
-first -- a counter not cleared, a partial not stored -- would come out wrong.
+the first, on the [8192, 8192] matrix, fills half of the array with its
+partials, so a second call that read a partial it had not written first
+would come out wrong.
 This file is collected last so that a failure here never hides another
 test's result; it also passes on its own in a fresh process.
 """
@@ -24,9 +24,9 @@ REL = 1e-5  # the tolerance of tests/test_gpu_sums.py
 
 VARIANTS = [tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED, tm.TM_VAR_CLUSTER, tm.TM_VAR_NAIVE]
 
-# (matrix, M, N, ld, TM, TN): the first fills the scratch (AUTO runs REGDIRECT
-# there: 64 strips are too many for the cluster form), the second is ragged
-# with 3e38 poison in its ld gap
+# (M, N, ld, TM, TN): the first fills half the scratch with partials (AUTO runs
+# REGDIRECT there: 64 strips are too many for the cluster form), the second is
+# ragged with 3e38 poison in its ld gap
 BIG = (8192, 8192, 8192, 32, 128)
 SMALL = (1500, 1001, 1004, 16, 64)
 
@@ -74,10 +74,10 @@ def test_noalloc_two_calls_in_a_row(cuda, oracle, inputs, variant, second_flags)
 
 @pytest.mark.gpu
 def test_noalloc_rejects_problems_beyond_its_scratch(cuda, oracle):
-    # [256, 2^19] at 8 x 256 tiles: 2048 strips of 4 chunks, a 1 KB partial
-    # each, 8 MiB plus the counters -- beyond the array, so rejected before
-    # anything runs, output untouched ...
-    M, N, TM, TN = 256, 1 << 19, 8, 256
+    # [192, 768000] at 8 x 256 tiles: 3000 strips of 3 chunks, a 1 KB partial
+    # each, 9000 KB -- beyond the array, so rejected before anything runs,
+    # output untouched ...
+    M, N, TM, TN = 192, 768000, 8, 256
     x = synth.uniform((M, N), 0.0, 1.0, 33)
     XD = DevBuf(x)
     for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
