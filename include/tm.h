@@ -262,11 +262,11 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  *   TM, TN      row tile x column strip: TM in 8..256 (powers of two),
  *               TN in 64, 128, 256; TM*TN <= 8192 for STAGED
  *               (NAIVE ignores them: its programs are 256 rows x 1 column)
- *   variant     TM_VAR_AUTO (the fastest measured: CLUSTER with 16 CTAs per
- *               strip when there are few strips, e.g. [4096, 4096] at
- *               TN 128, else REGDIRECT), _NAIVE, _STAGED, _REGDIRECT,
- *               _CLUSTER (8 or 16 CTAs per strip, 16 when that stays within
- *               about one wave); the workspace AUTO sizes is passed either way
+ *   variant     TM_VAR_AUTO (the fastest measured: CLUSTER whenever all its
+ *               clusters fit on the GPU at once -- e.g. [4096, 4096] and
+ *               [8192, 8192] at TN 128 -- else REGDIRECT), _NAIVE, _STAGED,
+ *               _REGDIRECT, _CLUSTER (16 CTAs per strip when there are few
+ *               strips, else 8); the workspace AUTO sizes is passed either way
  *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR,
  *               TM_PDL (the first pass overlaps the previous kernel; the
  *               finish pass of a two-pass variant always overlaps the first)

@@ -341,9 +341,12 @@ __global__ void __launch_bounds__(kThreads, 8) colsum_regdirect(const ColArgs a)
 // CTAs of a cluster split the rows of one TN-column strip, each adds its rows
 // into a TN-wide partial in its shared memory, and after one cluster barrier
 // rank 0 adds the CS partials over distributed shared memory, in rank order,
-// and writes c.  No workspace and no second pass.
-template <int TN, int CS, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, int64_t rows_per_cta)
+// and writes c.  No workspace and no second pass.  IT is the type of element
+// offsets: uint32_t when (M + 128) * ldx fits 32 bits (host-checked), which
+// keeps the kernel at 32 registers -- eight CTAs per SM, so 16 CTAs per strip
+// stay within one wave even at [8192, 8192].
+template <int TN, int CS, bool VEC, bool ALIGNED, typename IT>
+__global__ void __launch_bounds__(kThreads, 8) colsum_cluster(const ColArgs a, int64_t rows_per_cta)
 {
     constexpr int EW = VEC ? 4 : 1;
     constexpr int CL = TN / EW;           // column lanes
@@ -365,45 +368,47 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, int6
             return;
         }
     }
-    const uint32_t rank = cluster_rank();
-    const int64_t s = blockIdx.x / CS;
     const int cl = threadIdx.x % CL, rl = threadIdx.x / CL;
-    const int64_t j = s * TN + (int64_t)cl * EW;
-    const bool col_in = ALIGNED || j < a.N;
-    const int64_t r0 = (int64_t)rank * rows_per_cta;
-    const int64_t r1 = r0 + rows_per_cta < a.M ? r0 + rows_per_cta : a.M;
     float acc[EW];
 #pragma unroll
     for (int e = 0; e < EW; ++e) acc[e] = 0.0f;
-    if (col_in) {
-        const float *xp = a.X + j;
-        int64_t row = r0 + rl;
-        for (; row + (UNR - 1) * RL < r1; row += UNR * RL) {
-            uint32_t v[UNR][EW];
+    {
+        const int64_t j = (int64_t)(blockIdx.x / CS) * TN + (int64_t)cl * EW;
+        const int64_t r0 = (int64_t)cluster_rank() * rows_per_cta;
+        if ((ALIGNED || j < a.N) && r0 < a.M) {
+            const float *xp = a.X + j;
+            const IT ld = (IT)a.ldx;
+            const IT nrows = (IT)((r0 + rows_per_cta < a.M ? r0 + rows_per_cta : a.M) - r0);
+            IT off = ((IT)r0 + (IT)rl) * ld;        // element offset of this lane's next row
+            const IT end = ((IT)r0 + nrows) * ld;   // one row past the CTA's last
+            const IT step = (IT)RL * ld;
+            for (; off + (IT)(UNR - 1) * step < end; off += (IT)UNR * step) {
+                uint32_t v[UNR][EW];
 #pragma unroll
-            for (int q = 0; q < UNR; ++q) {
-                const float *ptr = xp + (row + (int64_t)q * RL) * a.ldx;
+                for (int q = 0; q < UNR; ++q) {
+                    const float *ptr = xp + (off + (IT)q * step);
+                    if constexpr (VEC) {
+                        u32x4 w = ld_nc_v4(ptr);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[q][e] = w.v[e];
+                    } else {
+                        v[q][0] = ld_nc_b32(ptr);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < UNR; ++q)
+#pragma unroll
+                    for (int e = 0; e < EW; ++e) acc[e] += as_f(v[q][e]);
+            }
+            for (; off < end; off += step) {
+                const float *ptr = xp + off;
                 if constexpr (VEC) {
                     u32x4 w = ld_nc_v4(ptr);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) v[q][e] = w.v[e];
+                    for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
                 } else {
-                    v[q][0] = ld_nc_b32(ptr);
+                    acc[0] += as_f(ld_nc_b32(ptr));
                 }
-            }
-#pragma unroll
-            for (int q = 0; q < UNR; ++q)
-#pragma unroll
-                for (int e = 0; e < EW; ++e) acc[e] += as_f(v[q][e]);
-        }
-        for (; row < r1; row += RL) {
-            const float *ptr = xp + row * a.ldx;
-            if constexpr (VEC) {
-                u32x4 w = ld_nc_v4(ptr);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] += as_f(w.v[e]);
-            } else {
-                acc[0] += as_f(ld_nc_b32(ptr));
             }
         }
     }
@@ -420,12 +425,12 @@ __global__ void __launch_bounds__(kThreads) colsum_cluster(const ColArgs a, int6
         }
     }
     cluster_sync();  // every CTA's partial of this strip is in its shared memory
-    if (rank == 0 && threadIdx.x < TN) {
+    if (cluster_rank() == 0 && threadIdx.x < TN) {
         const uint32_t mine = smem_u32(&part[threadIdx.x]);
         float t = 0.0f;
 #pragma unroll 4
         for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
-        const int64_t col = s * TN + threadIdx.x;
+        const int64_t col = (int64_t)(blockIdx.x / CS) * TN + threadIdx.x;
         pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
         if (col < a.N) a.c[col] = t;
     }
@@ -659,38 +664,108 @@ tm_status launch_finish_strips(const float *part, int64_t P, int64_t TN, int64_t
                             s);
 }
 
-// The cluster variant: CS CTAs per TN-column strip (2-CTA .. 16-CTA clusters
-// are launched with the cluster-dimension attribute; 16 needs the
-// non-portable cluster size).
+// The cluster variant: CS CTAs per TN-column strip (8-CTA clusters are
+// portable; 16 needs the non-portable cluster size, set once per kernel).
 template <int TN, int CS>
-tm_status launch_cluster_t(bool vec, bool aligned, const ColArgs &a, cudaStream_t s, bool pdl)
+const void *cluster_kernel(bool vec, bool aligned, bool narrow)
 {
-    const void *k;
-    if (vec) k = aligned ? (const void *)colsum_cluster<TN, CS, true, true> : (const void *)colsum_cluster<TN, CS, true, false>;
-    else k = aligned ? (const void *)colsum_cluster<TN, CS, false, true> : (const void *)colsum_cluster<TN, CS, false, false>;
-    if (CS > 8) {
-        static std::once_flag once[kMaxDevices][4];
-        int devno = 0;
-        cudaGetDevice(&devno);
-        bool ok = true;
-        std::call_once(once[devno][(vec ? 2 : 0) + (aligned ? 1 : 0)], [&] {
-            if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-                cudaGetLastError();
-                ok = false;
-            }
-        });
-        if (!ok) return TM_ERR_CUDA;
+    if (narrow) {
+        if (vec) return aligned ? (const void *)colsum_cluster<TN, CS, true, true, uint32_t>
+                                : (const void *)colsum_cluster<TN, CS, true, false, uint32_t>;
+        return aligned ? (const void *)colsum_cluster<TN, CS, false, true, uint32_t>
+                       : (const void *)colsum_cluster<TN, CS, false, false, uint32_t>;
     }
+    if (vec) return aligned ? (const void *)colsum_cluster<TN, CS, true, true, int64_t>
+                            : (const void *)colsum_cluster<TN, CS, true, false, int64_t>;
+    return aligned ? (const void *)colsum_cluster<TN, CS, false, true, int64_t>
+                   : (const void *)colsum_cluster<TN, CS, false, false, int64_t>;
+}
+
+const void *pick_cluster_kernel(int TN, int CS, bool vec, bool aligned, bool narrow)
+{
+    switch (TN) {
+    case 64: return CS == 16 ? cluster_kernel<64, 16>(vec, aligned, narrow) : cluster_kernel<64, 8>(vec, aligned, narrow);
+    case 128:
+        return CS == 16 ? cluster_kernel<128, 16>(vec, aligned, narrow) : cluster_kernel<128, 8>(vec, aligned, narrow);
+    default:
+        return CS == 16 ? cluster_kernel<256, 16>(vec, aligned, narrow) : cluster_kernel<256, 8>(vec, aligned, narrow);
+    }
+}
+
+// Per device and kernel: the non-portable cluster size allowed (16-CTA
+// kernels), and how many clusters of CS CTAs can be resident at once (the
+// occupancy API's answer; -1 if it could not answer).
+struct ClusterSlot {
+    const void *kernel;
+    int max_active;
+};
+std::mutex g_cluster_mu;
+ClusterSlot g_cluster_slots[kMaxDevices][64];
+
+tm_status cluster_prepare(const void *k, int CS, int *max_active)
+{
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess || devno < 0 || devno >= kMaxDevices) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_cluster_mu);
+    ClusterSlot *slots = g_cluster_slots[devno];
+    for (int i = 0; i < 64 && slots[i].kernel; ++i)
+        if (slots[i].kernel == k) {
+            *max_active = slots[i].max_active;
+            return TM_OK;
+        }
+    if (CS > 8 && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(CS * 64));
+    cfg.blockDim = dim3(kThreads);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)CS;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = -1;
+    if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = -1;
+    }
+    for (int i = 0; i < 64; ++i)
+        if (!slots[i].kernel) {
+            slots[i].kernel = k;
+            slots[i].max_active = n;
+            break;
+        }
+    *max_active = n;
+    return TM_OK;
+}
+
+// 32-bit element offsets in the cluster kernel when they cannot wrap: the row
+// loop looks up to UNR * RL <= 128 rows past the CTA's range before it
+// compares, so every offset it forms is below (M + 128) * ldx.
+bool cluster_narrow(int64_t M, int64_t ldx) { return ldx <= (int64_t)UINT32_MAX / (M + 128); }
+
+tm_status launch_cluster(int TN, int CS, bool vec, bool aligned, const ColArgs &a, cudaStream_t s, bool pdl)
+{
+    const void *k = pick_cluster_kernel(TN, CS, vec, aligned, cluster_narrow(a.M, a.ldx));
+    int max_active;
+    const tm_status st = cluster_prepare(k, CS, &max_active);
+    if (st != TM_OK) return st;
     int64_t rows_per_cta = (a.M + CS - 1) / CS;
     const int64_t strips = (a.N + TN - 1) / TN;
     void *args[] = {const_cast<ColArgs *>(&a), &rows_per_cta};
-    return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, 0, s, pdl, CS);
+    return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, 0, s, pdl, (unsigned)CS);
 }
 
-// CTAs per strip in the cluster variant: 8, or 16 (non-portable clusters)
-// when even 16 per strip stay within about one wave -- fewer rows per CTA,
-// fewer dependent load batches ([4096, 4096]: 17.5 -> ~15 us by kernel
-// time; at [8192, 8192] 16 per strip made 1.35 waves and 50 us against 43).
+// CTAs per strip in the cluster variant: 16 (non-portable clusters) when there
+// are few strips -- half the rows per CTA, half the dependent load batches
+// ([4096, 4096]: 17.9 against 19.2 us per call) -- else 8 ([8192, 8192]: 16
+// per strip measured 47.2 against 46.2 us, 38.1 against 36.2 chained).
 constexpr int kClusterCTAs = 8;
 constexpr int kClusterCTAsTall = 16;
 
@@ -784,12 +859,18 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     else if (variant == TM_VAR_STAGED) {
         if (tensor_map_encoder() == nullptr) return TM_ERR_CUDA;
         v = Variant::Staged;
-    } else if (cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall) {
-        // few strips: one pass of 16-CTA clusters ([4096, 4096], 32 x 128: 14.2 us by kernel time)
-        v = Variant::Cluster;
-    } else v = Variant::RegDirect;  // measured faster than STAGED at every tile on GB300 (e.g. 51.9 vs 66.2 us
-                                    // at 8192 x 8192, 32 x 128), and level with CLUSTER inside the bench step
-                                    // while CLUSTER needs enough strips to fill the GPU
+    } else {
+        // AUTO: the one-pass cluster form whenever all its clusters fit on the
+        // GPU at once (one wave), else the register-direct pass and its finish.
+        // [8192, 8192] at 32 x 128: 64 strips of 8-CTA clusters, 148 resident:
+        // 46.2 us per call plain and 36.2 chained, against 45.8 and 37.5;
+        // [4096, 4096]: 32 strips of 16-CTA clusters.
+        const int CS = cluster_ctas(pl.S, dev->sms);
+        int max_active = -1;
+        st = cluster_prepare(pick_cluster_kernel(TN, CS, vec, aligned, cluster_narrow(M, ldx)), CS, &max_active);
+        if (st != TM_OK) return st;
+        v = (max_active > 0 && pl.S <= max_active) ? Variant::Cluster : Variant::RegDirect;
+    }
 
     if (v == Variant::Naive) {
         float *part = static_cast<float *>(workspace);
@@ -816,20 +897,7 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     a.TM = TM;
     a.status = dev->status;
     a.part = pl.P > 1 ? static_cast<float *>(workspace) : nullptr;
-    if (v == Variant::Cluster) {
-        const bool tall = cluster_ctas(pl.S, dev->sms) == kClusterCTAsTall;
-        switch (TN) {
-        case 64:
-            return tall ? launch_cluster_t<64, kClusterCTAsTall>(vec, aligned, a, s, pdl)
-                        : launch_cluster_t<64, kClusterCTAs>(vec, aligned, a, s, pdl);
-        case 128:
-            return tall ? launch_cluster_t<128, kClusterCTAsTall>(vec, aligned, a, s, pdl)
-                        : launch_cluster_t<128, kClusterCTAs>(vec, aligned, a, s, pdl);
-        default:
-            return tall ? launch_cluster_t<256, kClusterCTAsTall>(vec, aligned, a, s, pdl)
-                        : launch_cluster_t<256, kClusterCTAs>(vec, aligned, a, s, pdl);
-        }
-    }
+    if (v == Variant::Cluster) return launch_cluster(TN, cluster_ctas(pl.S, dev->sms), vec, aligned, a, s, pdl);
 
     if (v == Variant::Staged) {
         CUtensorMap map;
