@@ -799,7 +799,8 @@ def run_sweep(args):
     flush = L2Flush(dev, args.flush)
     stream = torch.cuda.current_stream(dev)
     out = []
-    for lg in range(10, 31):
+    lo, hi = (int(v) for v in args.sweep_lg.split("-"))
+    for lg in range(lo, hi + 1):
         E = (1 << lg) // 4
         if E >= 4096:
             n = min(8192, E // 32)
@@ -839,8 +840,11 @@ CASES = {
     "scale_8192": ("scale_8192", "scale2d", ["aligned", "ragged_vec", "scalar"]),
     "ragged_copy": ("ragged_4100", "copy2d", ["auto", "scalar"]),
     "ragged_scale": ("ragged_4100", "scale2d", ["auto", "scalar"]),
+    "aligned_copy": ("aligned_4096", "copy2d", ["aligned", "auto"]),
     "rowsum_4096": ("coalesce_4096", "rowsum", ["vec", "scalar"]),
     "colsum_4096": ("coalesce_4096", "colsum", ["auto", "staged", "regdirect", "naive", "cluster"]),
+    # the plain streaming read of the same 64 MiB: the floor the sums are compared with
+    "read_floor_4096": ("coalesce_4096", "read_probe", ["u4", "u1", "u2", "u8", "u16"]),
     "rowmax_8192": ("rowmax_8192", "rowmax_masked", ["neg_inf", "zero", "scalar"]),
     "softmax_8192": ("rowmax_8192", "softmax_rowstats", ["neg_inf", "zero", "scalar"]),
     "pad_ragged": ("ragged_4100", "pad2d", ["auto"]),
@@ -1081,6 +1085,11 @@ def run_cases(args):
                          tm.tm_colsum_workspace_bytes(Mw, Nw, CT_, CN_, tm.TM_VAR_AUTO))
                 Wt = torch.empty(ws // 4, dtype=torch.float32, device=dev)
                 mk = lambda v: (lambda: tm.tm_colsum(X, Nw, Mw, Nw, O, Wt, ws, CT_, CN_, vm[v], 0, s))
+            elif kern == "read_probe":
+                U = {"u1": 1, "u2": 2, "u4": 4, "u8": 8, "u16": 16}
+                O = torch.empty(max(tm.tm_read_probe_blocks(Mw * Nw, 1), 1), dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw
+                mk = lambda v: (lambda: tm.tm_read_probe(X, Mw * Nw, O, U[v], s))
             elif kern == "pad2d":
                 Mp_, Np_ = tm.tm_padded_extent(Mw, [w["TM"]]), tm.tm_padded_extent(Nw, [w["TN"]])
                 ldp = tm.tm_row_stride(Np_, 16)
@@ -1148,6 +1157,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true", help="print the 1 KB..1 GB size sweep instead")
     ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--sweep-lg", default="10-30", help="--sweep: log2 byte sizes per tensor, LO-HI")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--e2e-mode", choices=["pipelined", "serial"], default="pipelined")
     ap.add_argument("--no-cpu-baseline", action="store_true")

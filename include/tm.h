@@ -435,6 +435,21 @@ tm_status tm_tile_walk_probe(int64_t K, int32_t T, int64_t *out4, tm_stream_t st
 tm_status tm_wait_timeout_probe(tm_stream_t stream);
 
 /*
+ * tm_read_probe -- the plain streaming read the reductions are measured
+ * against ("Memory Coalescing and Tensor Layout", "What it actually costs":
+ * the row walk's bandwidth is the ceiling to compare any kernel with).  The n
+ * floats of x (n % 4 == 0, x 16-byte aligned) are read once by a flat grid of
+ * 256-thread blocks, each thread issuing per_thread (1, 2, 4, 8 or 16)
+ * independent 16-byte loads together; block b writes out[b], the fp32 sum of
+ * elements [b*1024*per_thread, (b+1)*1024*per_thread) in a fixed order.  out
+ * holds tm_read_probe_blocks(n, per_thread) floats and must not overlap x.
+ * tm_read_probe_blocks returns -1 for a bad n or per_thread.
+ * Errors: INVALID_ARG, MISALIGNED, CUDA.
+ */
+int64_t tm_read_probe_blocks(int64_t n, int32_t per_thread);
+tm_status tm_read_probe(const float *x, int64_t n, float *out, int32_t per_thread, tm_stream_t stream);
+
+/*
  * tm_scale2d_unchecked -- tm_scale2d on its TM_ALIGNED path without the host
  * promise check, so the kernel's own entry check is what stands between a
  * broken promise and the tensor's end.  With a broken promise no element is

@@ -264,8 +264,10 @@ __global__ void __launch_bounds__(256) colsum_finish(const float *__restrict__ p
 }
 
 // ------------------------------------------------------------------ REGDIRECT
+// Four blocks per SM: room for all UNR vector loads of a batch in registers
+// (at eight blocks and 32 registers part of every batch was serialised).
 template <int TN, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, 8) colsum_regdirect(const ColArgs a)
+__global__ void __launch_bounds__(kThreads, 4) colsum_regdirect(const ColArgs a)
 {
     constexpr int EW = VEC ? 4 : 1;
     constexpr int CL = TN / EW;           // column lanes
@@ -343,10 +345,11 @@ __global__ void __launch_bounds__(kThreads, 8) colsum_regdirect(const ColArgs a)
 // rank 0 adds the CS partials over distributed shared memory, in rank order,
 // and writes c.  No workspace and no second pass.  IT is the type of element
 // offsets: uint32_t when (M + 128) * ldx fits 32 bits (host-checked), which
-// keeps the kernel at 32 registers -- eight CTAs per SM, so 16 CTAs per strip
-// stay within one wave even at [8192, 8192].
+// saves registers.  Four CTAs per SM, each free to hold all UNR loads of a
+// batch in flight (at eight CTAs, capped at 32 registers, the compiler
+// serialised part of every batch: [8192, 8192] 41.1 against 39.7 us).
 template <int TN, int CS, bool VEC, bool ALIGNED, typename IT>
-__global__ void __launch_bounds__(kThreads, 8) colsum_cluster(const ColArgs a, int64_t rows_per_cta)
+__global__ void __launch_bounds__(kThreads, 4) colsum_cluster(const ColArgs a, int64_t rows_per_cta)
 {
     constexpr int EW = VEC ? 4 : 1;
     constexpr int CL = TN / EW;           // column lanes

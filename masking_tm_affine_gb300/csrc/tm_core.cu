@@ -65,6 +65,35 @@ __global__ void tile_walk_probe_kernel(int64_t K, int64_t T, int64_t *out4)
     out4[3] = w.iters;
 }
 
+// The plain streaming read tm_read_probe times: a flat grid, each thread U
+// independent 16-byte loads issued together, one sum per block.
+template <int U>
+__global__ void __launch_bounds__(kThreads) read_probe_kernel(const float *__restrict__ x, int64_t n4,
+                                                              float *__restrict__ out)
+{
+    __shared__ float wsum[kThreads / 32];
+    const int64_t base = (int64_t)blockIdx.x * kThreads * U + threadIdx.x;
+    u32x4 v[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+        const int64_t i = base + (int64_t)q * kThreads;
+        v[q] = i < n4 ? ld_nc_v4(x + 4 * i) : u32x4{{0u, 0u, 0u, 0u}};
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int q = 0; q < U; ++q) s += (as_f(v[q].v[0]) + as_f(v[q].v[1])) + (as_f(v[q].v[2]) + as_f(v[q].v[3]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = wsum[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) t += wsum[w];
+        out[blockIdx.x] = t;
+    }
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -136,5 +165,39 @@ extern "C" tm_status tm_tile_walk_probe(int64_t K, int32_t T, int64_t *out4, tm_
     tm_status st = device_info(&dev);
     if (st != TM_OK) return st;
     tile_walk_probe_kernel<<<1, 1, 0, as_stream(stream)>>>(K, T, out4);
+    return launch_status();
+}
+
+extern "C" int64_t tm_read_probe_blocks(int64_t n, int32_t per_thread)
+{
+    if (n < 0 || n % 4 != 0 || !(per_thread == 1 || per_thread == 2 || per_thread == 4 || per_thread == 8 ||
+                                  per_thread == 16))
+        return -1;
+    const int64_t per_block = (int64_t)kThreads * per_thread * 4;
+    return (n + per_block - 1) / per_block;
+}
+
+extern "C" tm_status tm_read_probe(const float *x, int64_t n, float *out, int32_t per_thread, tm_stream_t stream)
+{
+    const int64_t blocks = tm_read_probe_blocks(n, per_thread);
+    if (blocks < 0 || blocks > INT32_MAX) return TM_ERR_INVALID_ARG;
+    if (n == 0) return TM_OK;
+    if (x == nullptr || out == nullptr) return TM_ERR_INVALID_ARG;
+    if (!aligned_to(x, 16) || !aligned_to(out, 4)) return TM_ERR_MISALIGNED;
+    const uintptr_t xlo = reinterpret_cast<uintptr_t>(x), xhi = xlo + (uintptr_t)n * 4;
+    const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + (uintptr_t)blocks * 4;
+    if (!(xhi <= olo || ohi <= xlo)) return TM_ERR_INVALID_ARG;
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    const int64_t n4 = n / 4;
+    cudaStream_t s = as_stream(stream);
+    switch (per_thread) {
+    case 1: read_probe_kernel<1><<<(unsigned)blocks, kThreads, 0, s>>>(x, n4, out); break;
+    case 2: read_probe_kernel<2><<<(unsigned)blocks, kThreads, 0, s>>>(x, n4, out); break;
+    case 4: read_probe_kernel<4><<<(unsigned)blocks, kThreads, 0, s>>>(x, n4, out); break;
+    case 8: read_probe_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(x, n4, out); break;
+    default: read_probe_kernel<16><<<(unsigned)blocks, kThreads, 0, s>>>(x, n4, out); break;
+    }
     return launch_status();
 }

@@ -17,6 +17,8 @@ Workloads (sizes from the pages; distributions and seeds fixed here):
   extents multiples of 4 but not of the tile).
 * ``coalesce_4096`` -- [4096, 4096], U[0, 1), seed 3
   ("Memory Coalescing and Tensor Layout", "What it actually costs": 64 MB).
+* ``aligned_4096`` -- [4096, 1000], U[-8, 8), seed 2, tiles 8 x 8: the ragged
+  workload's bytes on whole tiles (a measurement companion, not a page workload).
 * ``rowmax_8192``  -- [8192, 1000], U[-30, -1), seed 4, BC = 64
   ("Slicing, bounds and masking", "Reductions over a ragged tile": negative
   scores, last column tile ragged).
@@ -69,6 +71,10 @@ WORKLOADS = {
     "ragged_4100": dict(kind="copy_scale", M=4100, N=1000, dist=("uniform", -8.0, 8.0), seed=2,
                         TM=64, TN=64, alpha=1.5),
     "coalesce_4096": dict(kind="sums", M=4096, N=4096, dist=("uniform", 0.0, 1.0), seed=3),
+    # the ragged workload's aligned companion: nearly the same bytes on whole
+    # 8 x 8 tiles, so that a ragged-minus-aligned gap is the cost of masking
+    "aligned_4096": dict(kind="copy_scale", M=4096, N=1000, dist=("uniform", -8.0, 8.0), seed=2,
+                         TM=8, TN=8, alpha=1.5),
     "rowmax_8192": dict(kind="rowmax", M=8192, N=1000, dist=("uniform", -30.0, -1.0), seed=4,
                         BC=64),
     # per-channel scale and bias ("Memory Coalescing and Tensor Layout", "NCHW versus

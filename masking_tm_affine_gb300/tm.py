@@ -76,6 +76,8 @@ SIGNATURES = {
     "tm_tile_walk_probe": (_st, [_i64, _i32, _vp, _vp]),
     "tm_scale2d_unchecked": (_st, [_vp, _i64, _vp, _i64, _i64, _i64, _f32, _i32, _i32, _vp]),
     "tm_wait_timeout_probe": (_st, [_vp]),
+    "tm_read_probe_blocks": (_i64, [_i64, _i32]),
+    "tm_read_probe": (_st, [_vp, _i64, _vp, _i32, _vp]),
 }
 
 _lib = None
@@ -236,6 +238,15 @@ def tm_check(stream=None) -> None:
 
 def tm_tile_walk_probe(K: int, T: int, out4, stream=None) -> None:
     _ok(load().tm_tile_walk_probe(K, T, _ptr(out4), _stream(stream)), "tm_tile_walk_probe")
+
+
+def tm_read_probe_blocks(n: int, per_thread: int = 4) -> int:
+    return int(load().tm_read_probe_blocks(n, per_thread))
+
+
+def tm_read_probe(x, n: int, out, per_thread: int = 4, stream=None) -> None:
+    """The plain streaming read of n floats (one fp32 sum per 1024*per_thread elements)."""
+    _ok(load().tm_read_probe(_ptr(x), n, _ptr(out), per_thread, _stream(stream)), "tm_read_probe")
 
 
 def tm_wait_timeout_probe(stream=None) -> None:

@@ -114,6 +114,15 @@ def test_reduction_host_validation(lib):
     assert st("tm_colsum", P0, 4096, 4096, 4000, P1, P1 + (1 << 30), ws, 32, 128, 0, A, None) \
         == tm.TM_ERR_BROKEN_PROMISE
     assert st("tm_tile_walk_probe", 10, 0, P0, None) == tm.TM_ERR_INVALID_ARG
+    # the streaming-read probe: n % 4, per_thread, alignment, overlap
+    assert tm.tm_read_probe_blocks(1 << 24, 4) == 4096 and tm.tm_read_probe_blocks(4100, 1) == 5
+    assert tm.tm_read_probe_blocks(6, 4) == -1 and tm.tm_read_probe_blocks(8, 3) == -1
+    assert st("tm_read_probe", P0, 6, P1, 4, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_read_probe", P0, 8, P1, 5, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_read_probe", None, 8, P1, 4, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_read_probe", P0 + 4, 8, P1, 4, None) == tm.TM_ERR_MISALIGNED
+    assert st("tm_read_probe", P0, 1 << 20, P0 + 64, 4, None) == tm.TM_ERR_INVALID_ARG  # out inside x
+    assert st("tm_read_probe", P0, 0, None, 4, None) == tm.TM_OK                      # nothing to read
 
 
 def test_overlap_flag_host_validation(lib):

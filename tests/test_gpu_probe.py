@@ -1,12 +1,15 @@
 """The device-side tile-walk planner every kernel uses, read back through
 tm_tile_walk_probe, against the page's worked example and the closed form
-("Slicing, bounds and masking", "Loops over a dynamic extent")."""
+("Slicing, bounds and masking", "Loops over a dynamic extent"); and the
+streaming-read probe the reductions' floor is measured with, against the
+oracle's sums of the same blocks."""
 import numpy as np
 import pytest
 import torch
 
 from conftest import read_golden
-from masking_tm_affine_gb300 import tm
+from gpu_util import DevBuf
+from masking_tm_affine_gb300 import synth, tm
 
 pytestmark = pytest.mark.gpu
 
@@ -50,3 +53,22 @@ def test_bounded_wait_times_out_and_context_survives(cuda):
     tm.tm_affine(a, out, 1000)
     tm.tm_check()
     assert torch.equal(out, a * 2 + 1)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("per_thread", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("n", [4096 * 4096, 1 << 20, 1024 * 16 * 3 + 4 * 37])
+def test_read_probe_block_sums(cuda, oracle, per_thread, n):
+    # block b sums elements [b*1024*U, (b+1)*1024*U); the last block may be ragged
+    x = synth.uniform((n,), 0.0, 1.0, 40)
+    blocks = tm.tm_read_probe_blocks(n, per_thread)
+    span = 1024 * per_thread
+    assert blocks == -(-n // span)
+    padded = np.zeros(blocks * span, np.float32)
+    padded[:n] = x
+    want = oracle.rowsum(padded, span, blocks, span)
+    out = DevBuf.empty(blocks)
+    tm.tm_read_probe(DevBuf(x).ptr, n, out.ptr, per_thread)
+    tm.tm_check()
+    assert out.guards_intact()
+    assert np.all(np.abs(out.payload_f32() - want) <= 1e-5 * want)
