@@ -104,7 +104,8 @@ typedef enum tm_variant {
     /* tm_colsum ("Memory Coalescing and Tensor Layout", "What it actually costs",
      * "Seeing it in a real kernel") */
     TM_VAR_NAIVE = 5,     /* the column walk: 256-lane programs over rows, stride ld between lanes */
-    TM_VAR_STAGED = 6,    /* TMA tiles staged in shared memory, columns reduced from there */
+    TM_VAR_STAGED = 6,    /* TMA tiles staged in shared memory, columns reduced from there; a cluster per strip
+                             adds the partials over distributed shared memory (no workspace) */
     TM_VAR_REGDIRECT = 7, /* lanes over columns: coalesced row segments straight into registers */
     TM_VAR_CLUSTER = 8    /* REGDIRECT's layout in one pass: clusters of 8 or 16 CTAs split a strip's rows and add
                              their partials over distributed shared memory (no workspace) */
@@ -249,24 +250,27 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  * TN-column strip is a single row chunk -- tm_colsum_workspace_bytes returns
  * 0: at most max(64, TM) rows, or 8192 strips and more -- the first pass
  * writes c itself and needs no workspace.
- * TM_VAR_CLUSTER instead adds the partials of a strip's row chunks on chip
- * (a thread-block cluster's distributed shared memory), also in a fixed
- * order, in one pass.
+ * TM_VAR_CLUSTER and TM_VAR_STAGED instead add the partials of a strip's row
+ * chunks on chip (a thread-block cluster's distributed shared memory), also
+ * in a fixed order, in one pass; with the 16-byte path both give the same
+ * bits.
  *   X, ldx      device input [M, ldx]        c   device output, N floats
  *   workspace   device scratch of >= tm_colsum_workspace_bytes(...) bytes,
  *               16-byte aligned (128-byte alignment lets the second pass drop
  *               the partials from L2 without writing them back), owned by the
  *               caller; its contents on entry do not matter and on exit are
  *               unspecified.  NULL allowed when tm_colsum_workspace_bytes is 0
- *               (TM_VAR_CLUSTER always, the others for single-chunk strips)
+ *               (TM_VAR_CLUSTER and TM_VAR_STAGED always, the others for
+ *               single-chunk strips)
  *   TM, TN      row tile x column strip: TM in 8..256 (powers of two),
  *               TN in 64, 128, 256; TM*TN <= 8192 for STAGED
  *               (NAIVE ignores them: its programs are 256 rows x 1 column)
  *   variant     TM_VAR_AUTO (the fastest measured: CLUSTER whenever all its
  *               clusters fit on the GPU at once -- e.g. [4096, 4096] and
- *               [8192, 8192] at TN 128 -- else REGDIRECT), _NAIVE, _STAGED,
- *               _REGDIRECT, _CLUSTER (16 CTAs per strip when there are few
- *               strips, else 8); the workspace AUTO sizes is passed either way
+ *               [8192, 8192] at TN 128 -- else REGDIRECT), _NAIVE,
+ *               _REGDIRECT, _CLUSTER and _STAGED (16 CTAs per strip when there
+ *               are few strips, else 8); the workspace AUTO sizes is passed
+ *               either way
  *   flags       TM_ALIGNED (whole row tiles and strips: no masks), TM_PATH_SCALAR,
  *               TM_PDL (the first pass overlaps the previous kernel; the
  *               finish pass of a two-pass variant always overlaps the first)
@@ -326,7 +330,8 @@ tm_status tm_softmax_rowstats(const float *S, int64_t lds, int64_t M, int64_t N,
  *   the workspace.  Returns TM_ERR_WORKSPACE (nothing launched) when the
  *   arguments need more scratch than TM_NOALLOC_SCRATCH_BYTES, i.e. when
  *   tm_colsum_workspace_bytes(M, N, TM, TN, variant) exceeds it.
- *   TM_VAR_CLUSTER needs no scratch and so runs at any shape.
+ *   TM_VAR_CLUSTER and TM_VAR_STAGED need no scratch and so run at any
+ *   shape.
  *   The first call on each device that needs scratch looks up the array's
  *   device address with cudaGetSymbolAddress while that device is current,
  *   and keeps it for the life of the process; make that first call before

@@ -442,22 +442,38 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_cluster(const ColArgs a, i
 }
 
 // ------------------------------------------------------------------ STAGED (TMA)
-template <int TM, int TN, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads, 6) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
-                                                          int stages)
+// The page's fix on GB300: tiles are loaded once into fast on-chip memory and
+// read there in any order.  The CS CTAs of a cluster split the row tiles of
+// one TN-column strip; each streams its TM x TN tiles through a ring of
+// `stages` shared-memory stages filled by the TMA engine (one thread issues
+// cp.async.bulk.tensor copies into this CTA's own shared memory, an mbarrier
+// per stage counts the bytes in), and the threads read columns back out: lane
+// (cl, rl) adds rows rl, rl + RL, ... of every tile, in order.  TMA fills rows
+// past M and columns past N with 0, the masked-load value of "Slicing, bounds
+// and masking" ("Masking").  The CTAs' partials then meet over distributed
+// shared memory as in the cluster form: one pass, no workspace.  With the
+// same tile-aligned row split, lanes and order as colsum_cluster's 16-byte
+// path, the two give the same bits.  Every wait is bounded; a CTA whose wait
+// gives up records TM_ERR_TIMEOUT, drains the copies it started (bounded) and
+// still meets its cluster at both barriers.
+template <int TN, int CS, bool ALIGNED>
+__global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
+                                                          int TM, int64_t tiles_per_cta, int stages)
 {
-    pdl_trigger();  // the finish may launch once every block has started
-    constexpr int CL = TN / 4;            // column lanes, 4 columns each
-    constexpr int RL = kThreads / CL;     // row lanes
-    constexpr int TILE = TM * TN;         // floats per stage
-    static_assert(TM % RL == 0, "tile height must cover the row lanes");
+    constexpr int CL = TN / 4;         // column lanes, 4 columns each
+    constexpr int RL = kThreads / CL;  // row lanes
     extern __shared__ __align__(128) unsigned char smem[];
+    const int tile = TM * TN;          // floats per stage
     float *tiles = reinterpret_cast<float *>(smem);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * TILE * sizeof(float));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * tile * sizeof(float));
     __shared__ __align__(16) float red[RL][TN];
+    __shared__ float part[TN];
     __shared__ int abort_flag;
 
+    pdl_trigger();
     if constexpr (ALIGNED) {
+        // a pure function of the arguments: every CTA of every cluster returns
+        // together, so no CTA is left waiting at a cluster barrier
         const bool whole = (a.M % TM == 0) && (a.N % TN == 0);
         if (!whole) {
             if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, kStatusBrokenPromise);
@@ -465,96 +481,92 @@ __global__ void __launch_bounds__(kThreads, 6) colsum_staged(const __grid_consta
             return;
         }
     }
-    if (blockIdx.x >= a.units) {
-        pdl_wait();
-        return;
-    }
     const int tid = threadIdx.x;
     const int cl = tid % CL, rl = tid / CL;
-    const int64_t my_units = (a.units - blockIdx.x + gridDim.x - 1) / gridDim.x;
-    const int64_t slots = my_units * a.CT;
+    const int64_t strip = blockIdx.x / CS;
+    const int64_t t0 = (int64_t)cluster_rank() * tiles_per_cta;  // this CTA's first row tile
+    const int64_t t1 = t0 + tiles_per_cta < a.RT ? t0 + tiles_per_cta : a.RT;
+    const int n = t1 > t0 ? (int)(t1 - t0) : 0;
 
     if (tid == 0) {
         abort_flag = 0;
-        for (int s = 0; s < stages; ++s)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[s])) : "memory");
+        for (int st = 0; st < stages; ++st)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[st])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-
-    // slot k of this block's tile stream -> (strip, chunk, row tile)
-    auto decode = [&](int64_t k, int64_t &s, int64_t &p, int64_t &rt) {
-        const int64_t u = blockIdx.x + (k / a.CT) * (int64_t)gridDim.x;
-        s = u % a.S;
-        p = u / a.S;
-        rt = p * a.CT + k % a.CT;
-        return rt < a.RT;  // trailing slots of a short last chunk do not exist
-    };
-    auto issue = [&](int64_t k) {
-        if (k >= slots) return;
-        int64_t s, p, rt;
-        if (!decode(k, s, p, rt)) return;
-        const int st = (int)(k % stages);
+    auto issue = [&](int k) {
+        if (k >= n) return;
+        const int st = k % stages;
         const uint32_t bar = smem_u32(&full[st]);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"((uint32_t)(TILE * sizeof(float)))
+                     "r"((uint32_t)(tile * sizeof(float)))
                      : "memory");
         asm volatile(
             "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(tiles + (size_t)st * TILE)),
-            "l"(&tmap), "r"((int)(s * TN)), "r"((int)(rt * TM)), "r"(bar)
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(tiles + (size_t)st * tile)),
+            "l"(&tmap), "r"((int)(strip * TN)), "r"((int)((t0 + k) * TM)), "r"(bar)
             : "memory");
     };
-
     if (tid == 0)
         for (int k = 0; k < stages; ++k) issue(k);
 
-    uint32_t phase = 0;  // bit s: parity of the next completion of stage s
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    bool aborted = false;
-    for (int64_t k = 0; k < slots; ++k) {
-        int64_t s, p, rt;
-        const bool exists = decode(k, s, p, rt);
-        const int st = (int)(k % stages);
-        if (exists) {
-            if (!mbar_wait_bounded(smem_u32(&full[st]), (phase >> st) & 1u)) {
-                report(a.status, kStatusTimeout);
-                abort_flag = 1;
-            } else {
-                const float *t = tiles + (size_t)st * TILE;
-#pragma unroll
-                for (int rr = rl; rr < TM; rr += RL) {
-                    const float4 v = *reinterpret_cast<const float4 *>(t + rr * TN + cl * 4);
-                    acc[0] += v.x;
-                    acc[1] += v.y;
-                    acc[2] += v.z;
-                    acc[3] += v.w;
-                }
+    uint32_t phase = 0;  // bit st: parity of the next completion of stage st
+    int k = 0;
+    for (; k < n; ++k) {
+        const int st = k % stages;
+        if (!mbar_wait_bounded(smem_u32(&full[st]), (phase >> st) & 1u)) {
+            report(a.status, kStatusTimeout);
+            abort_flag = 1;
+        } else {
+            const float *t = tiles + (size_t)st * tile;
+            for (int rr = rl; rr < TM; rr += RL) {
+                const float4 v = *reinterpret_cast<const float4 *>(t + rr * TN + cl * 4);
+                acc[0] += v.x;
+                acc[1] += v.y;
+                acc[2] += v.z;
+                acc[3] += v.w;
             }
-            phase ^= 1u << st;
         }
-        if (k % a.CT == a.CT - 1 || k == slots - 1) {
-            // end of a unit: its partial (TMA zero-filled the columns past N)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                red[rl][cl * 4 + e] = acc[e];
-                acc[e] = 0.0f;
-            }
-            __syncthreads();
-            store_unit<TN, RL>(a, s, p, red);
-        }
-        __syncthreads();  // every read of stage st (and of red) is done
-        if (abort_flag) {
-            aborted = true;
-            break;
-        }
+        phase ^= 1u << st;
+        __syncthreads();  // every read of stage st is done
+        if (abort_flag) break;
         if (tid == 0) issue(k + stages);
     }
-    if (aborted && tid == 0) {
-        // let copies still in flight land before the block's shared memory goes away
-        for (int st = 0; st < stages; ++st) mbar_wait_bounded(smem_u32(&full[st]), (phase >> st) & 1u);
+    if (k < n && tid == 0) {
+        // a wait gave up at tile k: the copies of tiles k .. k + stages - 1
+        // may still be in flight; let them land before the block's shared
+        // memory goes away (tile j is use j / stages of its stage, whose
+        // completion has that parity; each wait bounded as well)
+        for (int j = k; j < n && j < k + stages; ++j)
+            mbar_wait_bounded(smem_u32(&full[j % stages]), (uint32_t)((j / stages) & 1));
     }
-    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
+
+#pragma unroll
+    for (int e = 0; e < 4; ++e) red[rl][cl * 4 + e] = acc[e];
+    __syncthreads();
+    if (rl == 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float t = red[0][cl * 4 + e];
+#pragma unroll
+            for (int q = 1; q < RL; ++q) t += red[q][cl * 4 + e];
+            part[cl * 4 + e] = t;
+        }
+    }
+    cluster_sync();  // every CTA's partial of this strip is in its shared memory
+    if (cluster_rank() == 0 && tid < TN) {
+        const uint32_t mine = smem_u32(&part[tid]);
+        float t = 0.0f;
+#pragma unroll 4
+        for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
+        const int64_t col = strip * TN + tid;
+        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
+        if (col < a.N) a.c[col] = t;
+    }
+    cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
+    pdl_wait();      // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ host side
@@ -566,14 +578,15 @@ bool staged_tile(int TM, int TN)
     return TM >= 1024 / TN && TM <= 256;
 }
 
-// A ring of ~16 KB (at least two stages) per block: small rings let more
-// blocks share an SM, and more blocks streaming at once beat deeper rings
-// (8192^2, 32 x 128 tiles: 61.1 us with 2 stages and 5 blocks per SM, 65.2 us
-// with 4 stages and 3 blocks, 118.9 us with 8 stages and 1 block).
+// The ring of the staged form: about 32 KB per CTA (at least two stages),
+// which leaves room for five or six CTAs per SM; a TMA streaming experiment
+// on this GPU found many CTAs with shallow rings faster than few CTAs with
+// deep ones ([4096, 4096]: 14.1 us with two 16 KB stages at five CTAs per SM
+// against 16.1 us with twelve stages at one).
 int staged_stages(int TM, int TN)
 {
     const int bytes = TM * TN * 4;
-    int s = (16 * 1024) / bytes;
+    int s = (32 * 1024) / bytes;
     if (s < 2) s = 2;
     if (s > 8) s = 8;
     return s;
@@ -584,57 +597,10 @@ bool pow2_in(int v, int lo, int hi)
     return v >= lo && v <= hi && (v & (v - 1)) == 0;
 }
 
-// Persistent: as many blocks as fit on the SMs at once, each streaming its
-// units' tiles through one ring (a block's stream runs on across unit
-// boundaries).  One block per unit, as for the register-direct pass, left
-// each block two tiles at 8192 x 8192 (32 x 128) and a TMA round trip per
-// 32 KB: 52.0 us kernel time (ncu) against 46.9 us persistent.
-template <int TM, int TN>
-tm_status launch_staged_t(bool aligned, const CUtensorMap &map, const ColArgs &a, int sms, cudaStream_t s, bool pdl)
+template <int TN, int CS>
+const void *staged_kernel(bool aligned)
 {
-    const void *k = aligned ? (const void *)colsum_staged<TM, TN, true> : (const void *)colsum_staged<TM, TN, false>;
-    const int max_stages = staged_stages(TM, TN);
-    const int64_t block_smem = (int64_t)max_stages * TM * TN * sizeof(float) + 8 * 1024;  // ring + static arrays
-    int64_t per_sm = (int64_t)(227 * 1024) / block_smem;
-    per_sm = per_sm < 1 ? 1 : (per_sm > 8 ? 8 : per_sm);
-    const int64_t grid = a.units < per_sm * sms ? a.units : per_sm * sms;
-    // a block that holds one unit needs no deeper ring than the unit's CT tiles
-    int stages = (a.units <= grid && a.CT < max_stages) ? (int)a.CT : max_stages;
-    const size_t max_smem = (size_t)max_stages * TM * TN * sizeof(float) + (size_t)max_stages * sizeof(uint64_t);
-    const size_t smem = (size_t)stages * TM * TN * sizeof(float) + (size_t)stages * sizeof(uint64_t);
-    static std::once_flag attr_once[kMaxDevices][2];
-    int devno = 0;
-    cudaGetDevice(&devno);
-    bool attr_ok = true;
-    std::call_once(attr_once[devno][aligned ? 1 : 0], [&] {
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem) != cudaSuccess) {
-            cudaGetLastError();
-            attr_ok = false;
-        }
-    });
-    if (!attr_ok) return TM_ERR_CUDA;
-    void *args[] = {const_cast<CUtensorMap *>(&map), const_cast<ColArgs *>(&a), &stages};
-    return launch_kernel(k, dim3(flat_grid(grid)), dim3(kThreads), args, smem, s, pdl);
-}
-
-tm_status launch_staged(int TM, int TN, bool aligned, const CUtensorMap &map, const ColArgs &a, int sms,
-                        cudaStream_t s, bool pdl)
-{
-#define TM_STAGED(tm_, tn_) \
-    if (TM == tm_ && TN == tn_) return launch_staged_t<tm_, tn_>(aligned, map, a, sms, s, pdl);
-    TM_STAGED(16, 64)
-    TM_STAGED(32, 64)
-    TM_STAGED(64, 64)
-    TM_STAGED(128, 64)
-    TM_STAGED(8, 128)
-    TM_STAGED(16, 128)
-    TM_STAGED(32, 128)
-    TM_STAGED(64, 128)
-    TM_STAGED(8, 256)
-    TM_STAGED(16, 256)
-    TM_STAGED(32, 256)
-#undef TM_STAGED
-    return TM_ERR_UNSUPPORTED_TILE;
+    return aligned ? (const void *)colsum_staged<TN, CS, true> : (const void *)colsum_staged<TN, CS, false>;
 }
 
 template <int TN>
@@ -759,10 +725,49 @@ tm_status launch_cluster(int TN, int CS, bool vec, bool aligned, const ColArgs &
     int max_active;
     const tm_status st = cluster_prepare(k, CS, &max_active);
     if (st != TM_OK) return st;
-    int64_t rows_per_cta = (a.M + CS - 1) / CS;
+    // whole row tiles per CTA (the split the staged form uses too)
+    int64_t rows_per_cta = (a.RT + CS - 1) / CS * a.TM;
     const int64_t strips = (a.N + TN - 1) / TN;
     void *args[] = {const_cast<ColArgs *>(&a), &rows_per_cta};
     return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, 0, s, pdl, (unsigned)CS);
+}
+
+// The staged form: clusters of CS CTAs per strip, each streaming whole row
+// tiles through its TMA ring.  Per kernel and device, once: the largest ring
+// (two 32 KB stages) and, for 16-CTA clusters, the non-portable cluster size.
+tm_status launch_staged(int TM, int TN, int CS, bool aligned, const CUtensorMap &map, const ColArgs &a,
+                        cudaStream_t s, bool pdl)
+{
+    const int kidx = (TN == 64 ? 0 : TN == 128 ? 1 : 2) * 4 + (CS == 16 ? 2 : 0) + (aligned ? 1 : 0);
+    const void *k;
+    switch (TN) {
+    case 64: k = CS == 16 ? staged_kernel<64, 16>(aligned) : staged_kernel<64, 8>(aligned); break;
+    case 128: k = CS == 16 ? staged_kernel<128, 16>(aligned) : staged_kernel<128, 8>(aligned); break;
+    default: k = CS == 16 ? staged_kernel<256, 16>(aligned) : staged_kernel<256, 8>(aligned); break;
+    }
+    static std::once_flag once[kMaxDevices][12];
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess || devno < 0 || devno >= kMaxDevices) {
+        cudaGetLastError();
+        return TM_ERR_CUDA;
+    }
+    bool ok = true;
+    std::call_once(once[devno][kidx], [&] {
+        const int most = 2 * 8192 * (int)sizeof(float) + 2 * (int)sizeof(uint64_t);
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess ||
+            (CS > 8 && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+            cudaGetLastError();
+            ok = false;
+        }
+    });
+    if (!ok) return TM_ERR_CUDA;
+    int stages = staged_stages(TM, TN);
+    int64_t tiles_per_cta = (a.RT + CS - 1) / CS;
+    if (tiles_per_cta < stages) stages = tiles_per_cta > 2 ? (int)tiles_per_cta : 2;  // no deeper than its tiles
+    const size_t smem = (size_t)stages * TM * TN * sizeof(float) + (size_t)stages * sizeof(uint64_t);
+    const int64_t strips = (a.N + TN - 1) / TN;
+    void *args[] = {const_cast<CUtensorMap *>(&map), const_cast<ColArgs *>(&a), &TM, &tiles_per_cta, &stages};
+    return launch_kernel(k, dim3((unsigned)(strips * CS)), dim3(kThreads), args, smem, s, pdl, (unsigned)CS);
 }
 
 // CTAs per strip in the cluster variant: 16 (non-portable clusters) when there
@@ -787,12 +792,12 @@ using namespace libtm;
 extern "C" size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, tm_variant variant)
 {
     if (M <= 0 || N <= 0) return 0;
-    if (variant == TM_VAR_CLUSTER) return 0;  // partials stay on chip
+    if (variant == TM_VAR_CLUSTER || variant == TM_VAR_STAGED) return 0;  // partials meet on chip
     if (variant == TM_VAR_NAIVE) {
         const int64_t rb = (M + kNaiveRows - 1) / kNaiveRows;
         return (size_t)(rb * ((N + 3) & ~int64_t(3)) * (int64_t)sizeof(float));
     }
-    if (variant != TM_VAR_AUTO && variant != TM_VAR_STAGED && variant != TM_VAR_REGDIRECT) return 0;
+    if (variant != TM_VAR_AUTO && variant != TM_VAR_REGDIRECT) return 0;
     if (!pow2_in(TM, 8, 256) || !(TN == 64 || TN == 128 || TN == 256)) return 0;
     return (size_t)partial_bytes(plan_chunks(M, N, TM, TN), TN);
 }
@@ -840,7 +845,8 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
             if (!(xhi <= wlo || whi <= xlo) || !(chi <= wlo || whi <= clo)) return TM_ERR_INVALID_ARG;
         }
         if (variant != TM_VAR_NAIVE) pl = plan_chunks(M, N, TM, TN);
-        if (variant == TM_VAR_CLUSTER && (N + TN - 1) / TN * kClusterCTAsTall > INT32_MAX) return TM_ERR_INVALID_ARG;
+        if ((variant == TM_VAR_CLUSTER || variant == TM_VAR_STAGED) && (N + TN - 1) / TN * kClusterCTAsTall > INT32_MAX)
+            return TM_ERR_INVALID_ARG;
     }
     const bool tma_shape = vec16 && M <= INT32_MAX && N <= INT32_MAX && staged_tile(TM, TN) &&
                            !(flags & (TM_PATH_SCALAR | TM_PATH_VEC));
@@ -912,13 +918,12 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
                                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return TM_ERR_CUDA;
-        st = launch_staged(TM, TN, aligned, map, a, dev->sms, s, pdl);
-    } else {
-        switch (TN) {
-        case 64: st = launch_regdirect_t<64>(vec, aligned, a, s, pdl); break;
-        case 128: st = launch_regdirect_t<128>(vec, aligned, a, s, pdl); break;
-        default: st = launch_regdirect_t<256>(vec, aligned, a, s, pdl); break;
-        }
+        return launch_staged(TM, TN, cluster_ctas(pl.S, dev->sms), aligned, map, a, s, pdl);
+    }
+    switch (TN) {
+    case 64: st = launch_regdirect_t<64>(vec, aligned, a, s, pdl); break;
+    case 128: st = launch_regdirect_t<128>(vec, aligned, a, s, pdl); break;
+    default: st = launch_regdirect_t<256>(vec, aligned, a, s, pdl); break;
     }
     if (st != TM_OK || pl.P == 1) return st;  // one chunk per strip: the pass wrote c itself
     return launch_finish_strips(a.part, pl.P, TN, N, c, s);

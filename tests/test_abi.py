@@ -172,14 +172,16 @@ def test_colsum_workspace_plan(lib):
     assert tm.tm_colsum_workspace_bytes(100, 0, 32, 128) == 0
     assert tm.tm_colsum_workspace_bytes(100, 10, 33, 128) == 0
     assert tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128, tm.TM_VAR_CLUSTER) == 0
-    # REGDIRECT / STAGED: a TN-wide partial per (strip, chunk); none when
-    # every strip is one chunk
+    assert tm.tm_colsum_workspace_bytes(4096, 4096, 32, 128, tm.TM_VAR_STAGED) == 0  # partials meet on chip
+    # REGDIRECT (and AUTO, which sizes for it): a TN-wide partial per (strip,
+    # chunk); none when every strip is one chunk
     for M, N, TM, TN in [(4100, 1001, 32, 128), (4096, 4096, 32, 128), (8192, 8192, 32, 128), (8192, 1000, 8, 64),
                          (3, 1 << 20, 8, 256), (1 << 20, 3, 256, 64), (192, 768000, 8, 256)]:
         S, P = colsum_plan(M, N, TM, TN)
         want = 0 if P == 1 else S * P * TN * 4
-        for v in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+        for v in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT):
             assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, v) == want, (M, N, TM, TN, v)
+        assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, tm.TM_VAR_STAGED) == 0
     assert colsum_plan(4100, 1001, 32, 128) == (8, 65)
     assert tm.tm_colsum_workspace_bytes(4100, 1001, 32, 128) == 8 * 65 * 128 * 4
     assert tm.tm_colsum_workspace_bytes(64, 4096, 32, 128) == 0  # one 64-row chunk per strip

@@ -68,13 +68,16 @@ def test_colsum_4096_workload(cuda, oracle, coalesce, variant):
         assert within(got_a, want, want)
 
 
-def test_colsum_staged_equals_regdirect_bitwise(cuda, coalesce):
-    # same rows to the same lanes, same order: identical partial sums
-    x = coalesce[:1000]
-    for TM, TN in [(32, 128), (16, 64), (8, 256), (64, 64)]:
-        a = colsum(x, 4096, 1000, 4096, TM, TN, tm.TM_VAR_STAGED)
-        b = colsum(x, 4096, 1000, 4096, TM, TN, tm.TM_VAR_REGDIRECT)
-        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (TM, TN)
+@pytest.mark.parametrize("M,N", [(1000, 4096), (4096, 4096), (777, 1000), (8192, 4096)])
+def test_colsum_staged_equals_cluster_bitwise(cuda, coalesce, M, N):
+    # the TMA-staged form and the cluster form split a strip's row tiles the
+    # same way over the same cluster and add the same rows to the same lanes
+    # in the same order (TMA's zero fill past M adds +0): identical bits
+    x = coalesce[:M, :N] if M <= 4096 else np.concatenate([coalesce, coalesce])[:, :N]
+    for TM, TN in [(32, 128), (16, 64), (8, 256), (64, 64), (128, 64), (32, 256)]:
+        a = colsum(x, N, M, N, TM, TN, tm.TM_VAR_STAGED)
+        b = colsum(x, N, M, N, TM, TN, tm.TM_VAR_CLUSTER)
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (M, N, TM, TN)
 
 
 def test_colsum_deterministic(cuda, coalesce):
@@ -154,7 +157,7 @@ def test_colsum_workspace_errors(cuda, oracle):
     assert ws > 0
     W = DevBuf.empty(ws // 4, lead=1)     # misaligned scratch
     for ptr, nbytes in [(W.ptr, ws), (W.ptr - 4, ws - 4), (None, 0)]:
-        for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+        for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT):
             with pytest.raises(tm.TmError) as e:
                 tm.tm_colsum(XD.ptr, N, M, N, C.ptr, ptr, nbytes, 32, 128, variant)
             assert e.value.status == tm.TM_ERR_WORKSPACE

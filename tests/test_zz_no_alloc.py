@@ -80,18 +80,20 @@ def test_noalloc_rejects_problems_beyond_its_scratch(cuda, oracle):
     M, N, TM, TN = 192, 768000, 8, 256
     x = synth.uniform((M, N), 0.0, 1.0, 33)
     XD = DevBuf(x)
-    for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT, tm.TM_VAR_STAGED):
+    for variant in (tm.TM_VAR_AUTO, tm.TM_VAR_REGDIRECT):
         assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, variant) > tm.TM_NOALLOC_SCRATCH_BYTES
         C = DevBuf.empty(N)
         rc = tm.load().tm_colsum_noalloc(XD.ptr, N, M, N, C.ptr, TM, TN, variant, 0, None)
         assert rc == tm.TM_ERR_WORKSPACE, variant
         assert tm.load().tm_check(None) == tm.TM_OK
         assert np.all(C.words() == 0xDEADBEEF)
-    # ... except by CLUSTER, which keeps its partials on chip and needs none
-    assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, tm.TM_VAR_CLUSTER) == 0
-    C = DevBuf.empty(N)
-    rc = tm.load().tm_colsum_noalloc(XD.ptr, N, M, N, C.ptr, TM, TN, tm.TM_VAR_CLUSTER, 0, None)
-    assert rc == tm.TM_OK, tm.status_string(rc)
-    assert tm.load().tm_check(None) == tm.TM_OK
-    assert C.guards_intact()
-    assert within(C.payload_f32(), x, oracle.colsum(x, N, M, N))
+    # ... except by CLUSTER and STAGED, which add their partials on chip and
+    # need none
+    for variant in (tm.TM_VAR_CLUSTER, tm.TM_VAR_STAGED):
+        assert tm.tm_colsum_workspace_bytes(M, N, TM, TN, variant) == 0
+        C = DevBuf.empty(N)
+        rc = tm.load().tm_colsum_noalloc(XD.ptr, N, M, N, C.ptr, TM, TN, variant, 0, None)
+        assert rc == tm.TM_OK, tm.status_string(rc)
+        assert tm.load().tm_check(None) == tm.TM_OK
+        assert C.guards_intact()
+        assert within(C.payload_f32(), x, oracle.colsum(x, N, M, N)), variant
