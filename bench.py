@@ -9,8 +9,8 @@ One step is one pass of the whole hot path over one batch: the fp32
   copy2d      B = X, 64 x 64 tiles, aligned promise
   rowsum      r = sum over each row (a block per row, 1024-column tiles)
   colsum      c = sum over each column (32 x 128 strips, AUTO variant: one
-              pass of the register-direct walk, the last block of each strip
-              adding its partials)
+              pass of 8-CTA thread-block clusters, a strip's partials added
+              over distributed shared memory)
   rowmax      m = ragged row max (a block per row), 64-column tiles, -inf fill
 
 Metric: achieved HBM GB/s (GB = 1e9 bytes, the pages' convention) over the
@@ -45,7 +45,7 @@ WORKLOAD = "scale_8192"
 M = N = 8192
 ALPHA = 1.5
 FALLBACK_HBM_GBS = 6800.0
-STEP_LAUNCHES = 7  # affine, scale2d, copy2d, rowsum, colsum (counter clearing + one pass), rowmax
+STEP_LAUNCHES = 6  # affine, scale2d, copy2d, rowsum, colsum (AUTO: one pass of 8-CTA clusters here), rowmax
 ROWSUM_TILE = (1, 1024)   # rows per block x columns per tile
 COLSUM_TILE = (32, 128)   # row tile x column strip
 ROWMAX_BR = 1             # rows per block (column tile BC = 64)
@@ -991,6 +991,9 @@ def time_oracle_case(kern, w, x, budget_s: float = 1.5) -> dict:
         if kern == "rowsum":
             oracle.rowsum(xs, cols, R, cols)
             return 4 * R * cols + 4 * R
+        if kern == "read_probe":  # a plain read of the same bytes: the oracle's row sums of them
+            oracle.rowsum(xs, cols, R, cols)
+            return 4 * R * cols
         if kern == "colsum":
             oracle.colsum(xs, cols, R, cols)
             return 4 * R * cols + 4 * cols
