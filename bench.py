@@ -490,6 +490,7 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
         torch.cuda.synchronize(dev)
         t = e0.elapsed_time(e1) * 1e-3
     else:
+        link = measure_link(hx, bufs["X"], bufs["A1"], dev)
         sets = [bufs, make_buffers(tm, x, dev)[0]]
         steps_of = [step, make_step(tm, sets[1], ws_bytes, stream, first_overlap=False)]
         hosts = [{k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs} for _ in range(2)]
@@ -531,11 +532,67 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
         e1.record(s_in)
         torch.cuda.synchronize(dev)
         t = e0.elapsed_time(e1) * 1e-3
-    return {"value": round(gbps(step_bytes * steps, t), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3), "mode": mode,
-            "path": "pinned host X -> device, the six C-ABI calls, every output -> pinned host"
-                    + (", one stream" if mode == "serial" else
-                       "; copy-in, kernels and copy-out of consecutive steps overlap on three streams")}
+    out = {"value": round(gbps(step_bytes * steps, t), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3), "mode": mode,
+           "path": "pinned host X -> device, the six C-ABI calls, every output -> pinned host"
+                   + (", one stream" if mode == "serial" else
+                      "; copy-in, kernels and copy-out of consecutive steps overlap on three streams")}
+    if mode != "serial":
+        # the host link bounds this number: a step cannot end before its bytes
+        # have crossed it, each direction at its own rate and both together
+        # at the two-way rate
+        floor = max(h2d / link["h2d_GBps"], d2h / link["d2h_GBps"], (h2d + d2h) / link["both_GBps"]) / 1e9
+        out["link"] = {**link, "floor_ms_per_step": round(floor * 1e3, 3),
+                       "frac_of_floor": round(floor / (t / steps), 4)}
+    return out
+
+
+def measure_link(hx, dx, dy, dev, reps=5):
+    """Copy-engine rates of the host link with the e2e run's own pinned buffer:
+    host -> device, device -> host, and both at once on two streams (each a
+    median of `reps` copies of hx's size, after two untimed)."""
+    import torch
+    hy = torch.empty_like(hx).pin_memory()
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    nb = hx.numel() * 4
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            fn()
+            e1.record(s1)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            dx.copy_(hx, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s1):
+            hy.copy_(dy, non_blocking=True)
+
+    def both():
+        ev = torch.cuda.Event()
+        ev.record(s1)
+        s2.wait_event(ev)
+        with torch.cuda.stream(s2):
+            hy.copy_(dy, non_blocking=True)
+        with torch.cuda.stream(s1):
+            dx.copy_(hx, non_blocking=True)
+        s1.wait_stream(s2)
+
+    th, td, tb = timed(h2d), timed(d2h), timed(both)
+    del hy
+    return {"h2d_GBps": round(nb / th / 1e9, 1), "d2h_GBps": round(nb / td / 1e9, 1),
+            "both_GBps": round(2 * nb / tb / 1e9, 1), "bytes_per_copy": nb,
+            "how": "pinned host <-> device copies of X's size on the copy engines, timed in this run"}
 
 
 # --------------------------------------------------------------------- per-config block
@@ -554,7 +611,13 @@ CONFIG_ENTRIES = [
     ("C4_colsum_auto", "C4", "coalesce_4096", "colsum", "auto", 0.70),
     ("C4_colsum_staged", "C4", "coalesce_4096", "colsum", "staged", 0.70),
     ("C5_rowmax_masked", "C5", "rowmax_8192", "rowmax_masked", "neg_inf", None),
+    # the floors C3 and C4 are read against, timed the same way in the same
+    # run: a device-to-device cudaMemcpyAsync of the ragged tensor's bytes,
+    # and the plain streaming read of the 64 MiB the sums read
+    ("C3_floor_memcpy", "C3", "ragged_4100", "memcpy", "d2d", None),
+    ("C4_floor_read", "C4", "coalesce_4096", "read_probe", "u4", None),
 ]
+FLOOR_OF = {"C3": "C3_floor_memcpy", "C4": "C4_floor_read"}
 AMORTIZED_BYTES = 512 << 20  # rotating copies of the inputs and outputs: 4x the L2
 
 
@@ -601,6 +664,27 @@ def config_kernel(tm, kern, path, w, x, dev):
         return ("tm_colsum %s [%d,%d] 32x128 (workspace %d B)" % (path.upper(), M, N, ws), N,
                 lambda X, O, W, s, pdl: tm.tm_colsum(X, N, M, N, O, W, ws, 32, 128, var, tm.TM_PDL if pdl else 0, s),
                 4 * M * N + 4 * N, max(ws // 4, 4), lambda o: bool(np.all(np.abs(o - want) <= tol)))
+    if kern == "memcpy":
+        n = M * N
+        want = x.reshape(-1).view(np.uint32)
+
+        def copy(X, O, W, s, pdl):
+            O.copy_(X, non_blocking=True)  # on torch's current stream: the timed stream, or the capture stream
+        return ("cudaMemcpyAsync device to device, %d bytes (torch copy_)" % (4 * n), n, copy, 8 * n, 0,
+                lambda o: bool(np.array_equal(o.view(np.uint32), want)))
+    if kern == "read_probe":
+        n = M * N
+        U = int(path[1:])
+        blocks = tm.tm_read_probe_blocks(n, U)
+        if (1024 * U) % N or blocks * 1024 * U != n:
+            raise ValueError("read probe blocks must be whole rows of the workload")
+        per = 1024 * U // N  # rows per block
+        xb = x.reshape(blocks, per * N)
+        want = oracle.rowsum(xb, per * N, blocks, per * N)
+        tol = 1e-5 * np.abs(xb.astype(np.float64)).sum(axis=1)
+        return ("tm_read_probe, %d floats, %d 16-byte loads per thread (no TM_PDL: plain launches)" % (n, U), blocks,
+                lambda X, O, W, s, pdl: tm.tm_read_probe(X, n, O, U, s), 4 * n + 4 * blocks, 0,
+                lambda o: bool(np.all(np.abs(o - want) <= tol)))
     if kern == "rowmax_masked":
         BC = w["BC"]
         want = oracle.rowmax_masked(x, N, M, N, BC)
@@ -624,7 +708,21 @@ def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
     from masking_tm_affine_gb300 import synth
     out = {}
     flush = L2Flush(dev, "dirty")
+    flush_clean = L2Flush(dev, "clean")
     inputs = {}
+
+    def lone_times(fl, call, X, O, W, stream, s):
+        ts = []
+        for rep in range(reps + 3):
+            fl()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(X, O, W, s, False)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= 3:
+                ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts), statistics.fmean(ts)
     for key, cfg, wl, kern, path, target in CONFIG_ENTRIES:
         if wl not in inputs:
             inputs[wl] = x_step if (wl == WORKLOAD and x_step is not None) else synth.workload_input(wl)
@@ -644,19 +742,10 @@ def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
         ok = check(Os[0].cpu().numpy()) if verify else None
         if verify and not ok:
             raise AssertionError("%s: output differs from the oracle" % key)
-        # lone launches, L2 flushed before each
-        ts = []
-        for rep in range(reps + 3):
-            flush()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            call(Xs[0], Os[0], W, s, False)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            if rep >= 3:
-                ts.append(e0.elapsed_time(e1) * 1e-3)
-        lone = statistics.median(ts)
-        lone_mean = statistics.fmean(ts)
+        # lone launches, L2 flushed before each: the flush's lines left dirty
+        # (the launch pays their write-back), and cleaned by a read after it
+        lone, lone_mean = lone_times(flush, call, Xs[0], Os[0], W, stream, s)
+        lone_c, lone_c_mean = lone_times(flush_clean, call, Xs[0], Os[0], W, stream, s)
         # back to back: n overlapped calls in one graph, rotating over R copies
         n = max(100, min(1000, int(2e-3 / max(lone_mean, 1e-6)) + 1))
         n = -(-n // R) * R
@@ -687,6 +776,10 @@ def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
                "lone": {"us": round(lone * 1e6, 2), "us_mean": round(lone_mean * 1e6, 2),
                         "GBps": round(gbps(nbytes, lone), 1), "frac": round(gbps(nbytes, lone) / peak, 4),
                         "reps": reps, "l2": "512 MiB dirty flush before each launch"},
+               "lone_clean": {"us": round(lone_c * 1e6, 2), "us_mean": round(lone_c_mean * 1e6, 2),
+                              "GBps": round(gbps(nbytes, lone_c), 1), "frac": round(gbps(nbytes, lone_c) / peak, 4),
+                              "reps": reps, "l2": "512 MiB write then 256 MiB read before each launch: "
+                                                  "cold L2 of clean lines, as under ncu"},
                "back_to_back": {"us_per_call": round(amort * 1e6, 3), "GBps": round(gbps(nbytes, amort), 1),
                                 "frac": round(gbps(nbytes, amort) / peak, 4), "calls": n, "copies": R,
                                 "how": "TM_PDL calls in one CUDA graph; inputs and outputs rotate over the copies "
@@ -694,10 +787,24 @@ def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
                "target": target, "verified": ok}
         if target is not None:
             row["target_met"] = {"lone": row["lone"]["frac"] >= target,
+                                 "lone_clean": row["lone_clean"]["frac"] >= target,
                                  "back_to_back": row["back_to_back"]["frac"] >= target}
         out[key] = row
         del Xs, Os, W, X0, g
         torch.cuda.empty_cache()
+    # each targeted row against its config's floor, timed the same way
+    for key, row in out.items():
+        fk = FLOOR_OF.get(row["config"])
+        if row["target"] is None or fk not in out:
+            continue
+        f = out[fk]
+        row["floor"] = {"entry": fk,
+                        "lone_frac": f["lone"]["frac"], "lone_clean_frac": f["lone_clean"]["frac"],
+                        "lone_vs_floor": round(row["lone"]["us"] / f["lone"]["us"], 3),
+                        "lone_clean_vs_floor": round(row["lone_clean"]["us"] / f["lone_clean"]["us"], 3),
+                        "how": "this row's lone time over the floor's (1.0 = as fast as the floor; "
+                               "per-byte: both move the same input bytes)"}
+        row["target_met"]["lone_within_5pct_of_floor"] = row["lone"]["us"] <= 1.05 * f["lone"]["us"]
     return out
 
 
@@ -855,6 +962,7 @@ CASES = {
     "rowsum_8192sq": ("scale_8192", "rowsum", ["vec"]),
     "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect", "cluster"]),
     "rowmax_8192sq": ("scale_8192", "rowmax_masked", ["neg_inf"]),
+    "read_floor_8192sq": ("scale_8192", "read_probe", ["u4", "u8"]),
     # the tensor-core gemm (3xTF32 by default; tf32 = one pass)
     "gemm_4100": ("gemm_4100", "gemm", ["3xtf32", "tf32"]),
     "gemm_8192": ("gemm_8192", "gemm", ["3xtf32", "tf32"]),

@@ -68,16 +68,29 @@ def test_colsum_4096_workload(cuda, oracle, coalesce, variant):
         assert within(got_a, want, want)
 
 
-@pytest.mark.parametrize("M,N", [(1000, 4096), (4096, 4096), (777, 1000), (8192, 4096)])
+@pytest.mark.parametrize("M,N", [(1000, 1000), (4096, 1000), (777, 1000), (8192, 1000), (4096, 4096), (8192, 4096)])
 def test_colsum_staged_equals_cluster_bitwise(cuda, coalesce, M, N):
-    # the TMA-staged form and the cluster form split a strip's row tiles the
-    # same way over the same cluster and add the same rows to the same lanes
-    # in the same order (TMA's zero fill past M adds +0): identical bits
+    # Both one-pass forms take the same cluster size (16 CTAs per strip for
+    # few strips, else 8), split a strip's row tiles the same way and add the
+    # same rows to the same lanes in the same order (TMA's zero fill past M
+    # adds +0): identical bits
     x = coalesce[:M, :N] if M <= 4096 else np.concatenate([coalesce, coalesce])[:, :N]
     for TM, TN in [(32, 128), (16, 64), (8, 256), (64, 64), (128, 64), (32, 256)]:
         a = colsum(x, N, M, N, TM, TN, tm.TM_VAR_STAGED)
         b = colsum(x, N, M, N, TM, TN, tm.TM_VAR_CLUSTER)
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (M, N, TM, TN)
+
+
+@pytest.mark.parametrize("variant", [tm.TM_VAR_STAGED, tm.TM_VAR_CLUSTER, tm.TM_VAR_AUTO])
+def test_colsum_one_pass_many_strips(cuda, oracle, variant):
+    # many strips: 128 64-column strips of [512, 8192] (8-CTA clusters, all
+    # resident), and 512 256-wide strips of a 2^17-wide matrix (8-CTA
+    # clusters in several waves; AUTO takes the two-pass form there)
+    for M, N, TM, TN in [(512, 8192, 16, 64), (64, 1 << 17, 8, 256), (2048, 8192, 32, 64)]:
+        x = synth.uniform((M, N), 0.0, 1.0, M + N)
+        got = colsum(x, N, M, N, TM, TN, variant)
+        want = oracle.colsum(x, N, M, N)
+        assert within(got, want, want), (variant, M, N, TM, TN)
 
 
 def test_colsum_deterministic(cuda, coalesce):
