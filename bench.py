@@ -538,13 +538,18 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
                    + (", one stream" if mode == "serial" else
                       "; copy-in, kernels and copy-out of consecutive steps overlap on three streams")}
     if mode != "serial":
-        # the host link bounds this number: a step cannot end before its bytes
-        # have crossed it, each direction at its own rate and both together
-        # at the two-way rate
-        floor = max(h2d / link["h2d_GBps"], d2h / link["d2h_GBps"], (h2d + d2h) / link["both_GBps"]) / 1e9
+        floor = link_floor_s(h2d, d2h, link)
         out["link"] = {**link, "floor_ms_per_step": round(floor * 1e3, 3),
                        "frac_of_floor": round(floor / (t / steps), 4)}
     return out
+
+
+def link_floor_s(h2d_bytes, d2h_bytes, link):
+    """Seconds a step needs at least to move its bytes over the host link: each
+    direction at its own measured rate, and both together at the two-way
+    rate (GB/s figures of `measure_link`)."""
+    return max(h2d_bytes / link["h2d_GBps"], d2h_bytes / link["d2h_GBps"],
+               (h2d_bytes + d2h_bytes) / link["both_GBps"]) / 1e9
 
 
 def measure_link(hx, dx, dy, dev, reps=5):
@@ -792,20 +797,27 @@ def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
         out[key] = row
         del Xs, Os, W, X0, g
         torch.cuda.empty_cache()
-    # each targeted row against its config's floor, timed the same way
-    for key, row in out.items():
+    attach_floors(out)
+    return out
+
+
+def attach_floors(rows):
+    """Each targeted row of the configs block against its config's floor row
+    (FLOOR_OF), timed the same way in the same run: its lone times over the
+    floor's, and whether the dirty-flush lone time is within 5 % of it."""
+    for key, row in rows.items():
         fk = FLOOR_OF.get(row["config"])
-        if row["target"] is None or fk not in out:
+        if row["target"] is None or fk not in rows:
             continue
-        f = out[fk]
+        f = rows[fk]
         row["floor"] = {"entry": fk,
                         "lone_frac": f["lone"]["frac"], "lone_clean_frac": f["lone_clean"]["frac"],
                         "lone_vs_floor": round(row["lone"]["us"] / f["lone"]["us"], 3),
                         "lone_clean_vs_floor": round(row["lone_clean"]["us"] / f["lone_clean"]["us"], 3),
                         "how": "this row's lone time over the floor's (1.0 = as fast as the floor; "
-                               "per-byte: both move the same input bytes)"}
+                               "both move the same input bytes)"}
         row["target_met"]["lone_within_5pct_of_floor"] = row["lone"]["us"] <= 1.05 * f["lone"]["us"]
-    return out
+    return rows
 
 
 # --------------------------------------------------------------------- reference arm

@@ -57,3 +57,48 @@ def test_reference_arm_runs_on_rank0_only(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     args = bench.argparse.Namespace(steps=1, warmup=0)
     assert bench.run_reference(args) is None
+
+
+def test_link_floor_takes_the_slowest_leg():
+    link = {"h2d_GBps": 200.0, "d2h_GBps": 100.0, "both_GBps": 250.0}
+    # 1 GB each way: the download leg binds (10 ms against 8 ms for both at once)
+    assert bench.link_floor_s(1e9, 1e9, link) == pytest.approx(1e9 / 100e9)
+    # download-light: the upload leg binds
+    assert bench.link_floor_s(4e9, 1e8, link) == pytest.approx(4e9 / 200e9)
+    # balanced and a slow two-way rate: the shared link binds
+    slow = dict(link, both_GBps=120.0)
+    assert bench.link_floor_s(1e9, 1e9, slow) == pytest.approx(2e9 / 120e9)
+
+
+def _cfg_row(config, us, us_clean, target):
+    return {"config": config, "target": target, "lone": {"us": us, "frac": 1.0 / us},
+            "lone_clean": {"us": us_clean, "frac": 1.0 / us_clean},
+            "target_met": {} if target is not None else None}
+
+
+def test_attach_floors_compares_with_the_same_config_floor():
+    rows = {
+        "C3_copy2d_ragged": _cfg_row("C3", 12.5, 8.2, 0.75),
+        "C4_rowsum": _cfg_row("C4", 17.06, 16.38, 0.85),
+        "C4_colsum_auto": _cfg_row("C4", 19.12, 18.43, 0.70),
+        "C5_rowmax_masked": _cfg_row("C5", 13.0, 12.3, None),
+        "C3_floor_memcpy": _cfg_row("C3", 16.03, 12.29, None),
+        "C4_floor_read": _cfg_row("C4", 17.06, 16.38, None),
+    }
+    bench.attach_floors(rows)
+    assert rows["C3_copy2d_ragged"]["floor"]["entry"] == "C3_floor_memcpy"
+    assert rows["C3_copy2d_ragged"]["floor"]["lone_vs_floor"] == round(12.5 / 16.03, 3)
+    assert rows["C3_copy2d_ragged"]["target_met"]["lone_within_5pct_of_floor"] is True
+    assert rows["C4_rowsum"]["floor"]["lone_vs_floor"] == 1.0
+    assert rows["C4_rowsum"]["target_met"]["lone_within_5pct_of_floor"] is True
+    assert rows["C4_colsum_auto"]["floor"]["lone_clean_vs_floor"] == round(18.43 / 16.38, 3)
+    assert rows["C4_colsum_auto"]["target_met"]["lone_within_5pct_of_floor"] is False
+    # untargeted rows and the floors themselves get no comparison
+    for k in ("C5_rowmax_masked", "C3_floor_memcpy", "C4_floor_read"):
+        assert "floor" not in rows[k]
+
+
+def test_every_floor_names_a_config_entry():
+    keys = {e[0]: e[1] for e in bench.CONFIG_ENTRIES}
+    for cfg, fk in bench.FLOOR_OF.items():
+        assert keys.get(fk) == cfg
