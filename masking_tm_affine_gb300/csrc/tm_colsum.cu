@@ -338,12 +338,42 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_regdirect(const ColArgs a)
     pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
+// The end of both one-pass forms, after the cluster barrier that follows the
+// partials: rank r adds up the strip's columns [r*TN/CS, (r+1)*TN/CS), the
+// CS partials of each in rank order from 0 (the order one thread adding all
+// of them would take), and writes them to c.  Thread (q, k) fetches rank q's
+// partial of the slice's column k over distributed shared memory, so every
+// fetch is in flight at once.  The caller's second cluster barrier keeps the
+// peers' partials alive until these fetches are done.
+template <int TN, int CS>
+__device__ __forceinline__ void cluster_add_partials(const float *part, float *c, int64_t N, int64_t strip)
+{
+    constexpr int SL = TN / CS;  // columns per rank
+    static_assert(SL >= 1 && SL * CS == TN, "the ranks split the strip evenly");
+    __shared__ float gath[CS][SL];
+    const uint32_t rank = cluster_rank();
+    if (threadIdx.x < TN) {
+        const int q = threadIdx.x / SL, k = threadIdx.x % SL;
+        gath[q][k] = ld_cluster_f32(cluster_addr(smem_u32(&part[rank * SL + k]), (uint32_t)q));
+    }
+    __syncthreads();
+    if (threadIdx.x < SL) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < CS; ++q) t += gath[q][threadIdx.x];
+        const int64_t col = strip * TN + (int64_t)rank * SL + threadIdx.x;
+        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
+        if (col < N) c[col] = t;
+    }
+}
+
 // ------------------------------------------------------------------ CLUSTER (one pass)
 // The register-direct layout, with the partial sums reduced on chip: the CS
 // CTAs of a cluster split the rows of one TN-column strip, each adds its rows
 // into a TN-wide partial in its shared memory, and after one cluster barrier
-// rank 0 adds the CS partials over distributed shared memory, in rank order,
-// and writes c.  No workspace and no second pass.  IT is the type of element
+// each rank adds the CS partials of its slice of the columns over distributed
+// shared memory, in rank order, and writes them to c.  No workspace and no
+// second pass.  IT is the type of element
 // offsets: uint32_t when (M + 128) * ldx fits 32 bits (host-checked), which
 // saves registers.  Four CTAs per SM, each free to hold all UNR loads of a
 // batch in flight (at eight CTAs, capped at 32 registers, the compiler
@@ -428,16 +458,8 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_cluster(const ColArgs a, i
         }
     }
     cluster_sync();  // every CTA's partial of this strip is in its shared memory
-    if (cluster_rank() == 0 && threadIdx.x < TN) {
-        const uint32_t mine = smem_u32(&part[threadIdx.x]);
-        float t = 0.0f;
-#pragma unroll 4
-        for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
-        const int64_t col = (int64_t)(blockIdx.x / CS) * TN + threadIdx.x;
-        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
-        if (col < a.N) a.c[col] = t;
-    }
-    cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
+    cluster_add_partials<TN, CS>(part, a.c, a.N, (int64_t)(blockIdx.x / CS));
+    cluster_sync();  // the peers' shared memory stays valid until every rank has read it
     pdl_wait();      // threads that stored nothing: the grid completes only after the one before it
 }
 
@@ -556,16 +578,8 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
         }
     }
     cluster_sync();  // every CTA's partial of this strip is in its shared memory
-    if (cluster_rank() == 0 && tid < TN) {
-        const uint32_t mine = smem_u32(&part[tid]);
-        float t = 0.0f;
-#pragma unroll 4
-        for (int q = 0; q < CS; ++q) t += ld_cluster_f32(cluster_addr(mine, (uint32_t)q));
-        const int64_t col = strip * TN + tid;
-        pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
-        if (col < a.N) a.c[col] = t;
-    }
-    cluster_sync();  // the peers' shared memory stays valid until rank 0 has read it
+    cluster_add_partials<TN, CS>(part, a.c, a.N, strip);
+    cluster_sync();  // the peers' shared memory stays valid until every rank has read it
     pdl_wait();      // threads that stored nothing: the grid completes only after the one before it
 }
 
