@@ -975,6 +975,10 @@ CASES = {
     "colsum_8192sq": ("scale_8192", "colsum", ["auto", "staged", "regdirect", "cluster"]),
     "rowmax_8192sq": ("scale_8192", "rowmax_masked", ["neg_inf"]),
     "read_floor_8192sq": ("scale_8192", "read_probe", ["u4", "u8"]),
+    # the same reads with every block's share fixed at launch (512 / 608 blocks):
+    # the floor of a one-pass walk that cannot rebalance, like the column sums'
+    "read_fixed_4096": ("coalesce_4096", "read_probe_fixed", ["b512", "b608"]),
+    "read_fixed_8192sq": ("scale_8192", "read_probe_fixed", ["b512", "b608"]),
     # the tensor-core gemm (3xTF32 by default; tf32 = one pass)
     "gemm_4100": ("gemm_4100", "gemm", ["3xtf32", "tf32"]),
     "gemm_8192": ("gemm_8192", "gemm", ["3xtf32", "tf32"]),
@@ -1111,7 +1115,7 @@ def time_oracle_case(kern, w, x, budget_s: float = 1.5) -> dict:
         if kern == "rowsum":
             oracle.rowsum(xs, cols, R, cols)
             return 4 * R * cols + 4 * R
-        if kern == "read_probe":  # a plain read of the same bytes: the oracle's row sums of them
+        if kern in ("read_probe", "read_probe_fixed"):  # a plain read of the same bytes: the oracle's row sums
             oracle.rowsum(xs, cols, R, cols)
             return 4 * R * cols
         if kern == "colsum":
@@ -1213,6 +1217,10 @@ def run_cases(args):
                 O = torch.empty(max(tm.tm_read_probe_blocks(Mw * Nw, 1), 1), dtype=torch.float32, device=dev)
                 nbytes = 4 * Mw * Nw
                 mk = lambda v: (lambda: tm.tm_read_probe(X, Mw * Nw, O, U[v], s))
+            elif kern == "read_probe_fixed":
+                O = torch.empty(65535, dtype=torch.float32, device=dev)
+                nbytes = 4 * Mw * Nw
+                mk = lambda v: (lambda: tm.tm_read_probe_fixed(X, Mw * Nw, O, int(v[1:]), s))
             elif kern == "pad2d":
                 Mp_, Np_ = tm.tm_padded_extent(Mw, [w["TM"]]), tm.tm_padded_extent(Nw, [w["TN"]])
                 ldp = tm.tm_row_stride(Np_, 16)

@@ -455,6 +455,22 @@ int64_t tm_read_probe_blocks(int64_t n, int32_t per_thread);
 tm_status tm_read_probe(const float *x, int64_t n, float *out, int32_t per_thread, tm_stream_t stream);
 
 /*
+ * tm_read_probe_fixed -- the same plain read with every block's share fixed
+ * before it starts: the floor of a one-pass walk that cannot hand work from a
+ * slow block to a fast one (the column sums' one-pass forms give each CTA a
+ * fixed part of a strip; "Memory Coalescing and Tensor Layout", "Seeing it in
+ * a real kernel").  Exactly `blocks` blocks (1 .. 65535) of 256 threads; with
+ * share = tm_read_probe_fixed_share(n, blocks) floats (a multiple of 8192:
+ * each step of a block is 256 threads x 8 16-byte loads), block b sums floats
+ * [b*share, min((b+1)*share, n)) of x into out[b] in a fixed order (0 for a
+ * block wholly past n).  n % 4 == 0, x 16-byte aligned, out holds `blocks`
+ * floats and must not overlap x.  tm_read_probe_fixed_share returns -1 for a
+ * bad n or blocks.  Errors: INVALID_ARG, MISALIGNED, CUDA.
+ */
+int64_t tm_read_probe_fixed_share(int64_t n, int32_t blocks);
+tm_status tm_read_probe_fixed(const float *x, int64_t n, float *out, int32_t blocks, tm_stream_t stream);
+
+/*
  * tm_scale2d_unchecked -- tm_scale2d on its TM_ALIGNED path without the host
  * promise check, so the kernel's own entry check is what stands between a
  * broken promise and the tensor's end.  With a broken promise no element is

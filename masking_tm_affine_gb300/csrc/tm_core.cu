@@ -94,6 +94,41 @@ __global__ void __launch_bounds__(kThreads) read_probe_kernel(const float *__res
     }
 }
 
+// The same read with each block's share fixed at launch: block b walks its
+// own contiguous range [b0, b1) of 16-byte vectors, 256 threads x 8 loads per
+// step, and writes one sum.  No block can take over another's work, as in
+// the column sums' one-pass forms, whose CTAs each own a fixed part of a
+// strip.
+__global__ void __launch_bounds__(kThreads) read_probe_fixed_kernel(const float *__restrict__ x, int64_t n4,
+                                                                    int64_t share4, float *__restrict__ out)
+{
+    constexpr int U = 8;
+    __shared__ float wsum[kThreads / 32];
+    const int64_t b0 = (int64_t)blockIdx.x * share4;
+    const int64_t b1 = b0 + share4 < n4 ? b0 + share4 : n4;
+    float s = 0.0f;
+    for (int64_t c = b0; c < b1; c += (int64_t)kThreads * U) {
+        u32x4 v[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int64_t i = c + threadIdx.x + (int64_t)q * kThreads;
+            v[q] = i < b1 ? ld_nc_v4(x + 4 * i) : u32x4{{0u, 0u, 0u, 0u}};
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q) s += (as_f(v[q].v[0]) + as_f(v[q].v[1])) + (as_f(v[q].v[2]) + as_f(v[q].v[3]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = wsum[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) t += wsum[w];
+        out[blockIdx.x] = t;
+    }
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -175,6 +210,31 @@ extern "C" int64_t tm_read_probe_blocks(int64_t n, int32_t per_thread)
         return -1;
     const int64_t per_block = (int64_t)kThreads * per_thread * 4;
     return (n + per_block - 1) / per_block;
+}
+
+extern "C" int64_t tm_read_probe_fixed_share(int64_t n, int32_t blocks)
+{
+    if (n < 0 || n % 4 != 0 || blocks < 1 || blocks > 65535) return -1;
+    const int64_t step = (int64_t)kThreads * 8 * 4;  // floats per block step
+    const int64_t steps = (n + step * blocks - 1) / (step * blocks);
+    return steps * step;
+}
+
+extern "C" tm_status tm_read_probe_fixed(const float *x, int64_t n, float *out, int32_t blocks, tm_stream_t stream)
+{
+    const int64_t share = tm_read_probe_fixed_share(n, blocks);
+    if (share < 0) return TM_ERR_INVALID_ARG;
+    if (n == 0) return TM_OK;
+    if (x == nullptr || out == nullptr) return TM_ERR_INVALID_ARG;
+    if (!aligned_to(x, 16) || !aligned_to(out, 4)) return TM_ERR_MISALIGNED;
+    const uintptr_t xlo = reinterpret_cast<uintptr_t>(x), xhi = xlo + (uintptr_t)n * 4;
+    const uintptr_t olo = reinterpret_cast<uintptr_t>(out), ohi = olo + (uintptr_t)blocks * 4;
+    if (!(xhi <= olo || ohi <= xlo)) return TM_ERR_INVALID_ARG;
+    const DevInfo *dev;
+    tm_status st = device_info(&dev);
+    if (st != TM_OK) return st;
+    read_probe_fixed_kernel<<<(unsigned)blocks, kThreads, 0, as_stream(stream)>>>(x, n / 4, share / 4, out);
+    return launch_status();
 }
 
 extern "C" tm_status tm_read_probe(const float *x, int64_t n, float *out, int32_t per_thread, tm_stream_t stream)

@@ -78,6 +78,8 @@ SIGNATURES = {
     "tm_wait_timeout_probe": (_st, [_vp]),
     "tm_read_probe_blocks": (_i64, [_i64, _i32]),
     "tm_read_probe": (_st, [_vp, _i64, _vp, _i32, _vp]),
+    "tm_read_probe_fixed_share": (_i64, [_i64, _i32]),
+    "tm_read_probe_fixed": (_st, [_vp, _i64, _vp, _i32, _vp]),
 }
 
 _lib = None
@@ -247,6 +249,15 @@ def tm_read_probe_blocks(n: int, per_thread: int = 4) -> int:
 def tm_read_probe(x, n: int, out, per_thread: int = 4, stream=None) -> None:
     """The plain streaming read of n floats (one fp32 sum per 1024*per_thread elements)."""
     _ok(load().tm_read_probe(_ptr(x), n, _ptr(out), per_thread, _stream(stream)), "tm_read_probe")
+
+
+def tm_read_probe_fixed_share(n: int, blocks: int) -> int:
+    return int(load().tm_read_probe_fixed_share(n, blocks))
+
+
+def tm_read_probe_fixed(x, n: int, out, blocks: int, stream=None) -> None:
+    """The same read with exactly `blocks` blocks, each summing its own fixed contiguous share."""
+    _ok(load().tm_read_probe_fixed(_ptr(x), n, _ptr(out), blocks, _stream(stream)), "tm_read_probe_fixed")
 
 
 def tm_wait_timeout_probe(stream=None) -> None:

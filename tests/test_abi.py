@@ -123,6 +123,18 @@ def test_reduction_host_validation(lib):
     assert st("tm_read_probe", P0 + 4, 8, P1, 4, None) == tm.TM_ERR_MISALIGNED
     assert st("tm_read_probe", P0, 1 << 20, P0 + 64, 4, None) == tm.TM_ERR_INVALID_ARG  # out inside x
     assert st("tm_read_probe", P0, 0, None, 4, None) == tm.TM_OK                      # nothing to read
+    # the fixed-share read: whole 8192-float steps per block, blocks in 1 .. 65535
+    assert tm.tm_read_probe_fixed_share(1 << 26, 512) == (1 << 26) // 512
+    assert tm.tm_read_probe_fixed_share(1 << 26, 608) == 8192 * -(-(1 << 26) // (8192 * 608))
+    assert tm.tm_read_probe_fixed_share(4, 1) == 8192 and tm.tm_read_probe_fixed_share(0, 7) == 0
+    assert tm.tm_read_probe_fixed_share(6, 4) == -1 and tm.tm_read_probe_fixed_share(8, 0) == -1
+    assert tm.tm_read_probe_fixed_share(8, 65536) == -1
+    assert st("tm_read_probe_fixed", P0, 6, P1, 4, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_read_probe_fixed", P0, 8, P1, 0, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_read_probe_fixed", P0, 8, None, 4, None) == tm.TM_ERR_INVALID_ARG
+    assert st("tm_read_probe_fixed", P0 + 4, 8, P1, 4, None) == tm.TM_ERR_MISALIGNED
+    assert st("tm_read_probe_fixed", P0, 1 << 20, P0 + 64, 4, None) == tm.TM_ERR_INVALID_ARG  # out inside x
+    assert st("tm_read_probe_fixed", P0, 0, None, 4, None) == tm.TM_OK
 
 
 def test_overlap_flag_host_validation(lib):

@@ -72,3 +72,21 @@ def test_read_probe_block_sums(cuda, oracle, per_thread, n):
     tm.tm_check()
     assert out.guards_intact()
     assert np.all(np.abs(out.payload_f32() - want) <= 1e-5 * want)
+
+
+@pytest.mark.parametrize("n,blocks", [(1 << 24, 512), (1 << 24, 608), (4_100_000, 300), (8192, 5), (4, 1)])
+def test_read_probe_fixed_block_sums(cuda, oracle, n, blocks):
+    # block b sums elements [b*share, min((b+1)*share, n)); blocks past n write 0
+    x = synth.uniform((n,), 0.0, 1.0, 41)
+    share = tm.tm_read_probe_fixed_share(n, blocks)
+    assert share % 8192 == 0 and share * blocks >= n and share * (blocks - 1) < n + 8192 * blocks
+    padded = np.zeros(blocks * share, np.float32)
+    padded[:n] = x
+    want = oracle.rowsum(padded, share, blocks, share)
+    out = DevBuf.empty(blocks)
+    tm.tm_read_probe_fixed(DevBuf(x).ptr, n, out.ptr, blocks)
+    tm.tm_check()
+    assert out.guards_intact()
+    got = out.payload_f32()
+    assert np.all(np.abs(got - want) <= 1e-5 * want)
+    assert np.all(got[want == 0] == 0)
