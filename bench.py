@@ -491,6 +491,7 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
         t = e0.elapsed_time(e1) * 1e-3
     else:
         link = measure_link(hx, bufs["X"], bufs["A1"], dev)
+        link.update(measure_step_copies(hx, bufs, outs, dev))
         sets = [bufs, make_buffers(tm, x, dev)[0]]
         steps_of = [step, make_step(tm, sets[1], ws_bytes, stream, first_overlap=False)]
         hosts = [{k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs} for _ in range(2)]
@@ -540,14 +541,51 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
     if mode != "serial":
         floor = link_floor_s(h2d, d2h, link)
         out["link"] = {**link, "floor_ms_per_step": round(floor * 1e3, 3),
-                       "frac_of_floor": round(floor / (t / steps), 4)}
+                       "frac_of_floor": round(floor / (t / steps), 4),
+                       "frac_of_copies_alone": round(link["copies_alone_ms_per_step"] * 1e-3 / (t / steps), 4)}
     return out
+
+
+def measure_step_copies(hx, bufs, outs, dev, reps=5):
+    """One step's own copies and nothing else: X in on one stream while every
+    output goes out on another (median of `reps`, after one untimed).  The
+    pipelined e2e step cannot beat this: its kernels run beside the copies."""
+    import torch
+    host = {k: torch.empty(bufs[k].numel(), dtype=torch.float32).pin_memory() for k in outs}
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def once():
+        ev = torch.cuda.Event()
+        ev.record(s1)
+        s2.wait_event(ev)
+        with torch.cuda.stream(s1):
+            bufs["X"].copy_(hx, non_blocking=True)
+        with torch.cuda.stream(s2):
+            for k in outs:
+                host[k].copy_(bufs[k], non_blocking=True)
+        s1.wait_stream(s2)
+
+    once()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s1)
+        once()
+        e1.record(s1)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    del host
+    return {"copies_alone_ms_per_step": round(statistics.median(ts) * 1e3, 3),
+            "copies_alone_how": "X in and every output out, concurrently on two streams, no kernels"}
 
 
 def link_floor_s(h2d_bytes, d2h_bytes, link):
     """Seconds a step needs at least to move its bytes over the host link: each
     direction at its own measured rate, and both together at the two-way
-    rate (GB/s figures of `measure_link`)."""
+    rate (GB/s figures of `measure_link`).  A lower bound: the link may not
+    reach it for an uneven mix (the step's own copies, timed alone, say what
+    it does reach)."""
     return max(h2d_bytes / link["h2d_GBps"], d2h_bytes / link["d2h_GBps"],
                (h2d_bytes + d2h_bytes) / link["both_GBps"]) / 1e9
 
