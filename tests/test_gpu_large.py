@@ -127,3 +127,36 @@ def test_gemm_past_2_31_elements(cuda, oracle):
     want = oracle.gemm_rows(a, K, b, N, None, 0, np.arange(len(rows)), N, K, 1.0, 0.0)
     assert np.array_equal(C[rows].cpu().numpy(), want)
     del A, B, C, raw
+
+
+def test_one_pass_colsums_with_64_bit_offsets(cuda):
+    # (M + 128) * ld > 2^32: the one-pass forms take 64-bit element offsets
+    # (and STAGED's tensor map row coordinates pass 2^17); 18.4 GB on the device
+    M, N = 140001, 32768
+    assert (M + 128) * N > (1 << 32)
+    X = torch.empty((M, N), device="cuda")
+    for r0 in range(0, M, 8192):  # the pattern in row chunks: bounded temporaries
+        r1 = min(M, r0 + 8192)
+        i = torch.arange(r0, r1, device="cuda", dtype=torch.int64)[:, None]
+        j = torch.arange(N, device="cuda", dtype=torch.int64)[None, :]
+        X[r0:r1] = (((i * 1000003 + j * 7919 + 5 * 104729) % 2039) - 1019).to(torch.float32) / 64.0
+        del i, j
+    got = {}
+    for var in (tm.TM_VAR_CLUSTER, tm.TM_VAR_STAGED, tm.TM_VAR_REGDIRECT):
+        ws = tm.tm_colsum_workspace_bytes(M, N, 32, 128, var)
+        W = torch.empty(max(ws // 4, 4), device="cuda")
+        c = torch.full((N,), float("nan"), device="cuda")
+        tm.tm_colsum(X, N, M, N, c, W, ws, 32, 128, var)
+        tm.tm_check()
+        got[var] = c.cpu().numpy()
+        del W
+    # the two one-pass forms add the same rows in the same order
+    assert np.array_equal(got[tm.TM_VAR_CLUSTER].view(np.uint32), got[tm.TM_VAR_STAGED].view(np.uint32))
+    cols = np.array([0, 1, 127, 128, N // 2 + 3, N - 1])
+    i = np.arange(M, dtype=np.int64)[:, None]
+    h = (i * 1000003 + cols[None, :] * 7919 + 5 * 104729) % 2039 - 1019
+    exact = h.sum(axis=0) / 64.0
+    tol = 1e-5 * (np.abs(h).sum(axis=0) / 64.0)
+    for var, c in got.items():
+        assert np.all(np.abs(c[cols].astype(np.float64) - exact) <= tol), var
+    del X
