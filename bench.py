@@ -660,13 +660,14 @@ CONFIG_ENTRIES = [
     ("C4_colsum_auto", "C4", "coalesce_4096", "colsum", "auto", 0.70),
     ("C4_colsum_staged", "C4", "coalesce_4096", "colsum", "staged", 0.70),
     ("C5_rowmax_masked", "C5", "rowmax_8192", "rowmax_masked", "neg_inf", None),
-    # the floors C3 and C4 are read against, timed the same way in the same
-    # run: a device-to-device cudaMemcpyAsync of the ragged tensor's bytes,
-    # and the plain streaming read of the 64 MiB the sums read
+    # the floors C3, C4 and C5 are read against, timed the same way in the
+    # same run: a device-to-device cudaMemcpyAsync of the ragged tensor's
+    # bytes, and the plain streaming read of what the reductions read
     ("C3_floor_memcpy", "C3", "ragged_4100", "memcpy", "d2d", None),
     ("C4_floor_read", "C4", "coalesce_4096", "read_probe", "u4", None),
+    ("C5_floor_read", "C5", "rowmax_8192", "read_probe", "u4", None),
 ]
-FLOOR_OF = {"C3": "C3_floor_memcpy", "C4": "C4_floor_read"}
+FLOOR_OF = {"C3": "C3_floor_memcpy", "C4": "C4_floor_read", "C5": "C5_floor_read"}
 AMORTIZED_BYTES = 512 << 20  # rotating copies of the inputs and outputs: 4x the L2
 
 
@@ -725,11 +726,11 @@ def config_kernel(tm, kern, path, w, x, dev):
         n = M * N
         U = int(path[1:])
         blocks = tm.tm_read_probe_blocks(n, U)
-        if (1024 * U) % N or blocks * 1024 * U != n:
-            raise ValueError("read probe blocks must be whole rows of the workload")
-        per = 1024 * U // N  # rows per block
-        xb = x.reshape(blocks, per * N)
-        want = oracle.rowsum(xb, per * N, blocks, per * N)
+        span = 1024 * U  # block b sums elements [b*span, (b+1)*span) of the flat tensor
+        xb = np.zeros(blocks * span, np.float32)
+        xb[:n] = x.reshape(-1)
+        xb = xb.reshape(blocks, span)
+        want = oracle.rowsum(xb, span, blocks, span)
         tol = 1e-5 * np.abs(xb.astype(np.float64)).sum(axis=1)
         return ("tm_read_probe, %d floats, %d 16-byte loads per thread (no TM_PDL: plain launches)" % (n, U), blocks,
                 lambda X, O, W, s, pdl: tm.tm_read_probe(X, n, O, U, s), 4 * n + 4 * blocks, 0,
@@ -846,12 +847,13 @@ def run_configs(tm, dev, peak, reps=20, verify=True, x_step=None):
 
 
 def attach_floors(rows):
-    """Each targeted row of the configs block against its config's floor row
+    """Each row of the configs block against its config's floor row
     (FLOOR_OF), timed the same way in the same run: its lone times over the
-    floor's, and whether the dirty-flush lone time is within 5 % of it."""
+    floor's, and for a targeted row whether the dirty-flush lone time is
+    within 5 % of it."""
     for key, row in rows.items():
         fk = FLOOR_OF.get(row["config"])
-        if row["target"] is None or fk not in rows:
+        if fk not in rows or key == fk:
             continue
         f = rows[fk]
         row["floor"] = {"entry": fk,
@@ -860,7 +862,8 @@ def attach_floors(rows):
                         "lone_clean_vs_floor": round(row["lone_clean"]["us"] / f["lone_clean"]["us"], 3),
                         "how": "this row's lone time over the floor's (1.0 = as fast as the floor; "
                                "both move the same input bytes)"}
-        row["target_met"]["lone_within_5pct_of_floor"] = row["lone"]["us"] <= 1.05 * f["lone"]["us"]
+        if row["target"] is not None:
+            row["target_met"]["lone_within_5pct_of_floor"] = row["lone"]["us"] <= 1.05 * f["lone"]["us"]
     return rows
 
 

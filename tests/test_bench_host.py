@@ -93,8 +93,12 @@ def test_attach_floors_compares_with_the_same_config_floor():
     assert rows["C4_rowsum"]["target_met"]["lone_within_5pct_of_floor"] is True
     assert rows["C4_colsum_auto"]["floor"]["lone_clean_vs_floor"] == round(18.43 / 16.38, 3)
     assert rows["C4_colsum_auto"]["target_met"]["lone_within_5pct_of_floor"] is False
-    # untargeted rows and the floors themselves get no comparison
-    for k in ("C5_rowmax_masked", "C3_floor_memcpy", "C4_floor_read"):
+    # an untargeted row gets the comparison but no verdict; the floors none
+    rows["C5_floor_read"] = _cfg_row("C5", 12.0, 11.0, None)
+    bench.attach_floors(rows)
+    assert rows["C5_rowmax_masked"]["floor"]["lone_vs_floor"] == round(13.0 / 12.0, 3)
+    assert rows["C5_rowmax_masked"]["target_met"] is None
+    for k in ("C3_floor_memcpy", "C4_floor_read", "C5_floor_read"):
         assert "floor" not in rows[k]
 
 
