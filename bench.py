@@ -660,14 +660,15 @@ CONFIG_ENTRIES = [
     ("C4_colsum_auto", "C4", "coalesce_4096", "colsum", "auto", 0.70),
     ("C4_colsum_staged", "C4", "coalesce_4096", "colsum", "staged", 0.70),
     ("C5_rowmax_masked", "C5", "rowmax_8192", "rowmax_masked", "neg_inf", None),
-    # the floors C3, C4 and C5 are read against, timed the same way in the
-    # same run: a device-to-device cudaMemcpyAsync of the ragged tensor's
-    # bytes, and the plain streaming read of what the reductions read
+    # the floors C1, C3, C4 and C5 are read against, timed the same way in
+    # the same run: a device-to-device cudaMemcpyAsync of the maps' bytes,
+    # and the plain streaming read of what the reductions read
+    ("C1_floor_memcpy", "C1", "affine_1m", "memcpy", "d2d", None),
     ("C3_floor_memcpy", "C3", "ragged_4100", "memcpy", "d2d", None),
     ("C4_floor_read", "C4", "coalesce_4096", "read_probe", "u4", None),
     ("C5_floor_read", "C5", "rowmax_8192", "read_probe", "u4", None),
 ]
-FLOOR_OF = {"C3": "C3_floor_memcpy", "C4": "C4_floor_read", "C5": "C5_floor_read"}
+FLOOR_OF = {"C1": "C1_floor_memcpy", "C3": "C3_floor_memcpy", "C4": "C4_floor_read", "C5": "C5_floor_read"}
 AMORTIZED_BYTES = 512 << 20  # rotating copies of the inputs and outputs: 4x the L2
 
 
@@ -683,6 +684,14 @@ def config_kernel(tm, kern, path, w, x, dev):
         return ("tm_affine %s, n=%d" % (path.upper(), n), n,
                 lambda X, O, W, s, pdl: tm.tm_affine(X, O, n, var | (tm.TM_PDL if pdl else 0), s),
                 8 * n, 0, lambda o: np.array_equal(o.view(np.uint32), want))
+    if kern == "memcpy":
+        n = x.size
+        want = x.reshape(-1).view(np.uint32)
+
+        def copy(X, O, W, s, pdl):
+            O.copy_(X, non_blocking=True)  # on torch's current stream: the timed stream, or the capture stream
+        return ("cudaMemcpyAsync device to device, %d bytes (torch copy_)" % (4 * n), n, copy, 8 * n, 0,
+                lambda o: bool(np.array_equal(o.view(np.uint32), want)))
     M, N = x.shape
     if kern in ("scale2d", "copy2d"):
         TM_, TN_ = w["TM"], w["TN"]
@@ -714,14 +723,6 @@ def config_kernel(tm, kern, path, w, x, dev):
         return ("tm_colsum %s [%d,%d] 32x128 (workspace %d B)" % (path.upper(), M, N, ws), N,
                 lambda X, O, W, s, pdl: tm.tm_colsum(X, N, M, N, O, W, ws, 32, 128, var, tm.TM_PDL if pdl else 0, s),
                 4 * M * N + 4 * N, max(ws // 4, 4), lambda o: bool(np.all(np.abs(o - want) <= tol)))
-    if kern == "memcpy":
-        n = M * N
-        want = x.reshape(-1).view(np.uint32)
-
-        def copy(X, O, W, s, pdl):
-            O.copy_(X, non_blocking=True)  # on torch's current stream: the timed stream, or the capture stream
-        return ("cudaMemcpyAsync device to device, %d bytes (torch copy_)" % (4 * n), n, copy, 8 * n, 0,
-                lambda o: bool(np.array_equal(o.view(np.uint32), want)))
     if kern == "read_probe":
         n = M * N
         U = int(path[1:])
