@@ -667,7 +667,11 @@ CONFIG_ENTRIES = [
     ("C3_floor_memcpy", "C3", "ragged_4100", "memcpy", "d2d", None),
     ("C4_floor_read", "C4", "coalesce_4096", "read_probe", "u4", None),
     ("C5_floor_read", "C5", "rowmax_8192", "read_probe", "u4", None),
+    # the same read with every block's share fixed at launch: the floor of the
+    # column sum's one-pass forms, which give each CTA a fixed band of rows
+    ("C4_floor_fixed_share", "C4", "coalesce_4096", "read_probe_fixed", "b512", None),
 ]
+FIXED_SHARE_FLOOR_OF = {"C4_colsum_auto": "C4_floor_fixed_share", "C4_colsum_staged": "C4_floor_fixed_share"}
 FLOOR_OF = {"C1": "C1_floor_memcpy", "C3": "C3_floor_memcpy", "C4": "C4_floor_read", "C5": "C5_floor_read"}
 AMORTIZED_BYTES = 512 << 20  # rotating copies of the inputs and outputs: 4x the L2
 
@@ -735,6 +739,19 @@ def config_kernel(tm, kern, path, w, x, dev):
         tol = 1e-5 * np.abs(xb.astype(np.float64)).sum(axis=1)
         return ("tm_read_probe, %d floats, %d 16-byte loads per thread (no TM_PDL: plain launches)" % (n, U), blocks,
                 lambda X, O, W, s, pdl: tm.tm_read_probe(X, n, O, U, s), 4 * n + 4 * blocks, 0,
+                lambda o: bool(np.all(np.abs(o - want) <= tol)))
+    if kern == "read_probe_fixed":
+        n = M * N
+        blocks = int(path[1:])
+        share = tm.tm_read_probe_fixed_share(n, blocks)
+        xb = np.zeros(blocks * share, np.float32)
+        xb[:n] = x.reshape(-1)
+        xb = xb.reshape(blocks, share)
+        want = oracle.rowsum(xb, share, blocks, share)
+        tol = 1e-5 * np.abs(xb.astype(np.float64)).sum(axis=1)
+        return ("tm_read_probe_fixed, %d floats, %d blocks of fixed %d-float shares (plain launches)"
+                % (n, blocks, share), blocks,
+                lambda X, O, W, s, pdl: tm.tm_read_probe_fixed(X, n, O, blocks, s), 4 * n + 4 * blocks, 0,
                 lambda o: bool(np.all(np.abs(o - want) <= tol)))
     if kern == "rowmax_masked":
         BC = w["BC"]
@@ -852,9 +869,15 @@ def attach_floors(rows):
     (FLOOR_OF), timed the same way in the same run: its lone times over the
     floor's, and for a targeted row whether the dirty-flush lone time is
     within 5 % of it."""
+    floors = set(FLOOR_OF.values()) | set(FIXED_SHARE_FLOOR_OF.values())
     for key, row in rows.items():
+        ff = FIXED_SHARE_FLOOR_OF.get(key)
+        if ff in rows:
+            f = rows[ff]
+            row["floor_fixed_share"] = {"entry": ff, "lone_vs_floor": round(row["lone"]["us"] / f["lone"]["us"], 3),
+                                        "lone_clean_vs_floor": round(row["lone_clean"]["us"] / f["lone_clean"]["us"], 3)}
         fk = FLOOR_OF.get(row["config"])
-        if fk not in rows or key == fk:
+        if fk not in rows or key in floors:
             continue
         f = rows[fk]
         row["floor"] = {"entry": fk,

@@ -100,9 +100,17 @@ def test_attach_floors_compares_with_the_same_config_floor():
     assert rows["C5_rowmax_masked"]["target_met"] is None
     for k in ("C3_floor_memcpy", "C4_floor_read", "C5_floor_read"):
         assert "floor" not in rows[k]
+    # the column sums also meet the fixed-share read; no other row does
+    rows["C4_floor_fixed_share"] = _cfg_row("C4", 18.0, 17.0, None)
+    bench.attach_floors(rows)
+    assert rows["C4_colsum_auto"]["floor_fixed_share"]["lone_vs_floor"] == round(19.12 / 18.0, 3)
+    assert "floor_fixed_share" not in rows["C4_rowsum"]
+    assert "floor" not in rows["C4_floor_fixed_share"]
 
 
 def test_every_floor_names_a_config_entry():
     keys = {e[0]: e[1] for e in bench.CONFIG_ENTRIES}
     for cfg, fk in bench.FLOOR_OF.items():
         assert keys.get(fk) == cfg
+    for row, fk in bench.FIXED_SHARE_FLOOR_OF.items():
+        assert keys.get(row) == keys.get(fk) and keys.get(fk) is not None
