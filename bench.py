@@ -526,9 +526,10 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
             one(k)
         torch.cuda.synchronize(dev)
         # the host side of the link may be shared with other work on the
-        # machine: three regions of `steps` steps, the median one reported
+        # machine (one region in three has measured ~60 % slower): five
+        # regions of `steps` steps, the median one reported
         regions = []
-        for _ in range(3):
+        for _ in range(5):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(s_in)
             for k in range(steps):
