@@ -338,42 +338,82 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_regdirect(const ColArgs a)
     pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
-// The end of both one-pass forms, after the cluster barrier that follows the
-// partials: rank r adds up the strip's columns [r*TN/CS, (r+1)*TN/CS), the
+// The end of both one-pass forms.  Every CTA holds the TN partial sums of its
+// rows of the strip; rank r owns columns [r*TN/CS, (r+1)*TN/CS) and adds the
 // CS partials of each in rank order from 0 (the order one thread adding all
-// of them would take), and writes them to c.  Thread (q, k) fetches rank q's
-// partial of the slice's column k over distributed shared memory, so every
-// fetch is in flight at once.  The caller's second cluster barrier keeps the
-// peers' partials alive until these fetches are done.
+// of them would take).  The partials travel by push: thread (q, k) of each
+// CTA stores its partial of rank q's column k straight into rank q's inbox
+// with st.async, and every such store counts its 4 bytes on that inbox's
+// mbarrier, so an owner starts adding as soon as its TN floats have landed,
+// with no cluster barrier and no round trip of remote reads before it.
 template <int TN, int CS>
-__device__ __forceinline__ void cluster_add_partials(const float *part, float *c, int64_t N, int64_t strip)
+struct Inbox {
+    uint64_t bar;          // counts TN * 4 bytes in, once per launch
+    float v[CS][TN / CS];  // v[q][k]: rank q's partial of this rank's column k
+};
+
+// At kernel start, in every thread (after any early return, which all CTAs
+// take together): thread 0 sets the inbox up, then every thread arrives at
+// the cluster barrier that cluster_push_partials waits on before its first
+// remote store, so no store can reach an inbox not yet set up.
+template <int TN, int CS>
+__device__ __forceinline__ void inbox_open(Inbox<TN, CS> &in)
+{
+    if (threadIdx.x == 0) {
+        const uint32_t bar = smem_u32(&in.bar);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(TN * sizeof(float)))
+                     : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// part[0 .. TN) holds this CTA's partials (written before the call by some
+// threads; every thread calls).  Pushes them, waits (bounded) for its own
+// inbox, adds and writes its columns of c.  The closing cluster barrier is
+// passed only once every CTA's inbox is full, so no store is still in flight
+// to a CTA that leaves.  A wait that gives up records kStatusTimeout and
+// writes nothing.
+template <int TN, int CS>
+__device__ __forceinline__ void cluster_push_partials(const float *part, Inbox<TN, CS> &in, float *c, int64_t N,
+                                                      int64_t strip, unsigned *status)
 {
     constexpr int SL = TN / CS;  // columns per rank
     static_assert(SL >= 1 && SL * CS == TN, "the ranks split the strip evenly");
-    __shared__ float gath[CS][SL];
-    const uint32_t rank = cluster_rank();
+    __syncthreads();                                                       // part[] complete
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every peer's inbox is set up
+    const uint32_t me = cluster_rank();
     if (threadIdx.x < TN) {
-        const int q = threadIdx.x / SL, k = threadIdx.x % SL;
-        gath[q][k] = ld_cluster_f32(cluster_addr(smem_u32(&part[rank * SL + k]), (uint32_t)q));
+        const uint32_t q = threadIdx.x / SL, k = threadIdx.x % SL;
+        const uint32_t dst = cluster_addr(smem_u32(&in.v[me][k]), q);
+        const uint32_t bar = cluster_addr(smem_u32(&in.bar), q);
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+                     "r"(as_u(part[q * SL + k])), "r"(bar)
+                     : "memory");
     }
-    __syncthreads();
-    if (threadIdx.x < SL) {
+    const bool ok = mbar_wait_bounded(smem_u32(&in.bar), 0);
+    if (!ok && threadIdx.x == 0) report(status, kStatusTimeout);
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");  // this inbox is full
+    if (ok && threadIdx.x < SL) {
         float t = 0.0f;
 #pragma unroll
-        for (int q = 0; q < CS; ++q) t += gath[q][threadIdx.x];
-        const int64_t col = strip * TN + (int64_t)rank * SL + threadIdx.x;
+        for (int q = 0; q < CS; ++q) t += in.v[q][threadIdx.x];
+        const int64_t col = strip * TN + (int64_t)me * SL + threadIdx.x;
         pdl_wait();  // the loads may run ahead of the previous kernel, the stores may not
         if (col < N) c[col] = t;
     }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every inbox is full
 }
 
 // ------------------------------------------------------------------ CLUSTER (one pass)
 // The register-direct layout, with the partial sums reduced on chip: the CS
 // CTAs of a cluster split the rows of one TN-column strip, each adds its rows
-// into a TN-wide partial in its shared memory, and after one cluster barrier
-// each rank adds the CS partials of its slice of the columns over distributed
-// shared memory, in rank order, and writes them to c.  No workspace and no
-// second pass.  IT is the type of element
+// into a TN-wide partial in its shared memory, and the CTAs then push each
+// rank its slice of the columns over distributed shared memory, where the
+// rank adds the CS partials in rank order and writes them to c (see
+// cluster_push_partials).  No workspace and no second pass.  IT is the type of element
 // offsets: uint32_t when (M + 128) * ldx fits 32 bits (host-checked), which
 // saves registers.  Four CTAs per SM, each free to hold all UNR loads of a
 // batch in flight (at eight CTAs, capped at 32 registers, the compiler
@@ -401,6 +441,8 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_cluster(const ColArgs a, i
             return;
         }
     }
+    __shared__ Inbox<TN, CS> inbox;
+    inbox_open(inbox);
     const int cl = threadIdx.x % CL, rl = threadIdx.x / CL;
     float acc[EW];
 #pragma unroll
@@ -457,10 +499,8 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_cluster(const ColArgs a, i
             part[cl * EW + e] = t;
         }
     }
-    cluster_sync();  // every CTA's partial of this strip is in its shared memory
-    cluster_add_partials<TN, CS>(part, a.c, a.N, (int64_t)(blockIdx.x / CS));
-    cluster_sync();  // the peers' shared memory stays valid until every rank has read it
-    pdl_wait();      // threads that stored nothing: the grid completes only after the one before it
+    cluster_push_partials(part, inbox, a.c, a.N, (int64_t)(blockIdx.x / CS), a.status);
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ STAGED (TMA)
@@ -473,11 +513,12 @@ __global__ void __launch_bounds__(kThreads, 4) colsum_cluster(const ColArgs a, i
 // (cl, rl) adds rows rl, rl + RL, ... of every tile, in order.  TMA fills rows
 // past M and columns past N with 0, the masked-load value of "Slicing, bounds
 // and masking" ("Masking").  The CTAs' partials then meet over distributed
-// shared memory as in the cluster form: one pass, no workspace.  With the
-// same tile-aligned row split, lanes and order as colsum_cluster's 16-byte
-// path, the two give the same bits.  Every wait is bounded; a CTA whose wait
-// gives up records TM_ERR_TIMEOUT, drains the copies it started (bounded) and
-// still meets its cluster at both barriers.
+// shared memory as in the cluster form (cluster_push_partials): one pass, no
+// workspace.  With the same tile-aligned row split, lanes and order as
+// colsum_cluster's 16-byte path, the two give the same bits.  Every wait is
+// bounded; a CTA whose wait gives up records TM_ERR_TIMEOUT, drains the
+// copies it started (bounded) and still takes its part in the cluster's end,
+// so its peers are not left waiting.
 template <int TN, int CS, bool ALIGNED>
 __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant__ CUtensorMap tmap, const ColArgs a,
                                                           int TM, int64_t tiles_per_cta, int stages)
@@ -510,12 +551,14 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
     const int64_t t1 = t0 + tiles_per_cta < a.RT ? t0 + tiles_per_cta : a.RT;
     const int n = t1 > t0 ? (int)(t1 - t0) : 0;
 
+    __shared__ Inbox<TN, CS> inbox;
     if (tid == 0) {
         abort_flag = 0;
         for (int st = 0; st < stages; ++st)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[st])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    inbox_open(inbox);
     __syncthreads();
     auto issue = [&](int k) {
         if (k >= n) return;
@@ -577,10 +620,8 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
             part[cl * 4 + e] = t;
         }
     }
-    cluster_sync();  // every CTA's partial of this strip is in its shared memory
-    cluster_add_partials<TN, CS>(part, a.c, a.N, strip);
-    cluster_sync();  // the peers' shared memory stays valid until every rank has read it
-    pdl_wait();      // threads that stored nothing: the grid completes only after the one before it
+    cluster_push_partials(part, inbox, a.c, a.N, strip, a.status);
+    pdl_wait();  // threads that stored nothing: the grid completes only after the one before it
 }
 
 // ------------------------------------------------------------------ host side

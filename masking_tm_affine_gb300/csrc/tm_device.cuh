@@ -166,13 +166,6 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t a)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
