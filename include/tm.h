@@ -275,8 +275,10 @@ size_t tm_colsum_workspace_bytes(int64_t M, int64_t N, int32_t TM, int32_t TN, t
  *               TM_PDL (the first pass overlaps the previous kernel; the
  *               finish pass of a two-pass variant always overlaps the first)
  * Errors: INVALID_ARG, UNSUPPORTED_TILE, MISALIGNED, BROKEN_PROMISE,
- *         WORKSPACE, CUDA; a stalled TMA pipeline is reported by tm_check as
- *         TM_ERR_TIMEOUT.
+ *         WORKSPACE, CUDA; a stalled TMA pipeline (STAGED) or partial sums
+ *         that never reach their cluster peer (CLUSTER, STAGED; each wait is
+ *         bounded) are reported by tm_check as TM_ERR_TIMEOUT, with the
+ *         affected columns of c left unwritten.
  */
 tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N, float *c, void *workspace,
                     size_t ws_bytes, int32_t TM, int32_t TN, tm_variant variant, uint32_t flags,
