@@ -14,27 +14,29 @@
 //                (two passes).
 //   REGDIRECT -- lanes over columns: a warp reads a contiguous row segment of a
 //                TN-column strip with 16-byte loads and walks down the rows,
-//                accumulating in registers.  No shared-memory staging needed;
-//                the fastest variant measured, so AUTO takes it.
+//                accumulating in registers, one block per (strip, row chunk);
+//                the units' partials go to the workspace, strip-major, and
+//                colsum_finish_strips adds each column's partials in ascending
+//                chunk order (a fixed order: the same bits run to run) and
+//                drops their lines from L2 without writing them back.  A strip
+//                of one chunk writes c itself, with no second pass.
+//   CLUSTER   -- REGDIRECT's layout in one pass: the CTAs of a thread-block
+//                cluster split a strip's row tiles, and their partials meet in
+//                distributed shared memory (cluster_push_partials); no
+//                workspace.
 //   STAGED    -- the page's fix on GB300 hardware: the TMA engine copies
 //                TM x TN tiles into a ring of shared-memory stages (mbarrier
 //                completion, bounded waits); threads read the columns back out
 //                of shared memory.  Ragged edges come free: TMA fills
 //                out-of-bounds elements with 0, the masked-load value of
-//                "Slicing, bounds and masking" ("Masking").
-//   CLUSTER   -- REGDIRECT's layout with a strip's row chunks spread over the
-//                CTAs of a thread-block cluster, whose partials meet in
-//                distributed shared memory: one pass, no workspace.
+//                "Slicing, bounds and masking" ("Masking").  The cluster
+//                form's grid and end: one pass, the same bits as CLUSTER.
+//   AUTO      -- CLUSTER when every cluster fits on the GPU at once, else
+//                REGDIRECT.
 //
-// REGDIRECT and STAGED cut the matrix into units of one TN-column strip by
-// one row chunk.  A unit's TN column sums go to the workspace as its partial,
-// strip-major (a strip's partials are contiguous); colsum_finish_strips then
-// adds each column's partials in ascending chunk order -- a fixed order, so
-// results are the same run to run -- and drops the partials' lines from L2
-// without writing them back.  When a strip is a single chunk its sums are c
-// itself and no second pass runs.  (A one-pass form, in which the block that
-// brought a strip's last partial added them all, measured slower: every block
-// then waited for a counter round trip before it could leave its SM.)
+// (A one-pass REGDIRECT, in which the block that brought a strip's last
+// partial added them all, measured slower: every block then waited for a
+// counter round trip before it could leave its SM.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -129,7 +131,7 @@ __device__ __forceinline__ void store_unit(const ColArgs &a, int64_t s, int64_t 
 }
 
 // ------------------------------------------------------------------ finish (strip-major partials)
-// c[j] = sum over chunks p (ascending) of the partials of REGDIRECT / STAGED.
+// c[j] = sum over chunks p (ascending) of REGDIRECT's partials.
 // A block takes 32 columns: 8 lanes of 4 columns by 32 row lanes; row lane r
 // adds chunks r, r + 32, r + 64, ..., issuing its loads together (one L2 round
 // trip for up to 128 chunks), then the 32 lane sums are added in order.  The
@@ -926,9 +928,11 @@ extern "C" tm_status tm_colsum(const float *X, int64_t ldx, int64_t M, int64_t N
     } else {
         // AUTO: the one-pass cluster form whenever all its clusters fit on the
         // GPU at once (one wave), else the register-direct pass and its finish.
-        // [8192, 8192] at 32 x 128: 64 strips of 8-CTA clusters, 148 resident:
-        // 46.2 us per call plain and 36.2 chained, against 45.8 and 37.5;
-        // [4096, 4096]: 32 strips of 16-CTA clusters.
+        // [8192, 8192] at 32 x 128: 64 strips of 8-CTA clusters, all resident
+        // at four CTAs per SM (one pass: 41.9 us by kernel time, against 41.1
+        // for the register-direct pass plus its second launch and the 4 MiB
+        // of partials it writes and reads back); [4096, 4096]: 32 strips of
+        // 16-CTA clusters.
         const int CS = cluster_ctas(pl.S, dev->sms);
         int max_active = -1;
         st = cluster_prepare(pick_cluster_kernel(TN, CS, vec, aligned, cluster_narrow(M, ldx)), CS, &max_active);
