@@ -525,27 +525,31 @@ def run_e2e(tm, bufs, x, step, stream, dev, steps, step_bytes, ws_bytes, mode="p
         for k in range(2):
             one(k)
         torch.cuda.synchronize(dev)
-        # the host side of the link may be shared with other work on the
-        # machine (one region in three has measured ~60 % slower): five
-        # regions of `steps` steps, the median one reported
-        regions = []
-        for _ in range(5):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(s_in)
-            for k in range(steps):
-                one(k)
-            s_in.wait_stream(s_out)
-            e1.record(s_in)
-            torch.cuda.synchronize(dev)
-            regions.append(e0.elapsed_time(e1) * 1e-3)
-        t = statistics.median(regions)
+        # One continuous pipeline of (1 + nseg) segments of `seg` steps, a
+        # timing event on the download stream each time a segment's last
+        # outputs have left the device.  The first segment fills the pipeline
+        # and is not counted; the step time is the median segment's (the host
+        # side of the link may be shared with other work on the machine: a
+        # stretch of ~0.1 - 0.3 s now and then runs ~60 % slower).
+        seg, nseg = max(1, steps // 3), 12
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
+        for k in range(seg * (nseg + 1)):
+            one(k)
+            if (k + 1) % seg == 0:
+                with torch.cuda.stream(s_out):
+                    marks[(k + 1) // seg - 1].record(s_out)
+        torch.cuda.synchronize(dev)
+        segments = [marks[i].elapsed_time(marks[i + 1]) * 1e-3 / seg for i in range(nseg)]
+        t = statistics.median(segments) * steps
     out = {"value": round(gbps(step_bytes * steps, t), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(t / steps * 1e3, 3), "mode": mode,
            "path": "pinned host X -> device, the six C-ABI calls, every output -> pinned host"
                    + (", one stream" if mode == "serial" else
                       "; copy-in, kernels and copy-out of consecutive steps overlap on three streams")}
     if mode != "serial":
-        out["regions_ms_per_step"] = [round(r / steps * 1e3, 3) for r in regions]
+        out["segments_ms_per_step"] = [round(r * 1e3, 3) for r in segments]
+        out["timing"] = ("one continuous pipeline: %d segments of %d steps after one that fills it; the median "
+                         "segment's time per step" % (nseg, seg))
         floor = link_floor_s(h2d, d2h, link)
         out["link"] = {**link, "floor_ms_per_step": round(floor * 1e3, 3),
                        "frac_of_floor": round(floor / (t / steps), 4),
