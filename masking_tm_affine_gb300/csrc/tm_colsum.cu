@@ -554,6 +554,10 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
     const int n = t1 > t0 ? (int)(t1 - t0) : 0;
 
     __shared__ Inbox<TN, CS> inbox;
+    // the tiles are read once: evict-first, so that loading them does not
+    // push out (and force the write-back of) lines an earlier kernel left
+    // dirty in L2 ([8192, 8192] after a 512 MiB write: 49.8 against 58.0 us)
+    const uint64_t pol = tid == 0 ? l2_evict_first_policy() : 0;
     if (tid == 0) {
         abort_flag = 0;
         for (int st = 0; st < stages; ++st)
@@ -570,9 +574,9 @@ __global__ void __launch_bounds__(kThreads) colsum_staged(const __grid_constant_
                      "r"((uint32_t)(tile * sizeof(float)))
                      : "memory");
         asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(tiles + (size_t)st * tile)),
-            "l"(&tmap), "r"((int)(strip * TN)), "r"((int)((t0 + k) * TM)), "r"(bar)
+            "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+            " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(tiles + (size_t)st * tile)),
+            "l"(&tmap), "r"((int)(strip * TN)), "r"((int)((t0 + k) * TM)), "r"(bar), "l"(pol)
             : "memory");
     };
     if (tid == 0)

@@ -148,6 +148,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// An L2 cache policy that marks lines evict-first: for data read once (a TMA
+// copy of a streamed tile), so that it, and not older lines still to be
+// written back, is what L2 gives up first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // ---------------------------------------------------------------- clusters
 // Rank of this CTA in its cluster, the address of a shared variable in CTA
 // `rank` of the cluster (distributed shared memory), and a full cluster
