@@ -1319,7 +1319,7 @@ def run_cases(args):
                 nbytes = 4 * Mw * Nw + 8 * Mw
                 fm = {"neg_inf": (tm.TM_FILL_NEG_INF, 0), "zero": (tm.TM_FILL_ZERO, 0),
                       "scalar": (tm.TM_FILL_NEG_INF, tm.TM_PATH_SCALAR)}
-                SB_, SC_ = tile or (16 if Nw < 4096 else 4, w.get("BC", 64))
+                SB_, SC_ = tile or (16 if Nw < 4096 else 8, w.get("BC", 64))  # wide rows: a warp per row
                 mk = lambda v: (lambda: tm.tm_softmax_rowstats(X, Nw, Mw, Nw, O, O2, SB_, SC_, fm[v][0], fm[v][1], s))
             else:
                 O = torch.empty(Mw, dtype=torch.float32, device=dev)

@@ -63,15 +63,18 @@ __device__ __forceinline__ void absorb(float &m, float &l, const float (&v)[K])
     m = mn;
 }
 
+// Four blocks per SM, each lane holding 8 vector loads (32 values) in flight
+// per batch: at [8192, 8192] 44.5 against 48.1 us with 4 (16 values) and no
+// bound; a batch still takes one exponential per value plus one.
 template <int BR, bool VEC, bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) softmax_rowstats_kernel(const float *__restrict__ S, int64_t lds,
+__global__ void __launch_bounds__(kThreads, 4) softmax_rowstats_kernel(const float *__restrict__ S, int64_t lds,
                                                                     int64_t M, int64_t N, float *__restrict__ m_out,
                                                                     float *__restrict__ l_out, int BC, int fill_zero,
                                                                     unsigned *status)
 {
     constexpr int L = kThreads / BR;   // lanes sharing a row
     constexpr int EW = VEC ? 4 : 1;
-    constexpr int U = VEC ? 4 : 16;    // accesses in flight per lane (16 values per batch: fewer registers)
+    constexpr int U = VEC ? 8 : 16;    // accesses in flight per lane (32 vector values or 16 scalars per batch)
     constexpr int W = L > 32 ? L / 32 : 1;
     constexpr int kPre = 1;  // remainder-tile vectors a lane loads up front
     __shared__ float part_m[BR][W], part_l[BR][W];
